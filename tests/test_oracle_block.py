@@ -1,0 +1,49 @@
+"""Pins of the synthetic block pieces (LayerNorm vs torch) and properties of
+the small stack that follow from the method's rules."""
+import numpy as np
+import torch
+
+import synthetic
+from oracle import block, codecs
+
+
+def test_layernorm_vs_torch():
+    rng = np.random.default_rng(0)
+    x = codecs.f32_to_bf16(rng.standard_normal((17, 96)).astype(np.float32) * 3 + 1)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(codecs.bf16_to_f32(x).astype(np.float64)), (96,), eps=1e-5)
+    assert np.array_equal(block.layernorm(x), codecs.f64_to_bf16(ref.numpy()))
+
+
+def _tiny_stack(steps=5, nb=3, M=40, H=64, F=128, seed=7):
+    st = synthetic.stack_setup(seed, nb, H, F)
+    wq = [{k: block.quantize_weights(v) for k, v in b.items()} for b in st["blocks"]]
+    xs = synthetic.stack_inputs(st["noise_seed"], M, H, steps)
+    return st, wq, xs
+
+
+def test_stack_tdc_off_equals_zero_threshold():
+    st, wq, xs = _tiny_stack()
+    a = block.run_stack(xs, wq, st["alpha"], st["beta"], 0.05, 0.0, 1, use_tdc=True)
+    b = block.run_stack(xs, wq, st["alpha"], st["beta"], 0.05, 0.05, 1, use_tdc=False)
+    for x, y in zip(a["outputs"], b["outputs"]):
+        assert np.array_equal(x, y)
+    assert not np.any(a["skips"])
+
+
+def test_stack_flags_follow_gamma_and_uniform_extremes():
+    st, wq, xs = _tiny_stack(steps=3)
+    r = block.run_stack(xs, wq, st["alpha"], st["beta"], np.inf, 0.0, 1)
+    assert not r["flags"][0].any() and all(f.all() for f in r["flags"][1:])
+    forced = [np.ones(12, np.uint8)] * 3
+    forced[0] = np.zeros(12, np.uint8)
+    r2 = block.run_stack(xs, wq, st["alpha"], st["beta"], 0.0, 0.0, 1, forced_flags=forced)
+    for x, y in zip(r["outputs"], r2["outputs"]):
+        assert np.array_equal(x, y)
+
+
+def test_stack_skip_reuses_delta():
+    st, wq, xs = _tiny_stack(steps=6)
+    r = block.run_stack(xs, wq, st["alpha"], st["beta"], 0.05, 10.0, 1)   # huge tau_tdc: skip when allowed
+    skips = np.array(r["skips"])
+    assert not skips[:2].any()                     # need two fresh updates first
+    assert skips[2].all() and not skips[3].any() and skips[4].all()   # max_skip = 1 alternates

@@ -1,0 +1,119 @@
+"""Pins of Gamma / Delta / r2, the DMPQ assignment and the TDC state machine."""
+import numpy as np
+
+from oracle import codecs, dmpq, gamma, tdc
+from oracle.codecs import f32_to_bf16
+
+
+def _bits(x):
+    return f32_to_bf16(np.asarray(x, np.float32))
+
+
+def test_gamma_closed_forms():
+    rng = np.random.default_rng(0)
+    x = _bits(rng.standard_normal((7, 33)))
+    assert gamma.gamma(x, x) == 0.0
+    x2 = _bits(2 * codecs.bf16_to_f32(x))
+    assert gamma.gamma(x, x2) == 1.0                      # power-of-two scaling is exact
+    c = _bits(np.full((4, 10), 0.5))
+    c3 = _bits(np.full((4, 10), 2.0))
+    assert gamma.gamma(c, c3) == np.float32(3.0)           # |2 - 0.5| / 0.5
+    z = _bits(np.zeros((3, 3)))
+    assert gamma.gamma(z, c[:3, :3]) == 0.0                # ||in|| = 0 -> 0 by definition
+
+
+def test_delta_and_r2_closed_forms():
+    rng = np.random.default_rng(1)
+    xin = _bits(rng.standard_normal((5, 16)))
+    d = _bits(rng.standard_normal((5, 16)) * 0.1)
+    xout = _bits(codecs.bf16_to_f32(xin) + codecs.bf16_to_f32(d))
+    dn = gamma.delta(xin, xout)
+    assert gamma.rel_l2_sq(dn, dn) == 0.0
+    d2 = _bits(2 * codecs.bf16_to_f32(dn))
+    assert gamma.rel_l2_sq(d2, dn) == 1.0                  # ||2D - D|| / ||D|| = 1
+    assert gamma.rel_l2_sq(dn, _bits(np.zeros((5, 16)))) == np.inf
+    assert abs(gamma.cosine(d2, dn) - 1.0) < 1e-12
+    assert abs(gamma.cosine(_bits(-codecs.bf16_to_f32(dn)), dn) + 1.0) < 1e-12
+
+
+def test_delta_is_f32_difference_rounded_to_bf16():
+    xin = _bits([[1.0, 3.0, -2.0]])
+    xout = _bits([[1.5, 3.015625, 2.0]])
+    assert codecs.bf16_to_f32(gamma.delta(xin, xout)).tolist() == [[0.5, 0.015625, 4.0]]
+
+
+def test_block_pass_contract():
+    rng = np.random.default_rng(2)
+    xin = _bits(rng.standard_normal((3, 8)))
+    xout = _bits(rng.standard_normal((3, 8)))
+    g, dn, r2 = gamma.block_pass(xin, xout, None, computed=True)
+    assert dn is not None and r2 is None
+    g2, dn2, r22 = gamma.block_pass(xin, xout, dn, computed=True)
+    assert g2 == g and r22 == 0.0
+    g3, dn3, r23 = gamma.block_pass(xin, xout, dn, computed=False)
+    assert g3 == g and dn3 is None and r23 is None
+
+
+def test_dmpq_extremes_reproduce_uniform_policies():
+    rng = np.random.default_rng(3)
+    G = rng.uniform(0, 0.5, 6).astype(np.float32)
+    alpha = rng.uniform(0.5, 1.5, 24).astype(np.float32)
+    beta = rng.uniform(0, 0.01, 24).astype(np.float32)
+    lb = np.repeat(np.arange(6), 4)
+    assert dmpq.assign(G, alpha, beta, lb, np.inf, 3).all()             # uniform W4A4
+    assert not dmpq.assign(G, alpha, beta, lb, -np.inf, 3).any()        # uniform W4A8
+    assert not dmpq.assign(G, alpha, beta, lb, np.inf, 0).any()         # step 0 -> INT8
+    f = dmpq.assign(G, np.zeros(24, np.float32), beta, lb, np.float32(0.005), 2)
+    assert np.array_equal(f, (beta < np.float32(0.005)).astype(np.uint8))
+
+
+def test_dmpq_tie_goes_to_int8_and_layer_block_map():
+    G = np.array([0.25, 0.5], np.float32)
+    alpha = np.array([1.0, 1.0, 2.0], np.float32)
+    beta = np.array([0.0, 0.25, 0.0], np.float32)
+    lb = np.array([0, 0, 1])
+    p = dmpq.predict(G, alpha, beta, lb)
+    assert p.tolist() == [0.25, 0.5, 1.0]
+    assert dmpq.assign(G, alpha, beta, lb, 0.5, 1).tolist() == [1, 0, 0]
+
+
+def test_dmpq_calibration_fraction():
+    p = np.arange(1000, dtype=np.float32)
+    tau = dmpq.calibrate_tau(p, 0.6)
+    assert abs(np.mean(p < tau) - 0.6) < 0.002
+
+
+def test_tdc_state_machine_hand_sequence():
+    # r2 values as produced by consecutive computed steps; tau 0.05 -> tau^2 = 0.0025
+    c = tdc.BlockCache()
+    seq = []
+    r2_next = [None, 0.001, 0.001, 0.01, 0.0001, 0.0001]
+    i = 0
+    for step in range(8):
+        if tdc.decide(c, 0.05, 1):
+            tdc.after_skip(c)
+            seq.append("S")
+        else:
+            tdc.after_compute(c, np.zeros(1, np.uint16), r2_next[i])
+            i += 1
+            seq.append("C")
+    # C (first delta) C (r2 .001, 2 fresh) S C (r2 .001, consec reset) S C (r2 .01) C (r2 1e-4) S
+    assert "".join(seq) == "CCSCSCCS"
+
+
+def test_tdc_never_skips_with_zero_threshold_or_zero_max_skip():
+    c = tdc.BlockCache(fresh_count=5, consec=0, r2=np.float32(0.0), delta=None)
+    assert not tdc.decide(c, 0.0, 1)                      # r2 < 0 is impossible
+    assert not tdc.decide(c, 1.0, 0)
+    assert tdc.decide(c, 1.0, 1)
+
+
+def test_tdc_apply_identity():
+    rng = np.random.default_rng(4)
+    xin = _bits(rng.standard_normal((6, 40)))
+    d = _bits(rng.standard_normal((6, 40)) * 0.05)
+    out = tdc.apply(xin, d)
+    back = codecs.bf16_to_f32(out).astype(np.float64) - codecs.bf16_to_f32(xin)
+    ulp = np.abs(codecs.bf16_to_f32(out)).astype(np.float64) * 2.0 ** -8
+    assert (np.abs(back - codecs.bf16_to_f32(d)) <= ulp + 1e-30).all()
+    assert np.array_equal(tdc.apply(xin, _bits(np.zeros((6, 40)))), xin)

@@ -1,0 +1,194 @@
+/*
+ * sixbit.h -- C ABI of the GB300 (sm_103a) hot path of 6Bit-Diffusion:
+ * inference-time NVFP4/INT8 mixed-precision quantized linear layers for
+ * video diffusion transformers, with the DMPQ precision predictor and the
+ * Temporal Delta Cache (TDC).
+ *
+ * Method source: "6Bit-Diffusion: Inference-Time Mixed-Precision
+ * Quantization for Video Diffusion Models" (arXiv 2603.18742) --
+ * mlsanity.com page, "Abstract"; thelatestinai.com page, Figures 1-4 and
+ * Tables 2-3.  Each entry point names the passage that defines it.
+ *
+ * Conventions for every call:
+ *  - Pointers are DEVICE pointers owned by the caller unless stated.  The
+ *    library never allocates or frees device memory; scratch ("ws") is
+ *    caller memory of sixbit_workspace_size() bytes.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and never synchronizes the host, except
+ *    sixbit_get_error().
+ *  - bf16 tensors are raw 16-bit bf16 bit patterns, row-major; `ld*` is the
+ *    row stride in elements.  Sizes are element counts.
+ *  - `pred` (nullable) is a device byte: the launched kernels exit at once
+ *    when *pred == 0.  This is how on-device DMPQ/TDC decisions gate work
+ *    without a host round trip.
+ *  - Return value: SIXBIT_OK, or a negative code for an argument the host
+ *    can check (nothing is launched then), or SIXBIT_ELAUNCH when CUDA
+ *    rejected a launch.  Device-side failures (a bounded wait that gave up)
+ *    set a device error word read by sixbit_get_error().
+ */
+#ifndef SIXBIT_H
+#define SIXBIT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* sixbit_stream_t;   /* same object as cudaStream_t */
+
+enum {
+  SIXBIT_OK = 0,
+  SIXBIT_EINVAL = -1,   /* null pointer where one is required, bad enum, negative size */
+  SIXBIT_ESHAPE = -2,   /* unsupported shape, e.g. K % 64 != 0 for NVFP4 operands */
+  SIXBIT_EALIGN = -3,   /* pointer or stride not 16-byte aligned where TMA/vector loads need it */
+  SIXBIT_ELAUNCH = -4,  /* CUDA launch or driver error */
+  SIXBIT_EDEVICE = -5   /* returned by sixbit_get_error(): a device wait gave up */
+};
+
+enum { SIXBIT_F32 = 0, SIXBIT_BF16 = 1 };          /* dtype / out_dtype */
+enum { SIXBIT_EPI_GELU = 1 };                       /* epilogue flag bits */
+
+/* Library version string (static storage). */
+const char* sixbit_version(void);
+
+/* Bytes of the swizzled E4M3 scale-factor buffer of an NVFP4 operand with
+ * `rows` rows and reduction length K: rows padded to 128, K/16 scale columns
+ * padded to 4.  Byte of (row m, scale column c) sits at
+ *   ((m/128)*(Kc4/4) + c/4)*512 + (m%32)*16 + ((m%128)/32)*4 + c%4
+ * (the 128x4 atom layout the block-scaled tensor-core MMA reads). */
+size_t sixbit_sf_bytes(int64_t rows, int64_t K);
+
+/* Scratch bytes for sixbit_quantize_act_nvfp4(amax_in = NULL),
+ * sixbit_quantize_weight_nvfp4 and sixbit_block_gamma over n = M*K elements.
+ * The buffer must be zero-filled once before its first use; every call
+ * leaves it ready for the next (calls sharing one buffer must not overlap). */
+size_t sixbit_workspace_size(int64_t M, int64_t K);
+
+/* a1 -- absolute maxima of a bf16 tensor [M, K] (row stride ldx).
+ * amax_out (nullable): max |x| over the tensor (the NVFP4 tensor amax);
+ * row_amax_out (nullable): max |x| per row, [M] (the per-token INT8 amax).
+ * Source: NVFP4/INT8 activation quantization on the fly ("Abstract",
+ * mlsanity.com page).  At least one output must be given. */
+int sixbit_amax_bf16(const void* x, int64_t M, int64_t K, int64_t ldx,
+                     float* amax_out, float* row_amax_out, sixbit_stream_t stream);
+
+/* a2 -- NVFP4 activation quantization ("Abstract": NVFP4 for temporally
+ * stable layers).  x bf16 [M, K], K % 64 == 0, ldx % 8 == 0.
+ *   g = amax/2688 (1 if amax = 0); per 16-block S = E4M3(amax_b*448/amax);
+ *   codes = E2M1(x * (1/(S*g))) (RNE, satfinite), +0 codes when S*g = 0.
+ * amax_in (nullable): tensor amax from the producer; when NULL the call
+ *   runs its own amax pass into `ws` (then ws must be non-NULL).
+ * codes: [M, K/2] bytes, element 2j in the low nibble.
+ * sf: sixbit_sf_bytes(M, K) bytes, swizzled; pad rows are written as 0.
+ * g_out: [1] float, the dequantization tensor scale. */
+int sixbit_quantize_act_nvfp4(const void* x, int64_t M, int64_t K, int64_t ldx,
+                              const float* amax_in, uint8_t* codes, uint8_t* sf, float* g_out,
+                              const uint8_t* pred, void* ws, sixbit_stream_t stream);
+
+/* a4 -- NVFP4 weight quantization, offline, same rules as a2 on W [N, K]
+ * (out x in, K contiguous).  dtype SIXBIT_F32 or SIXBIT_BF16.  Uses ws for
+ * the tensor amax.  Source: "W4" weights of Table 2 / Table 3. */
+int sixbit_quantize_weight_nvfp4(const void* w, int dtype, int64_t N, int64_t K,
+                                 uint8_t* codes, uint8_t* sf, float* g_out,
+                                 void* ws, sixbit_stream_t stream);
+
+/* a3 -- per-token symmetric INT8 activation quantization ("Abstract": INT8
+ * for volatile layers).  x bf16 [M, K], K % 64 == 0, K <= 16384.
+ *   inv = 127/amax_m; q = clamp(rne(x*inv), -127, 127); s_m = amax_m/127;
+ *   a zero row gives q = 0, s_m = 0.
+ * row_amax_in (nullable): per-row amax from the producer.
+ * q (nullable): int8 [M, K].
+ * planes (nullable): the GEMM operand form of q, three E2M1 digit planes
+ *   [3][M][K/2] bytes with q = 64*a + 8*b + c (plane 0 = a, 1 = b, 2 = c;
+ *   each digit an integer in [-4, 4]); exact, no rounding.
+ * row_scale: [M] float s_m.  At least one of q / planes must be given. */
+int sixbit_quantize_act_int8(const void* x, int64_t M, int64_t K, int64_t ldx,
+                             const float* row_amax_in, int8_t* q, uint8_t* planes,
+                             float* row_scale, const uint8_t* pred, sixbit_stream_t stream);
+
+/* a5 -- W4A4 linear: y = g_a g_w sum_k (E2M1*S)_a (E2M1*S)_w + bias,
+ * optional tanh-GELU, optional + residual; fp32 accumulation on tcgen05
+ * block-scaled FP4 tensor cores.  Source: uniform W4A4 of Table 3, NVFP4
+ * layers of the "Abstract".
+ * A: codes [M, K/2], sf swizzled for M rows, g_a [1].  W: codes [N, K/2],
+ * sf swizzled for N rows, g_w [1].  K % 64 == 0, N % 16 == 0.
+ * bias (nullable) bf16 [N]; residual (nullable) bf16 [M, N] stride ldr;
+ * epi: SIXBIT_EPI_GELU bit; out_dtype SIXBIT_F32 / SIXBIT_BF16;
+ * y [M, N] stride ldy (ldy*elt % 16 == 0). */
+int sixbit_qlinear_w4a4(const uint8_t* a_codes, const uint8_t* a_sf, const float* g_a,
+                        int64_t M, int64_t K,
+                        const uint8_t* w_codes, const uint8_t* w_sf, const float* g_w, int64_t N,
+                        const void* bias, const void* residual, int64_t ldr, int epi,
+                        int out_dtype, void* y, int64_t ldy,
+                        const uint8_t* pred, sixbit_stream_t stream);
+
+/* a6 -- W4A8 linear: y = s_a[m] g_w sum_k q (E2M1*S)_w + same epilogue.
+ * Source: uniform W4A8 of Table 3, INT8 layers of the "Abstract".
+ * The INT8 activations come as the digit planes of sixbit_quantize_act_int8
+ * ([3][M][K/2]) plus row_scale [M]; the products q*w are exact and
+ * accumulate in fp32 on the FP4 tensor cores (three digit MMAs per K step).
+ * Weights, epilogue and constraints as sixbit_qlinear_w4a4. */
+int sixbit_qlinear_w4a8(const uint8_t* a_planes, const float* row_scale, int64_t M, int64_t K,
+                        const uint8_t* w_codes, const uint8_t* w_sf, const float* g_w, int64_t N,
+                        const void* bias, const void* residual, int64_t ldr, int epi,
+                        int out_dtype, void* y, int64_t ldy,
+                        const uint8_t* pred, sixbit_stream_t stream);
+
+/* a7 -- one pass over a block's input/output (Figure 2: Gamma; Figure 4:
+ * update Delta and its relative L2 change).  in, out: bf16 [n] (whole block
+ * tensor).  Always: gamma_out[0] = ||out-in||_1/||in||_1 (0 if ||in|| = 0).
+ * computed (nullable; NULL = computed): the TDC byte of this step, 1 if
+ * the block ran, 0 if TDC skipped it.  When computed and delta != NULL:
+ * delta (bf16 [n], in: previous update, out: bf16(f32(out)-f32(in))) is
+ * replaced in place, and if tdc_state[0] >= 1 (or tdc_state is NULL and
+ * r2_out is given) the relative change
+ * r2_out[0] = ||D_new-D_old||^2/||D_old||^2 (+inf if ||D_old|| = 0) is
+ * written.  tdc_state (nullable) int32[2] = {fresh_count, consec}:
+ * computed -> {fresh+1, 0}; skipped -> {fresh, consec+1}.
+ * Deterministic: fixed 16384-element tiles, fp32 inside a tile, fp64
+ * across tiles.  ws: sixbit_workspace_size(n, 1) bytes. */
+int sixbit_block_gamma(const void* in, const void* out, int64_t n, void* delta,
+                       float* gamma_out, float* r2_out, int32_t* tdc_state,
+                       const uint8_t* computed, void* ws, sixbit_stream_t stream);
+
+/* a8 -- DMPQ assignment (Figure 3: per-layer line E_rel = alpha*Gamma_{t-1}
+ * + beta; "Abstract": NVFP4 for stable layers).  For each layer l:
+ *   p = f32(f32(alpha[l]*gamma[layer_block[l]]) + beta[l]);
+ *   use_nvfp4[l] = (*step > 0) && (p < tau)      (tie -> INT8)
+ * gates (nullable) uint8 [n_layers][2] = {use_nvfp4, !use_nvfp4}: the
+ * `pred` bytes of the layer's NVFP4 and INT8 kernels.  step: device int32. */
+int sixbit_dmpq_assign(const float* gamma, const float* alpha, const float* beta,
+                       const int32_t* layer_block, int32_t n_layers, float tau,
+                       const int32_t* step, uint8_t* use_nvfp4, uint8_t* gates,
+                       sixbit_stream_t stream);
+
+/* a9 -- TDC decision and reuse (Figure 2: skip from the updates of the two
+ * preceding steps; "Abstract": skip invariant blocks).
+ *   skip = tdc_state[0] >= 2 && r2[0] < f32(tau_tdc^2) && tdc_state[1] < max_skip
+ * compute_out[0] = !skip.  If skip: out = bf16(f32(in) + f32(delta)) over n
+ * elements and gates[0..n_gates) are cleared (so the block's kernels exit).
+ * The counters are advanced by sixbit_block_gamma, not here. */
+int sixbit_tdc_decide_and_apply(const void* in, const void* delta, int64_t n, const float* r2,
+                                float tau_tdc, int32_t max_skip, const int32_t* tdc_state,
+                                uint8_t* compute_out, void* out, uint8_t* gates, int32_t n_gates,
+                                sixbit_stream_t stream);
+
+/* Block harness: LayerNorm without affine over rows of H, eps given,
+ * fp32 statistics, bf16 out.  Optional side outputs for the next quantizer:
+ * amax_out (tensor max |y|, zeroed by the call) and row_amax_out [M]. */
+int sixbit_layernorm_bf16(const void* x, int64_t M, int64_t H, int64_t ldx, float eps,
+                          void* y, int64_t ldy, float* amax_out, float* row_amax_out,
+                          const uint8_t* pred, sixbit_stream_t stream);
+
+/* Synchronizes `stream`, returns SIXBIT_EDEVICE if a device wait gave up
+ * since the last call (and clears the word), else the stream's CUDA status
+ * mapped to SIXBIT_OK / SIXBIT_ELAUNCH. */
+int sixbit_get_error(sixbit_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SIXBIT_H */

@@ -1,0 +1,302 @@
+// Block-level kernels: Gamma/Delta/r2 pass (a7), DMPQ assignment (a8),
+// TDC decision and reuse (a9), and the LayerNorm of the block harness.
+//
+// Method: 6Bit-Diffusion, thelatestinai.com page -- Figure 2 (Gamma = block
+// relative L1 input/output distance at the preceding step drives DMPQ; TDC
+// decides from the updates of the two preceding steps), Figure 3 (per-layer
+// line alpha*Gamma + beta), Figure 4 (updates compared by relative L2).
+// Decisions are computed and consumed on the device: no host round trip.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sixbit {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTile = 16384;                  // elements per CTA of the Gamma pass
+constexpr int kVecPerThread = kTile / (8 * kThreads);   // 8 x 16-byte vectors
+
+struct GammaWs {                              // layout of the scratch buffer
+  unsigned int counter;                       // CTAs finished (reset by the last one)
+  unsigned int pad[3];
+};
+
+// Fixed-order block reduction of 4 floats: warp xor tree, then warps 0..7 in order.
+__device__ __forceinline__ void block_sum4(float v[4], float (*sm)[4]) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = warp_sum(v[i]);
+  if (lane == 0)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sm[w][i] = v[i];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 4; ++i) {
+      float acc = 0.f;
+      for (int k = 0; k < kThreads / 32; ++k) acc += sm[k][i];
+      v[i] = acc;
+    }
+  }
+}
+
+// a7: one pass over (in, out, previous Delta).  Per element:
+//   d = f32(out) - f32(in); S1 += |d|; S0 += |in|;
+//   if computed: D_new = bf16(d) (stored over D_old); if r2 wanted:
+//   e = f32(D_new) - f32(D_old); Sd += e*e; So += D_old^2.
+// CTA partials go to scratch as float64; the last CTA sums them in tile
+// order, writes Gamma / r2 and advances the TDC counters.
+__global__ void __launch_bounds__(kThreads) gamma_kernel(const uint16_t* __restrict__ xin, const uint16_t* __restrict__ xout,
+                                                         int64_t n, uint16_t* delta, float* gamma_out, float* r2_out,
+                                                         int32_t* tdc_state, const uint8_t* computed_ptr,
+                                                         GammaWs* ws, double* partials) {
+  __shared__ float sm[kThreads / 32][4];
+  __shared__ bool is_last;
+  const bool computed = computed_ptr ? (*computed_ptr != 0) : true;
+  const bool do_delta = computed && delta != nullptr;
+  const bool do_r2 = do_delta && r2_out != nullptr && (tdc_state ? tdc_state[0] >= 1 : true);
+  const int64_t base = int64_t(blockIdx.x) * kTile;
+  float s1 = 0.f, s0 = 0.f, sd = 0.f, so = 0.f;
+  uint4 vi[kVecPerThread], vo[kVecPerThread], vd[kVecPerThread];
+#pragma unroll
+  for (int i = 0; i < kVecPerThread; ++i) {
+    const int64_t idx = base + (int64_t(i) * kThreads + threadIdx.x) * 8;
+    if (idx + 8 <= n) {
+      vi[i] = ldg_nc_v4(xin + idx);
+      vo[i] = ldg_nc_v4(xout + idx);
+      if (do_r2) vd[i] = ldg_v4(delta + idx);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kVecPerThread; ++i) {
+    const int64_t idx = base + (int64_t(i) * kThreads + threadIdx.x) * 8;
+    if (idx >= n) continue;
+    float fi[8], fo[8], fd[8];
+    int cnt = 8;
+    if (idx + 8 <= n) {
+      const uint32_t* a = &vi[i].x;
+      const uint32_t* b = &vo[i].x;
+      const uint32_t* c = &vd[i].x;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        fi[2 * e] = bf16lo(a[e]); fi[2 * e + 1] = bf16hi(a[e]);
+        fo[2 * e] = bf16lo(b[e]); fo[2 * e + 1] = bf16hi(b[e]);
+        if (do_r2) { fd[2 * e] = bf16lo(c[e]); fd[2 * e + 1] = bf16hi(c[e]); }
+      }
+    } else {                                  // ragged tail (scalar)
+      cnt = int(n - idx);
+      for (int e = 0; e < 8; ++e) {
+        fi[e] = e < cnt ? bf16_to_f32(xin[idx + e]) : 0.f;
+        fo[e] = e < cnt ? bf16_to_f32(xout[idx + e]) : 0.f;
+        fd[e] = (e < cnt && do_r2) ? bf16_to_f32(delta[idx + e]) : 0.f;
+      }
+    }
+    uint16_t dn[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float d = __fsub_rn(fo[e], fi[e]);
+      s1 += fabsf(d);
+      s0 += fabsf(fi[e]);
+      dn[e] = f32_to_bf16(d);
+      if (do_r2) {
+        const float ee = __fsub_rn(bf16_to_f32(dn[e]), fd[e]);
+        sd = __fmaf_rn(ee, ee, sd);
+        so = __fmaf_rn(fd[e], fd[e], so);
+      }
+    }
+    if (do_delta) {
+      if (cnt == 8) {
+        uint4 w;
+        w.x = dn[0] | (uint32_t(dn[1]) << 16); w.y = dn[2] | (uint32_t(dn[3]) << 16);
+        w.z = dn[4] | (uint32_t(dn[5]) << 16); w.w = dn[6] | (uint32_t(dn[7]) << 16);
+        *reinterpret_cast<uint4*>(delta + idx) = w;
+      } else {
+        for (int e = 0; e < cnt; ++e) delta[idx + e] = dn[e];
+      }
+    }
+  }
+  float v[4] = {s1, s0, sd, so};
+  block_sum4(v, sm);
+  if (threadIdx.x == 0) {
+    double* p = partials + 4 * int64_t(blockIdx.x);
+    p[0] = v[0]; p[1] = v[1]; p[2] = v[2]; p[3] = v[3];
+    __threadfence();
+    const unsigned int ticket = atomicAdd(&ws->counter, 1u);
+    is_last = (ticket == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  // Last CTA: float64 sum of the partials, thread t over tiles t, t+256, ...
+  // then a fixed tree.
+  __shared__ double dsm[kThreads][4];
+  double acc[4] = {0, 0, 0, 0};
+  for (int64_t t = threadIdx.x; t < gridDim.x; t += kThreads) {
+    const volatile double* p = partials + 4 * t;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] += p[i];
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dsm[threadIdx.x][i] = acc[i];
+  __syncthreads();
+  for (int h = kThreads / 2; h > 0; h >>= 1) {
+    if (threadIdx.x < h)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dsm[threadIdx.x][i] += dsm[threadIdx.x + h][i];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double S1 = dsm[0][0], S0 = dsm[0][1], Sd = dsm[0][2], So = dsm[0][3];
+    if (gamma_out) *gamma_out = (S0 == 0.0) ? 0.f : float(S1 / S0);
+    if (do_r2) *r2_out = (So == 0.0) ? __int_as_float(0x7f800000) : float(Sd / So);
+    if (tdc_state) {
+      if (computed) { tdc_state[0] += 1; tdc_state[1] = 0; }
+      else tdc_state[1] += 1;
+    }
+    ws->counter = 0u;
+  }
+}
+
+// a8: p = f32(f32(alpha*Gamma) + beta); NVFP4 iff step > 0 and p < tau.
+__global__ void dmpq_kernel(const float* __restrict__ gamma, const float* __restrict__ alpha,
+                            const float* __restrict__ beta, const int32_t* __restrict__ layer_block,
+                            int32_t n_layers, float tau, const int32_t* step, uint8_t* use_nvfp4, uint8_t* gates) {
+  const int l = blockIdx.x * blockDim.x + threadIdx.x;
+  if (l >= n_layers) return;
+  const float p = __fadd_rn(__fmul_rn(alpha[l], gamma[layer_block[l]]), beta[l]);
+  const uint8_t f = (*step > 0 && p < tau) ? 1 : 0;
+  if (use_nvfp4) use_nvfp4[l] = f;
+  if (gates) { gates[2 * l] = f; gates[2 * l + 1] = 1 - f; }
+}
+
+// a9: every CTA evaluates the (read-only) decision; CTA 0 publishes it; on a
+// skip all CTAs write out = bf16(f32(in) + f32(delta)).
+__global__ void __launch_bounds__(kThreads) tdc_kernel(const uint16_t* __restrict__ xin, const uint16_t* __restrict__ delta,
+                                                       int64_t n, const float* r2, float tau2, int32_t max_skip,
+                                                       const int32_t* tdc_state, uint8_t* compute_out,
+                                                       uint16_t* __restrict__ out, uint8_t* gates, int32_t n_gates) {
+  const bool skip = tdc_state[0] >= 2 && *r2 < tau2 && tdc_state[1] < max_skip;
+  if (blockIdx.x == 0) {
+    if (threadIdx.x == 0) *compute_out = skip ? 0 : 1;
+    if (skip && gates)
+      for (int i = threadIdx.x; i < n_gates; i += blockDim.x) gates[i] = 0;
+  }
+  if (!skip) return;
+  const int64_t nvec = n / 8;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec; v += stride) {
+    const uint4 a = ldg_nc_v4(xin + v * 8), b = ldg_nc_v4(delta + v * 8);
+    const uint32_t* pa = &a.x;
+    const uint32_t* pb = &b.x;
+    uint4 w;
+    uint32_t* pw = &w.x;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      pw[e] = pack_bf16x2(__fadd_rn(bf16lo(pa[e]), bf16lo(pb[e])), __fadd_rn(bf16hi(pa[e]), bf16hi(pb[e])));
+    *reinterpret_cast<uint4*>(out + v * 8) = w;
+  }
+  if (blockIdx.x == 0)
+    for (int64_t i = nvec * 8 + threadIdx.x; i < n; i += blockDim.x)
+      out[i] = f32_to_bf16(__fadd_rn(bf16_to_f32(xin[i]), bf16_to_f32(delta[i])));
+}
+
+// LayerNorm without affine, one warp per row; float32 mean, then the
+// centered second moment; y = (x - mean) / sqrt(var + eps) rounded to bf16.
+__global__ void __launch_bounds__(kThreads) layernorm_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t H, int64_t ldx,
+                                                             float eps, uint16_t* __restrict__ y, int64_t ldy,
+                                                             float* amax_out, float* row_amax_out, const uint8_t* pred) {
+  if (pred && *pred == 0) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
+  const int64_t nvec = H / 8;
+  float tmax = 0.f;
+  for (int64_t m = warp; m < M; m += nwarps) {
+    const uint16_t* row = x + m * ldx;
+    float s = 0.f;
+    for (int64_t j = lane; j < nvec; j += 32) {
+      const uint4 v = ldg_v4(row + j * 8);
+      const uint32_t* p = &v.x;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s += bf16lo(p[e]) + bf16hi(p[e]);
+    }
+    const float mean = __fdiv_rn(warp_sum(s), float(H));
+    float q = 0.f;
+    for (int64_t j = lane; j < nvec; j += 32) {
+      const uint4 v = ldg_v4(row + j * 8);
+      const uint32_t* p = &v.x;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float a = bf16lo(p[e]) - mean, b = bf16hi(p[e]) - mean;
+        q += a * a + b * b;
+      }
+    }
+    const float var = __fdiv_rn(warp_sum(q), float(H));
+    const float rstd = __fdiv_rn(1.f, __fsqrt_rn(var + eps));
+    float rmax = 0.f;
+    for (int64_t j = lane; j < nvec; j += 32) {
+      const uint4 v = ldg_v4(row + j * 8);
+      const uint32_t* p = &v.x;
+      uint4 w;
+      uint32_t* pw = &w.x;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        pw[e] = pack_bf16x2((bf16lo(p[e]) - mean) * rstd, (bf16hi(p[e]) - mean) * rstd);
+        rmax = fmaxf(rmax, fmaxf(fabsf(bf16lo(pw[e])), fabsf(bf16hi(pw[e]))));
+      }
+      *reinterpret_cast<uint4*>(y + m * ldy + j * 8) = w;
+    }
+    rmax = warp_max(rmax);
+    if (row_amax_out && lane == 0) row_amax_out[m] = rmax;
+    tmax = fmaxf(tmax, rmax);
+  }
+  if (amax_out && lane == 0) atomic_max_nonneg(amax_out, tmax);
+}
+
+}  // namespace
+
+size_t gamma_ws_bytes(int64_t n) { return sizeof(GammaWs) + size_t(cdiv(n, kTile)) * 4 * sizeof(double) + 256; }
+
+int launch_block_gamma(const void* xin, const void* xout, int64_t n, void* delta, float* gamma_out, float* r2_out,
+                       int32_t* tdc_state, const uint8_t* computed, void* ws, cudaStream_t s) {
+  const int64_t tiles = cdiv(n, kTile);
+  GammaWs* w = static_cast<GammaWs*>(ws);
+  double* partials = reinterpret_cast<double*>(static_cast<char*>(ws) + 256);
+  gamma_kernel<<<unsigned(tiles), kThreads, 0, s>>>(static_cast<const uint16_t*>(xin), static_cast<const uint16_t*>(xout),
+                                                    n, static_cast<uint16_t*>(delta), gamma_out, r2_out, tdc_state,
+                                                    computed, w, partials);
+  return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
+}
+
+int launch_dmpq(const float* gamma, const float* alpha, const float* beta, const int32_t* layer_block,
+                int32_t n_layers, float tau, const int32_t* step, uint8_t* use_nvfp4, uint8_t* gates, cudaStream_t s) {
+  const int threads = 128;
+  dmpq_kernel<<<unsigned(cdiv(n_layers, threads)), threads, 0, s>>>(gamma, alpha, beta, layer_block, n_layers, tau,
+                                                                     step, use_nvfp4, gates);
+  return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
+}
+
+int launch_tdc(const void* xin, const void* delta, int64_t n, const float* r2, float tau2, int32_t max_skip,
+               const int32_t* tdc_state, uint8_t* compute_out, void* out, uint8_t* gates, int32_t n_gates,
+               int num_sms, cudaStream_t s) {
+  int64_t want = cdiv(n / 8 + 1, kThreads * 4);
+  int64_t cap = int64_t(num_sms) * 8;
+  const unsigned grid = unsigned(want < cap ? (want < 1 ? 1 : want) : cap);
+  tdc_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(xin), static_cast<const uint16_t*>(delta), n, r2,
+                                       tau2, max_skip, tdc_state, compute_out, static_cast<uint16_t*>(out), gates,
+                                       n_gates);
+  return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
+}
+
+int launch_layernorm(const void* x, int64_t M, int64_t H, int64_t ldx, float eps, void* y, int64_t ldy,
+                     float* amax_out, float* row_amax_out, const uint8_t* pred, int num_sms, cudaStream_t s) {
+  if (amax_out && cudaMemsetAsync(amax_out, 0, sizeof(float), s) != cudaSuccess) return kELaunch;
+  int64_t want = cdiv(M, kThreads / 32);
+  int64_t cap = int64_t(num_sms) * 8;
+  const unsigned grid = unsigned(want < cap ? (want < 1 ? 1 : want) : cap);
+  layernorm_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), M, H, ldx, eps,
+                                             static_cast<uint16_t*>(y), ldy, amax_out, row_amax_out, pred);
+  return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
+}
+
+}  // namespace sixbit

@@ -1,0 +1,494 @@
+// Block-scaled FP4 GEMM on the sm_103a tensor cores (tcgen05), with the
+// dequant / bias / GELU / residual epilogue fused.  Serves both linear
+// layer types of 6Bit-Diffusion ("Abstract", mlsanity.com page; uniform
+// W4A4 / W4A8 of Table 3, thelatestinai.com page):
+//
+//  mode 0, W4A4:  y = g_a g_w sum_k (E2M1 S)_a (E2M1 S)_w
+//  mode 1, W4A8:  y = s_a[m] g_w sum_k q (E2M1 S)_w, with the INT8 code q
+//                 given as three E2M1 digit planes, q = 64 a + 8 b + c.
+//                 Each K step issues one MMA per plane with a constant
+//                 E4M3 block scale (64, 8, 1) for A, so the tensor cores
+//                 form q * w exactly and accumulate in fp32.  (sm_103a has
+//                 no tcgen05 int8 kind, and its warp-level int8 MMA runs at
+//                 ~150 TOP/s, far below the FP4 pipe.)
+//
+// Structure: persistent, warp-specialized CTA of 6 warps over 128 x BN
+// output tiles, K in steps of 256 (128 bytes of codes per row):
+//   warp 0      TMA producer: A/B code tiles (128B swizzle) and the
+//               scale-factor atoms into a STAGES-deep shared-memory ring;
+//   warp 1      TMEM owner and MMA issuer: tcgen05.cp of the scale atoms
+//               into TMEM, tcgen05.mma kind::mxf4nvf4 scale_vec::4X into a
+//               double-buffered TMEM accumulator, tcgen05.commit to free
+//               stages and publish finished tiles;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane
+//               quarter per warp, one output row per thread), scale, bias,
+//               GELU, residual, store -- overlapping the next tile's MMAs.
+// Every mbarrier wait is bounded; on expiry the CTA records an error in the
+// device error word, drains its own copies and MMAs, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sixbit {
+namespace {
+
+constexpr int BM = 128;
+constexpr int kKB = 128;                 // bytes of packed codes per row per K step (256 elements)
+constexpr int kThreads = 192;
+constexpr uint32_t kSpinCap = 1u << 22;  // polls of a bounded mbarrier wait
+constexpr uint32_t kTmemCols = 512;
+
+template <int BN, int MODE, int STAGES>
+struct Cfg {
+  static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
+  static constexpr int kPlanes = MODE == 0 ? 1 : 3;
+  static constexpr int kRT = BN / 128;                     // 128-row scale tiles of W per N tile
+  static constexpr int kA = BM * kKB;                      // one A plane tile
+  static constexpr int kB = BN * kKB;
+  static constexpr int kSFA = MODE == 0 ? 2048 : 0;        // 4 atoms of 512 bytes
+  static constexpr int kSFB = 2048 * kRT;
+  static constexpr int offB = kPlanes * kA;
+  static constexpr int offSFA = offB + kB;
+  static constexpr int offSFB = offSFA + kSFA;
+  static constexpr int kStage = offSFB + kSFB;             // multiple of 1024
+  static constexpr uint32_t kTx = kStage;                  // bytes landed per stage
+  // TMEM columns
+  static constexpr int kSfStride = (MODE == 0 ? 16 : 0) + 16 * kRT;
+  static constexpr int kNAcc = (2 * BN + STAGES * kSfStride + 12 <= int(kTmemCols)) ? 2 : 1;
+  static constexpr int kSfBase = kNAcc * BN;
+  static constexpr int kConstCol = kSfBase + STAGES * kSfStride;
+  static_assert(kConstCol + 12 <= int(kTmemCols), "TMEM budget");
+  static constexpr int kExtra = 2048;                      // constant digit-scale atoms + barriers
+  static constexpr size_t kSmem = size_t(STAGES) * kStage + kExtra + 1024;
+};
+
+// ------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return uint32_t(__cvta_generic_to_shared(p)); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false when the cap expired or another role aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  for (uint32_t i = 0; i < kSpinCap; ++i) {
+    if (mbar_try(bar, parity)) return true;
+    if ((i & 255u) == 255u && abort_flag && *abort_flag) return false;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// 512-byte scale atom (32 rows x 16 bytes) -> 4 TMEM columns, replicated to
+// the four lane quarters; the MMA reads row r's scales from column r/32.
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tc_mma_fp4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                           uint32_t sfb, uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accum), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128
+// bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) | (uint64_t(1) << 46) |
+         (uint64_t(2) << 61);
+}
+// Descriptor of a 512-byte scale atom: 8-row core matrices of 16-byte rows, 128 bytes apart.
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
+  return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(128 >> 4) << 32) | (uint64_t(1) << 46);
+}
+// Instruction descriptor, kind::mxf4nvf4: A, B = E2M1, K-major, dense,
+// UE4M3 scales, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_fp4(int n) {
+  return (1u << 7) | (1u << 10) | (uint32_t(n >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ float gelu_tanh(float x) {
+  const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
+  return 0.5f * x * (1.f + tanhf(u));
+}
+
+struct Params {
+  int M, N, K, KT, MT, NT;
+  const float* g_a;
+  const float* row_scale;
+  const float* g_w;
+  const uint16_t* bias;
+  const uint16_t* residual;
+  int64_t ldr;
+  void* y;
+  int64_t ldy;
+  int out_bf16, gelu;
+  const uint8_t* pred;
+  int* err;
+};
+
+template <int BN, int MODE, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                    const Params p) {
+  using C = Cfg<BN, MODE, STAGES>;
+  if (p.pred && *p.pred == 0) return;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* extra = smem + size_t(STAGES) * C::kStage;
+  uint8_t* const_sfa = extra;                                    // 3 x 512 bytes (mode 1)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(extra + 1536);    // full[S] empty[S] tfull[2] tempty[2] drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * uint32_t(s); };
+  auto empty_bar = [&](int s) { return bar0 + 8u * uint32_t(STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * uint32_t(2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * uint32_t(2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * uint32_t(2 * STAGES + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(tfull_bar(a), 1); mbar_init(tempty_bar(a), 128); }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_tmap(&tmA); prefetch_tmap(&tmB); prefetch_tmap(&tmB);
+    if (MODE == 0) prefetch_tmap(&tmSFA);
+    prefetch_tmap(&tmSFB);
+  }
+  if (MODE == 1) {
+    // constant digit scales 64, 8, 1 as E4M3 bytes (0x68, 0x50, 0x38)
+    for (int i = threadIdx.x; i < 3 * 128; i += kThreads) {
+      const uint32_t b = i < 128 ? 0x68u : (i < 256 ? 0x50u : 0x38u);
+      reinterpret_cast<uint32_t*>(const_sfa)[i] = b * 0x01010101u;
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int ntiles = p.MT * p.NT;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    if (p.err) atomicExch(p.err, int(kErrWaitTimeout));
+  };
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, last_par = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      const int mt = tile / p.NT, nt = tile - mt * p.NT;
+      for (int kt = 0; kt < p.KT; ++kt) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { fail(); ok = false; break; }
+        uint8_t* sb = smem + size_t(stage) * C::kStage;
+        const uint32_t fb = full_bar(stage);
+        mbar_expect_tx(fb, C::kTx);
+        if (MODE == 0) {
+          tma_load_2d(smem_u32(sb), &tmA, kt * kKB, mt * BM, fb);
+          tma_load_3d(smem_u32(sb + C::offSFA), &tmSFA, 0, kt * 4, mt, fb);
+        } else {
+#pragma unroll
+          for (int pl = 0; pl < 3; ++pl) tma_load_3d(smem_u32(sb + pl * C::kA), &tmA, kt * kKB, mt * BM, pl, fb);
+        }
+        tma_load_2d(smem_u32(sb + C::offB), &tmB, kt * kKB, nt * BN, fb);
+        tma_load_3d(smem_u32(sb + C::offSFB), &tmSFB, 0, kt * 4, nt * C::kRT, fb);
+        issued |= 1u << stage;
+        last_par = (last_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok) {   // let the copies already issued land before the CTA exits
+      for (int s = 0; s < STAGES; ++s)
+        if (issued & (1u << s)) mbar_wait(full_bar(s), (last_par >> s) & 1u, nullptr);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_fp4(BN);
+    if (MODE == 1) {
+#pragma unroll
+      for (int pl = 0; pl < 3; ++pl) tc_cp_sf(tmem + C::kConstCol + 4 * pl, desc_sf(smem_u32(const_sfa + 512 * pl)));
+    }
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) { fail(); ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + uint32_t(acc * BN);
+      for (int kt = 0; kt < p.KT; ++kt) {
+        if (!mbar_wait(full_bar(stage), phase, abort_flag)) { fail(); ok = false; break; }
+        tc_fence_after();
+        uint8_t* sb = smem + size_t(stage) * C::kStage;
+        const uint32_t sfa_t = tmem + uint32_t(C::kSfBase + stage * C::kSfStride);
+        const uint32_t sfb_t = sfa_t + (MODE == 0 ? 16u : 0u);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (MODE == 0) tc_cp_sf(sfa_t + 4 * j, desc_sf(smem_u32(sb + C::offSFA + 512 * j)));
+#pragma unroll
+          for (int r = 0; r < C::kRT; ++r)
+            tc_cp_sf(sfb_t + 4 * (C::kRT * j + r), desc_sf(smem_u32(sb + C::offSFB + 512 * (4 * r + j))));
+        }
+        const uint64_t bdesc0 = desc_sw128(smem_u32(sb + C::offB));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint64_t bdesc = bdesc0 + uint64_t((32 * j) >> 4);
+          const uint32_t sfb = sfb_t + 4 * C::kRT * j;
+          if (MODE == 0) {
+            const uint64_t adesc = desc_sw128(smem_u32(sb)) + uint64_t((32 * j) >> 4);
+            tc_mma_fp4(d_tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb, (kt | j) != 0);
+          } else {
+#pragma unroll
+            for (int pl = 0; pl < 3; ++pl) {
+              const uint64_t adesc = desc_sw128(smem_u32(sb + pl * C::kA)) + uint64_t((32 * j) >> 4);
+              tc_mma_fp4(d_tmem, adesc, bdesc, idesc, tmem + C::kConstCol + 4 * pl, sfb, (kt | j | pl) != 0);
+            }
+          }
+        }
+        tc_commit(empty_bar(stage));
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      tc_commit(tfull_bar(acc));
+      if (C::kNAcc == 2) { acc ^= 1; if (acc == 0) acc_phase ^= 1u; }
+      else acc_phase ^= 1u;
+    }
+    // all MMAs issued by this thread complete before TMEM is released
+    tc_commit(drain_bar);
+    mbar_wait(drain_bar, 0, nullptr);
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                      // TMEM lane quarter of this warp
+    const int row = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const float gw = *p.g_w;
+    const float gscale = MODE == 0 ? __fmul_rn(*p.g_a, gw) : gw;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      const int mt = tile / p.NT, nt = tile - mt * p.NT;
+      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) { fail(); break; }
+      tc_fence_after();
+      const int m = mt * BM + row;
+      const bool row_ok = m < p.M;
+      const float scale = MODE == 0 ? gscale : (row_ok ? __fmul_rn(p.row_scale[m], gw) : 0.f);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(tmem + uint32_t(acc * BN + c * 32) + (uint32_t(q * 32) << 16), r);
+        tmem_ld_wait();
+        const int n0 = nt * BN + c * 32;
+        if (!row_ok || n0 >= p.N) continue;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(__uint_as_float(r[i]), scale);
+        const int cols = (p.N - n0) < 32 ? (p.N - n0) : 32;   // 16 or 32 (N % 16 == 0)
+        if (p.bias) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (8 * i >= cols) break;
+            const uint4 b = *reinterpret_cast<const uint4*>(p.bias + n0 + 8 * i);
+            const uint32_t* pb = &b.x;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              v[8 * i + 2 * e] = __fadd_rn(v[8 * i + 2 * e], bf16lo(pb[e]));
+              v[8 * i + 2 * e + 1] = __fadd_rn(v[8 * i + 2 * e + 1], bf16hi(pb[e]));
+            }
+          }
+        }
+        if (p.gelu) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+        }
+        if (p.residual) {
+          const uint16_t* rp = p.residual + int64_t(m) * p.ldr + n0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (8 * i >= cols) break;
+            const uint4 b = *reinterpret_cast<const uint4*>(rp + 8 * i);
+            const uint32_t* pb = &b.x;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              v[8 * i + 2 * e] = __fadd_rn(v[8 * i + 2 * e], bf16lo(pb[e]));
+              v[8 * i + 2 * e + 1] = __fadd_rn(v[8 * i + 2 * e + 1], bf16hi(pb[e]));
+            }
+          }
+        }
+        if (p.out_bf16) {
+          uint16_t* yp = static_cast<uint16_t*>(p.y) + int64_t(m) * p.ldy + n0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (8 * i >= cols) break;
+            uint4 w;
+            w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+            w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+            w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+            w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+            *reinterpret_cast<uint4*>(yp + 8 * i) = w;
+          }
+        } else {
+          float* yp = static_cast<float*>(p.y) + int64_t(m) * p.ldy + n0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (4 * i >= cols) break;
+            *reinterpret_cast<float4*>(yp + 4 * i) = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar(acc));
+      if (C::kNAcc == 2) { acc ^= 1; if (acc == 0) acc_phase ^= 1u; }
+      else acc_phase ^= 1u;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+  }
+}
+
+// ------------------------------------------------------------------ host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+              const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  uint32_t es[3] = {1, 1, 1};
+  return fn(m, dt, rank, const_cast<void*>(base), dims, strides_bytes, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int MODE, int STAGES>
+int run(const GemmCall& c, int num_sms, cudaStream_t s) {
+  using Cf = Cfg<BN, MODE, STAGES>;
+  const int64_t kb = c.K / 2;                       // bytes of codes per row
+  const int64_t natoms = c.K / 64;                  // 512-byte scale atoms per 128-row tile
+  CUtensorMap tA, tB, tSA, tSB;
+  bool ok = true;
+  if (MODE == 0) {
+    uint64_t d[2] = {uint64_t(kb), uint64_t(c.M)}, st[1] = {uint64_t(kb)};
+    uint32_t b[2] = {uint32_t(kKB), uint32_t(BM)};
+    ok &= make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.a, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    uint64_t d2[3] = {128, uint64_t(natoms), uint64_t(cdiv(c.M, 128))}, st2[2] = {512, uint64_t(natoms) * 512};
+    uint32_t b2[3] = {128, 4, 1};
+    ok &= make_map(&tSA, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, c.a_sf, d2, st2, b2, CU_TENSOR_MAP_SWIZZLE_NONE);
+  } else {
+    uint64_t d[3] = {uint64_t(kb), uint64_t(c.M), 3}, st[2] = {uint64_t(kb), uint64_t(kb) * uint64_t(c.M)};
+    uint32_t b[3] = {uint32_t(kKB), uint32_t(BM), 1};
+    ok &= make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c.a, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    tSA = tA;   // unused in mode 1
+  }
+  {
+    uint64_t d[2] = {uint64_t(kb), uint64_t(c.N)}, st[1] = {uint64_t(kb)};
+    uint32_t b[2] = {uint32_t(kKB), uint32_t(BN)};
+    ok &= make_map(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.w, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    uint64_t d2[3] = {128, uint64_t(natoms), uint64_t(cdiv(c.N, 128))}, st2[2] = {512, uint64_t(natoms) * 512};
+    uint32_t b2[3] = {128, 4, uint32_t(Cf::kRT)};
+    ok &= make_map(&tSB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, c.w_sf, d2, st2, b2, CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  if (!ok) return kELaunch;
+  Params p;
+  p.M = int(c.M); p.N = int(c.N); p.K = int(c.K);
+  p.KT = int(cdiv(c.K, 256));
+  p.MT = int(cdiv(c.M, BM));
+  p.NT = int(cdiv(c.N, BN));
+  p.g_a = c.g_a; p.row_scale = c.row_scale; p.g_w = c.g_w;
+  p.bias = static_cast<const uint16_t*>(c.bias);
+  p.residual = static_cast<const uint16_t*>(c.residual);
+  p.ldr = c.ldr; p.y = c.y; p.ldy = c.ldy; p.out_bf16 = c.out_bf16; p.gelu = c.gelu; p.pred = c.pred; p.err = c.err;
+  auto kern = gemm_fp4_kernel<BN, MODE, STAGES>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cf::kSmem)) != cudaSuccess)
+      return kELaunch;
+    attr_set = true;
+  }
+  const int tiles = p.MT * p.NT;
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  kern<<<grid, kThreads, Cf::kSmem, s>>>(tA, tB, tSA, tSB, p);
+  return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
+}
+
+}  // namespace
+
+int launch_gemm_fp4(const GemmCall& c, int num_sms, cudaStream_t s) {
+  if (c.mode == 0) return run<128, 0, 5>(c, num_sms, s);
+  return run<128, 1, 3>(c, num_sms, s);
+}
+
+}  // namespace sixbit

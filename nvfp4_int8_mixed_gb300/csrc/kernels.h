@@ -1,0 +1,51 @@
+// Host-side launchers of the sixbit kernels (internal to the library).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sixbit {
+
+int launch_amax(const void* x, int dtype, int64_t M, int64_t K, int64_t ldx, float* amax_out, float* row_amax_out,
+                int num_sms, cudaStream_t s);
+int launch_nvfp4_quant(const void* x, int dtype, int64_t M, int64_t K, int64_t ldx, const float* amax,
+                       uint8_t* codes, uint8_t* sf, float* g_out, const uint8_t* pred, int num_sms, cudaStream_t s);
+int launch_int8_quant(const void* x, int64_t M, int64_t K, int64_t ldx, const float* row_amax_in, int8_t* q,
+                      uint8_t* planes, float* row_scale, const uint8_t* pred, int num_sms, cudaStream_t s);
+
+size_t gamma_ws_bytes(int64_t n);
+int launch_block_gamma(const void* xin, const void* xout, int64_t n, void* delta, float* gamma_out, float* r2_out,
+                       int32_t* tdc_state, const uint8_t* computed, void* ws, cudaStream_t s);
+int launch_dmpq(const float* gamma, const float* alpha, const float* beta, const int32_t* layer_block,
+                int32_t n_layers, float tau, const int32_t* step, uint8_t* use_nvfp4, uint8_t* gates, cudaStream_t s);
+int launch_tdc(const void* xin, const void* delta, int64_t n, const float* r2, float tau2, int32_t max_skip,
+               const int32_t* tdc_state, uint8_t* compute_out, void* out, uint8_t* gates, int32_t n_gates,
+               int num_sms, cudaStream_t s);
+int launch_layernorm(const void* x, int64_t M, int64_t H, int64_t ldx, float eps, void* y, int64_t ldy,
+                     float* amax_out, float* row_amax_out, const uint8_t* pred, int num_sms, cudaStream_t s);
+
+// Block-scaled FP4 GEMM on tcgen05.  mode 0: W4A4 (A = NVFP4 codes + scales),
+// mode 1: W4A8 (A = three E2M1 digit planes of the INT8 codes + row scales).
+struct GemmCall {
+  int mode;
+  const uint8_t* a;          // codes [M, K/2] or planes [3][M][K/2]
+  const uint8_t* a_sf;       // mode 0: swizzled scales of A
+  const float* g_a;          // mode 0
+  const float* row_scale;    // mode 1
+  const uint8_t* w;          // [N, K/2]
+  const uint8_t* w_sf;       // swizzled scales of W
+  const float* g_w;
+  int64_t M, N, K;
+  const void* bias;          // bf16 [N] or null
+  const void* residual;      // bf16 [M, ldr] or null
+  int64_t ldr;
+  int gelu;
+  int out_bf16;
+  void* y;
+  int64_t ldy;
+  const uint8_t* pred;
+  int* err;                  // device error word
+};
+int launch_gemm_fp4(const GemmCall& c, int num_sms, cudaStream_t s);
+
+}  // namespace sixbit

@@ -1,0 +1,75 @@
+"""The C-ABI library loads without a GPU, exports every symbol the header
+declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sixbit.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import nvfp4_int8_mixed_gb300 as sb
+    if not os.path.exists(sb.LIB_PATH):
+        from nvfp4_int8_mixed_gb300 import build
+        build.build()
+    return sb.lib()
+
+
+def declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sixbit_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_binding_covers_header():
+    import nvfp4_int8_mixed_gb300 as sb
+    assert set(declared()) == set(sb._SIGS)
+
+
+def test_host_helpers(lib):
+    assert lib.sixbit_version().startswith(b"sixbit")
+    assert lib.sixbit_sf_bytes(256, 256) == 256 * 16
+    assert lib.sixbit_sf_bytes(200, 1920) == 256 * 120        # rows padded to 128
+    assert lib.sixbit_sf_bytes(1, 64) == 128 * 4
+    assert lib.sixbit_workspace_size(17776, 1920) >= 256 + 4 * 8 * ((17776 * 1920 + 16383) // 16384)
+
+
+def test_argument_errors_before_launch(lib):
+    import nvfp4_int8_mixed_gb300 as sb
+    P = ctypes.c_void_p
+    fake = P(1 << 20)       # never dereferenced: checks fail first
+    # null input
+    assert lib.sixbit_quantize_act_nvfp4(None, 16, 64, 64, fake, fake, fake, fake, None, None, None) == sb.EINVAL
+    # K not a multiple of 64
+    assert lib.sixbit_quantize_act_nvfp4(fake, 16, 96, 96, fake, fake, fake, fake, None, None, None) == sb.ESHAPE
+    # misaligned codes pointer
+    assert lib.sixbit_quantize_act_nvfp4(fake, 16, 64, 64, fake, P((1 << 20) + 4), fake, fake, None, None,
+                                         None) == sb.EALIGN
+    # INT8: neither q nor planes
+    assert lib.sixbit_quantize_act_int8(fake, 4, 64, 64, None, None, None, fake, None, None) == sb.EINVAL
+    assert lib.sixbit_quantize_act_int8(fake, 4, 32768, 32768, None, fake, None, fake, None, None) == sb.ESHAPE
+    # GEMM: N not a multiple of 16, bad dtype, ldy < N
+    args = lambda N, dt, ldy: (fake, fake, fake, 128, 256, fake, fake, fake, N, None, None, 0, 0, dt, fake, ldy,
+                               None, None)
+    assert lib.sixbit_qlinear_w4a4(*args(40, sb.BF16, 40)) == sb.ESHAPE
+    assert lib.sixbit_qlinear_w4a4(*args(64, 7, 64)) == sb.EINVAL
+    assert lib.sixbit_qlinear_w4a4(*args(64, sb.BF16, 32)) == sb.ESHAPE
+    assert lib.sixbit_qlinear_w4a8(fake, None, 128, 256, fake, fake, fake, 64, None, None, 0, 0, sb.F32, fake, 64,
+                                   None, None) == sb.EINVAL
+    assert lib.sixbit_block_gamma(fake, fake, 0, None, fake, None, None, None, fake, None) == sb.EINVAL
+    assert lib.sixbit_dmpq_assign(fake, fake, fake, fake, 0, ctypes.c_float(0.1), fake, fake, None, None) == sb.EINVAL
+    assert lib.sixbit_tdc_decide_and_apply(fake, fake, 16, fake, ctypes.c_float(0.05), 1, None, fake, fake, None, 0,
+                                           None) == sb.EINVAL
+    assert lib.sixbit_layernorm_bf16(fake, 4, 20, 20, ctypes.c_float(1e-5), fake, 20, None, None, None,
+                                     None) == sb.ESHAPE

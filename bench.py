@@ -1,0 +1,480 @@
+"""Benchmark of the 6Bit-Diffusion hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 2b|5b]
+
+One step = one pass of the whole hot path over one batch of synthetic input
+shaped like the 2B-class video-DiT GEMM set (M = 17776 tokens):
+for each linear layer (QKV 1920->5760, out-proj 1920->1920 + residual,
+FFN-up 1920->7680 + GELU, FFN-down 7680->1920 + residual)
+    NVFP4: tensor amax -> quantize -> W4A4 GEMM (bf16 out)
+    INT8:  per-token quantize (digit planes) -> W4A8 GEMM (bf16 out)
+then the block Gamma/Delta/r2 pass over a [M, 1920] block input/output,
+DMPQ assignment of the block's 4 layers, and the TDC decision.
+Weights are quantized once (offline) before timing.
+
+value = quantized-linear TFLOP/s = sum over the 8 GEMMs of 2MNK / step time
+(inputs already in HBM).  The working set of a step (~1.5 GB) is larger than
+the 129 MB L2, so no explicit flush is done between steps.
+
+--impl reference times the CPU oracle on a bounded sample of the same
+workload (the reference arm); other ranks exit at once.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+
+METRIC = "quantized-linear TFLOPS (NVFP4, INT8) + DiT blocks/s w/ DMPQ+TDC; % roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 : BF16 tensor ratio on GB300
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return FALLBACK, "fallback"
+
+
+def workload_layers(name: str):
+    return synthetic.GEMM_SHAPES["2B" if name == "2b" else "5B"]
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", gpu_id], stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.tmp.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.tmp.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- ncu traffic
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gemm_fp4.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "nvfp4_int8_mixed_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when there is none or the GEMM source changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = None
+    vals = {}
+    for line in open(path):
+        line = line.strip()
+        if line.startswith("source_sha256_16:"):
+            src = line.split(":", 1)[1].strip()
+        elif line and not line.startswith("#") and "=" in line:
+            k, v = line.split("=", 1)
+            try:
+                vals[k.strip()] = float(v)
+            except ValueError:
+                pass
+    if src != kernel_source_hash():
+        return None
+    return vals.get(kernel)
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_sample(layers, rows_per_layer: int, cols_per_layer: int, seed: int, M: int, prep=None):
+    """Prepare (untimed) oracle inputs for a sample: row/column subsets of
+    every layer, weights quantized by the oracle itself."""
+    from oracle import codecs, nvfp4
+    if prep is not None:
+        return prep
+    out = []
+    rng = np.random.default_rng(seed)
+    for li, (name, K, N, gelu, res) in enumerate(layers):
+        lay = synthetic.gemm_layer(1, M, K, N, res)
+        af = codecs.bf16_to_f32(lay["a"])
+        amax_t = np.float32(np.max(np.abs(af)))
+        rows = rng.choice(M, rows_per_layer, replace=False)
+        cols = rng.choice(N, cols_per_layer, replace=False)
+        wc, wsf, gw, _ = nvfp4.quantize(lay["w"][cols])
+        out.append(dict(a=af[rows], amax=amax_t, wc=wc, wsf=wsf, gw=gw, gelu=gelu,
+                        res=None if lay["residual"] is None else lay["residual"][rows][:, cols], K=K))
+    g = synthetic.gamma_pair(7, 64, 1920)
+    return dict(layers=out, gamma=g)
+
+
+def oracle_step(prep):
+    """One bounded oracle pass: quantize + both GEMMs per layer sample, Gamma,
+    DMPQ, TDC decision.  Returns the algorithmic FLOPs it covered."""
+    from oracle import dmpq, gamma, gemm, int8, nvfp4, tdc
+    flops = 0
+    for L in prep["layers"]:
+        c, s, g, _ = nvfp4.quantize(L["a"], L["amax"])
+        gemm.w4a4(c, s, g, L["wc"], L["wsf"], L["gw"], gelu=L["gelu"], residual=L["res"], out_dtype="bf16")
+        q, sc, _ = int8.quantize(L["a"])
+        gemm.w4a8(q, sc, L["wc"], L["wsf"], L["gw"], gelu=L["gelu"], residual=L["res"], out_dtype="bf16")
+        flops += 2 * 2 * L["a"].shape[0] * L["wc"].shape[0] * L["K"]
+    p = prep["gamma"]
+    G, dn, r2 = gamma.block_pass(p["xin"], p["xout"], p["delta_prev"])
+    dmpq.assign(np.array([G]), np.ones(4, np.float32), np.zeros(4, np.float32), np.zeros(4, np.int64), 0.1, 1)
+    tdc.decide(tdc.BlockCache(fresh_count=2, r2=r2), 0.05, 1)
+    return flops
+
+
+def cpu_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        n = max([i.get("num_threads", 1) for i in info] or [1])
+        return int(n)
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def time_oracle(layers, M, rows, cols, steps=1, warmup=0, seed=0):
+    prep = oracle_sample(layers, rows, cols, seed, M)
+    for _ in range(warmup):
+        oracle_step(prep)
+    t0 = time.perf_counter()
+    flops = 0
+    for _ in range(steps):
+        flops += oracle_step(prep)
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, dt, flops
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    layers = workload_layers(args.workload)
+    M = synthetic.M_2B if args.workload == "2b" else synthetic.M_2B
+    rows, cols = 8, 128
+    prep = oracle_sample(layers, rows, cols, 0, M)
+    for _ in range(args.warmup):
+        oracle_step(prep)
+    t0 = time.perf_counter()
+    flops = sum(oracle_step(prep) for _ in range(args.steps))
+    dt = time.perf_counter() - t0
+    v = flops / dt / 1e12
+    sample = (f"per step: {rows} random rows x {cols} random output columns of each of the 4 layers, "
+              f"NVFP4+W4A4 and INT8+W4A8, plus Gamma/DMPQ/TDC on a 64x1920 block pair")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.workload.upper()}-class video-DiT GEMM set, M={M}, oracle sample"},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import nvfp4_int8_mixed_gb300 as sb
+    if not os.path.exists(sb.LIB_PATH):
+        from nvfp4_int8_mixed_gb300 import build as _b
+        _b.build()
+    sb.lib()
+
+    layers = workload_layers(args.workload)
+    M = synthetic.M_2B
+    H = layers[0][1]
+    to_dev = lambda bits: torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    # ---- setup (untimed): inputs in HBM, weights quantized once
+    L = []
+    host_inputs = []
+    for li, (name, K, N, gelu, res) in enumerate(layers):
+        lay = synthetic.gemm_layer(1, M, K, N, res)
+        x = to_dev(lay["a"])
+        r = to_dev(lay["residual"]) if res else None
+        wc, wsf, gw = sb.quantize_weight_nvfp4(torch.from_numpy(lay["w"]).to(dev))
+        L.append(dict(name=name, K=K, N=N, gelu=gelu, x=x, r=r, wc=wc, wsf=wsf, gw=gw,
+                      codes=torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
+                      sf=torch.empty(sb.sf_bytes(M, K), dtype=torch.uint8, device=dev),
+                      ga=torch.empty(1, dtype=torch.float32, device=dev),
+                      planes=torch.empty((3, M, K // 2), dtype=torch.uint8, device=dev),
+                      s=torch.empty(M, dtype=torch.float32, device=dev),
+                      y4=torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+                      y8=torch.empty((M, N), dtype=torch.bfloat16, device=dev)))
+        host_inputs.append((lay["a"], lay["residual"]))
+    gp = synthetic.gamma_pair(7, M, H)
+    bin_, bout, bdelta = to_dev(gp["xin"]), to_dev(gp["xout"]), to_dev(gp["delta_prev"])
+    gamma_t = torch.zeros(4, dtype=torch.float32, device=dev)   # [gamma, r2, ...]
+    state = torch.tensor([1, 0], dtype=torch.int32, device=dev)
+    step_t = torch.ones(1, dtype=torch.int32, device=dev)
+    alpha = torch.linspace(0.5, 1.5, 4, device=dev)
+    beta = torch.full((4,), 0.005, device=dev)
+    lbk = torch.zeros(4, dtype=torch.int32, device=dev)
+    flags = torch.empty(4, dtype=torch.uint8, device=dev)
+    gates = torch.empty((4, 2), dtype=torch.uint8, device=dev)
+    cflag = torch.empty(1, dtype=torch.uint8, device=dev)
+    tdc_out = torch.empty_like(bin_)
+    sb.workspace(int(sb.lib().sixbit_workspace_size(M * H, 1)))
+
+    flops_layer = [2 * M * l["N"] * l["K"] for l in L]
+    flops_step = 2 * sum(flops_layer)
+    names = []
+    for l in L:
+        names += [f"quant_nvfp4[{l['name']}]", f"w4a4[{l['name']}]", f"quant_int8[{l['name']}]", f"w4a8[{l['name']}]"]
+    names += ["gamma_delta", "dmpq", "tdc"]
+    launches_per_step = 4 * 5 + 3      # amax + nvfp4 quant + w4a4 + int8 quant + w4a8 per layer; gamma, dmpq, tdc
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        k = 0
+        for l in L:
+            ops = [
+                lambda: sb.quantize_act_nvfp4(l["x"], out=(l["codes"], l["sf"], l["ga"])),
+                lambda: sb.qlinear_w4a4(l["codes"], l["sf"], l["ga"], l["wc"], l["wsf"], l["gw"], residual=l["r"],
+                                        gelu=l["gelu"], out=l["y4"]),
+                lambda: sb.quantize_act_int8(l["x"], out=(None, l["planes"], l["s"])),
+                lambda: sb.qlinear_w4a8(l["planes"], l["s"], l["wc"], l["wsf"], l["gw"], residual=l["r"],
+                                        gelu=l["gelu"], out=l["y8"]),
+            ]
+            for op in ops:
+                if evs is not None:
+                    evs[k][0].record(stream)
+                op()
+                if evs is not None:
+                    evs[k][1].record(stream)
+                k += 1
+        tail = [
+            lambda: sb.block_gamma(bin_, bout, delta=bdelta, gamma_out=gamma_t[0:1], r2_out=gamma_t[1:2],
+                                   tdc_state=state),
+            lambda: sb.dmpq_assign(gamma_t[0:1], alpha, beta, lbk, 0.1, step_t, use_nvfp4=flags, gates=gates),
+            lambda: sb.tdc_decide_and_apply(bin_, bdelta, gamma_t[1:2], 0.05, 1, state, cflag, tdc_out, gates=gates),
+        ]
+        for op in tail:
+            if evs is not None:
+                evs[k][0].record(stream)
+            op()
+            if evs is not None:
+                evs[k][1].record(stream)
+            k += 1
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    sb.get_error()
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- device-resident timing (headline value) with per-kernel events
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in names]
+           for _ in range(args.steps)]
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", ""))
+    sampler = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or str(local)))
+    time.sleep(0.3)
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    sb.get_error()
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    if ws > 1:
+        tt = torch.tensor([elapsed], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed = float(tt.item())
+    per_kernel = {n: [] for n in names}
+    for i in range(args.steps):
+        for k, n in enumerate(names):
+            per_kernel[n].append(evs[i][k][0].elapsed_time(evs[i][k][1]) / 1e3)
+    mean_t = {n: float(np.mean(v)) for n, v in per_kernel.items()}
+    value = flops_step * args.steps * ws / elapsed / 1e12
+
+    # ---- end to end through the public API: pinned host inputs copied in every step
+    pinned = []
+    h2d = 0
+    for (a, r), l in zip(host_inputs, L):
+        ha = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hr = torch.from_numpy(r.view(np.int16)).view(torch.bfloat16).pin_memory() if r is not None else None
+        pinned.append((ha, hr))
+        h2d += ha.numel() * 2 + (hr.numel() * 2 if hr is not None else 0)
+    hb = [torch.from_numpy(gp[k].view(np.int16)).view(torch.bfloat16).pin_memory() for k in ("xin", "xout")]
+    h2d += sum(t.numel() * 2 for t in hb)
+    res_host = torch.empty(4 + 4 + 1, dtype=torch.uint8).pin_memory()
+    d2h = res_host.numel() + 8
+    out_host = torch.empty(2, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        for (ha, hr), l in zip(pinned, L):
+            l["x"].copy_(ha, non_blocking=True)
+            if hr is not None:
+                l["r"].copy_(hr, non_blocking=True)
+        bin_.copy_(hb[0], non_blocking=True)
+        bout.copy_(hb[1], non_blocking=True)
+        step()
+        out_host.copy_(gamma_t[0:2], non_blocking=True)
+        res_host[0:4].copy_(flags, non_blocking=True)
+        res_host[4:8].copy_(gates.view(-1)[0:4], non_blocking=True)
+        res_host[8:9].copy_(cflag, non_blocking=True)
+
+    e2e_steps = max(3, args.steps // 4)
+    e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_elapsed = e0.elapsed_time(e1) / 1e3
+    if ws > 1:
+        tt = torch.tensor([e2e_elapsed], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_elapsed = float(tt.item())
+    e2e_value = flops_step * e2e_steps * ws / e2e_elapsed / 1e12
+
+    # ---- roofline of the dominant kernel
+    peaks, peak_kind = load_peaks()
+    fp4_peak = float(peaks["bf16_tflops"]) * FP4_OVER_BF16
+    family = {}
+    for n, t in mean_t.items():
+        family.setdefault(n.split("[")[0], []).append((n, t))
+    gemm_names = [n for n in names if n.startswith("w4a")]
+    dom = max(gemm_names, key=lambda n: mean_t[n])
+    li = [l["name"] for l in L].index(dom.split("[")[1][:-1])
+    dom_flops = flops_layer[li]
+    # W4A8 runs three FP4 digit MMAs per product: its ceiling is a third of the FP4 peak
+    dom_peak = fp4_peak / 3.0 if dom.startswith("w4a8") else fp4_peak
+    achieved = dom_flops / mean_t[dom] / 1e12
+    traffic = dram_traffic(dom)
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": dom_peak, "unit": "TFLOP/s",
+                "frac": achieved / dom_peak, "traffic": traffic,
+                "peak_note": f"{peak_kind} bf16 burst {peaks['bf16_tflops']} TFLOP/s x nominal FP4/BF16 ratio 6"
+                             + ("; / 3 for the three digit-plane MMAs of W4A8" if dom.startswith("w4a8") else "")}
+    hbm = float(peaks["hbm_gbs"])
+    byte_rows = {}
+    for l in L:
+        n_el = M * l["K"]
+        byte_rows[f"quant_nvfp4[{l['name']}]"] = (2 + 2 + 0.5 + 1 / 16) * n_el   # amax read, read, codes, scales
+        byte_rows[f"quant_int8[{l['name']}]"] = (2 + 2 + 1.5) * n_el + 4 * M     # 2 reads (2nd from L2), planes
+    byte_rows["gamma_delta"] = 8.0 * M * H
+    bw = {n: {"ms": mean_t[n] * 1e3, "GB/s": byte_rows[n] / mean_t[n] / 1e9,
+              "frac_hbm": byte_rows[n] / mean_t[n] / 1e9 / hbm} for n in byte_rows}
+    tf = {n: {"ms": mean_t[n] * 1e3, "TFLOP/s": flops_layer[[l["name"] for l in L].index(n.split("[")[1][:-1])]
+                    / mean_t[n] / 1e12} for n in gemm_names}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rows, cols = 64, 512
+        v_cpu, dt_cpu, fl = time_oracle(layers, M, rows, cols, steps=1, warmup=0, seed=1)
+        cpu = {"value": v_cpu, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+               "sample": f"{rows} random rows x {cols} random output columns of each of the 4 layers, NVFP4+W4A4 and "
+                         f"INT8+W4A8 ({fl / 1e9:.1f} GFLOP, {dt_cpu:.1f} s), plus Gamma/DMPQ/TDC on a 64x1920 pair"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+                "warmup": max(args.warmup, 3), "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "fp4 (e2m1 x e2m1, fp32 accumulate)",
+                "data": "synthetic",
+                "config": {"workload": f"{args.workload.upper()}-class video-DiT GEMM set, M={M} tokens, "
+                                       "4 linears x (NVFP4+W4A4, INT8+W4A8) + Gamma/DMPQ/TDC",
+                           "shapes": [[l["name"], M, l["K"], l["N"]] for l in L], "l2": "inputs larger than L2",
+                           "parallelism": f"replicas x{ws}"},
+                "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+                        "d2h_bytes_per_step": int(d2h)},
+                "gpu_launches": launches_per_step * args.steps,
+                "clocks": clocks, "roofline": roofline, "cpu_baseline": cpu,
+                "per_kernel": {"gemm": tf, "bandwidth": bw, "dmpq_ms": mean_t["dmpq"] * 1e3,
+                               "tdc_ms": mean_t["tdc"] * 1e3}}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["2b", "5b"], default="2b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -18,8 +18,11 @@ W4A8) and stores bf16.  Biases are zero.  The stack feeds step t's input to
 block 0, chains the blocks, and records the last block's output (reading:
 the output is not fed back into the next step's input).
 
-Parity: LN pinned against torch's layer_norm (float64); the block and stack
-are compositions of pinned parts (no separate pin).
+Parity: LN pinned against torch's layer_norm (float64); the block's wiring
+pinned by zero weights (the block is then the identity) and by weights
+confined to the Q/K rows (the V slice is zero, so x1 = x); the stack's rules
+pinned by properties (TDC off == tau_tdc = 0, forced flags == tau = inf, the
+alternating skip pattern under max_skip = 1).
 """
 from __future__ import annotations
 

@@ -47,3 +47,33 @@ def test_stack_skip_reuses_delta():
     skips = np.array(r["skips"])
     assert not skips[:2].any()                     # need two fresh updates first
     assert skips[2].all() and not skips[3].any() and skips[4].all()   # max_skip = 1 alternates
+
+
+def test_block_residual_wiring_with_zero_weights():
+    # all weights zero: every linear outputs 0 (+ residual), GELU(0) = 0, so out == in exactly
+    rng = np.random.default_rng(3)
+    H, F, M = 64, 128, 24
+    x = codecs.f32_to_bf16(rng.standard_normal((M, H)).astype(np.float32))
+    zero = lambda n, k: block.quantize_weights(np.zeros((n, k), np.float32))
+    wq = dict(qkv=zero(3 * H, H), out=zero(H, H), up=zero(F, H), down=zero(H, F))
+    for flags in ([0, 0, 0, 0], [1, 1, 1, 1], [1, 0, 1, 0]):
+        assert np.array_equal(block.block_forward(x, wq, flags), x)
+
+
+def test_block_out_proj_reads_the_v_slice():
+    # weights only in the Q and K rows of W_qkv: the V slice is zero, so x1 = x and
+    # with W_up = 0 the block is the identity; weights in the V rows change the output
+    rng = np.random.default_rng(4)
+    H, F, M = 64, 128, 24
+    x = codecs.f32_to_bf16(rng.standard_normal((M, H)).astype(np.float32))
+    w_qk = np.zeros((3 * H, H), np.float32)
+    w_qk[:2 * H] = rng.standard_normal((2 * H, H)).astype(np.float32)
+    w_v = np.zeros((3 * H, H), np.float32)
+    w_v[2 * H:] = rng.standard_normal((H, H)).astype(np.float32)
+    eye = block.quantize_weights(np.eye(H, dtype=np.float32))
+    zero = lambda n, k: block.quantize_weights(np.zeros((n, k), np.float32))
+    base = dict(out=eye, up=zero(F, H), down=zero(H, F))
+    out_qk = block.block_forward(x, dict(base, qkv=block.quantize_weights(w_qk)), [1, 1, 1, 1])
+    out_v = block.block_forward(x, dict(base, qkv=block.quantize_weights(w_v)), [1, 1, 1, 1])
+    assert np.array_equal(out_qk, x)
+    assert not np.array_equal(out_v, x)

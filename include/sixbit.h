@@ -154,6 +154,26 @@ int sixbit_block_gamma(const void* in, const void* out, int64_t n, void* delta,
                        float* gamma_out, float* r2_out, int32_t* tdc_state,
                        const uint8_t* computed, void* ws, sixbit_stream_t stream);
 
+/* Scratch-free variant of sixbit_block_gamma.  The paper has no counterpart:
+ * this exists for callers that cannot hand the library scratch memory --
+ * applications whose device memory is fully planned by another allocator,
+ * or code running where allocation is not allowed (a plugin's enqueue step,
+ * a latency-critical loop that cannot take cudaMalloc's implicit device
+ * synchronization).  Same arguments and results as sixbit_block_gamma
+ * without `ws`; n <= SIXBIT_NOALLOC_GAMMA_MAX_ELEMS, else SIXBIT_ESHAPE and
+ * nothing is launched.  The scratch is a fixed 262,400-byte device array
+ * inside the library that every device loading the library holds until the
+ * process exits.  The first call on a device looks up that array's device
+ * address (with the device current), so make that first call before any
+ * stream capture.  Every call clears the array's counter (an async memset on
+ * `stream`) and then reuses it, so calls whose kernels overlap on the GPU --
+ * on different streams, or on different host threads -- race and must be
+ * avoided.  Allocates no device memory. */
+#define SIXBIT_NOALLOC_GAMMA_MAX_ELEMS (((int64_t)1) << 27)
+int sixbit_block_gamma_noalloc(const void* in, const void* out, int64_t n, void* delta,
+                               float* gamma_out, float* r2_out, int32_t* tdc_state,
+                               const uint8_t* computed, sixbit_stream_t stream);
+
 /* a8 -- DMPQ assignment (Figure 3: per-layer line E_rel = alpha*Gamma_{t-1}
  * + beta; "Abstract": NVFP4 for stable layers).  For each layer l:
  *   p = f32(f32(alpha[l]*gamma[layer_block[l]]) + beta[l]);

@@ -40,6 +40,7 @@ _SIGS = {
     "sixbit_qlinear_w4a4": ([_P, _P, _P, _I64, _I64, _P, _P, _P, _I64, _P, _P, _I64, _INT, _INT, _P, _I64, _P, _P], _INT),
     "sixbit_qlinear_w4a8": ([_P, _P, _I64, _I64, _P, _P, _P, _I64, _P, _P, _I64, _INT, _INT, _P, _I64, _P, _P], _INT),
     "sixbit_block_gamma": ([_P, _P, _I64, _P, _P, _P, _P, _P, _P, _P], _INT),
+    "sixbit_block_gamma_noalloc": ([_P, _P, _I64, _P, _P, _P, _P, _P, _P], _INT),
     "sixbit_dmpq_assign": ([_P, _P, _P, _P, _I32, _F, _P, _P, _P, _P], _INT),
     "sixbit_tdc_decide_and_apply": ([_P, _P, _I64, _P, _F, _I32, _P, _P, _P, _P, _I32, _P], _INT),
     "sixbit_layernorm_bf16": ([_P, _I64, _I64, _I64, _F, _P, _I64, _P, _P, _P, _P], _INT),

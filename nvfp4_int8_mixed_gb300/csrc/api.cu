@@ -173,6 +173,14 @@ int sixbit_block_gamma(const void* in, const void* out, int64_t n, void* delta, 
   return launch_block_gamma(in, out, n, delta, gamma_out, r2_out, tdc_state, computed, ws, cs(stream));
 }
 
+int sixbit_block_gamma_noalloc(const void* in, const void* out, int64_t n, void* delta, float* gamma_out,
+                               float* r2_out, int32_t* tdc_state, const uint8_t* computed, sixbit_stream_t stream) {
+  if (!in || !out || !gamma_out || n <= 0) return kEInval;
+  if (n > block_gamma_noalloc_max_elems()) return kEShape;
+  if (!aligned16(in) || !aligned16(out) || (delta && !aligned16(delta))) return kEAlign;
+  return launch_block_gamma_noalloc(in, out, n, delta, gamma_out, r2_out, tdc_state, computed, cs(stream));
+}
+
 int sixbit_dmpq_assign(const float* gamma, const float* alpha, const float* beta, const int32_t* layer_block,
                        int32_t n_layers, float tau, const int32_t* step, uint8_t* use_nvfp4, uint8_t* gates,
                        sixbit_stream_t stream) {

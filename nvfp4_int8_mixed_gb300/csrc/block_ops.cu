@@ -6,6 +6,8 @@
 // decides from the updates of the two preceding steps), Figure 3 (per-layer
 // line alpha*Gamma + beta), Figure 4 (updates compared by relative L2).
 // Decisions are computed and consumed on the device: no host round trip.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -254,6 +256,53 @@ __global__ void __launch_bounds__(kThreads) layernorm_kernel(const uint16_t* __r
 }
 
 }  // namespace
+
+// ---------------------------------------------------------------------------
+// Scratch-free Gamma pass.  Some callers cannot give this library scratch
+// memory: their device memory is entirely planned by another allocator, or
+// they run where allocating is not allowed (a plugin's enqueue step, a
+// latency-critical loop that cannot afford cudaMalloc's implicit device
+// synchronization).  For them the pass keeps its CTA counter and float64
+// partial sums in this fixed device array instead of caller scratch.  The
+// array lives on every device that loads the library, until the process
+// exits, and bounds the tensor size to kNoAllocMaxElems.
+constexpr int64_t kNoAllocMaxElems = int64_t(1) << 27;                  // 134,217,728 elements
+constexpr int64_t kNoAllocMaxTiles = kNoAllocMaxElems / kTile;           // 8192 tiles
+constexpr size_t kNoAllocBytes = 256 + size_t(kNoAllocMaxTiles) * 4 * sizeof(double);   // 262,400 bytes
+static __device__ __align__(256) unsigned char g_gamma_scratch[kNoAllocBytes];
+
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_scratch[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array for the current device.  Host code may
+// not use the array's name as a device pointer; the address is looked up
+// once per device, with that device current, on the first call there.
+void* noalloc_scratch_for_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_scratch[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_gamma_scratch) != cudaSuccess) return nullptr;
+    g_noalloc_scratch[dev] = p;
+  }
+  return g_noalloc_scratch[dev];
+}
+}  // namespace
+
+int64_t block_gamma_noalloc_max_elems() { return kNoAllocMaxElems; }
+
+int launch_block_gamma_noalloc(const void* xin, const void* xout, int64_t n, void* delta, float* gamma_out,
+                               float* r2_out, int32_t* tdc_state, const uint8_t* computed, cudaStream_t s) {
+  if (n > kNoAllocMaxElems) return kEShape;
+  void* scratch = noalloc_scratch_for_current_device();
+  if (!scratch) return kELaunch;
+  // The array keeps the previous call's contents: the CTA counter must start at 0.
+  if (cudaMemsetAsync(scratch, 0, 256, s) != cudaSuccess) return kELaunch;
+  return launch_block_gamma(xin, xout, n, delta, gamma_out, r2_out, tdc_state, computed, scratch, s);
+}
 
 size_t gamma_ws_bytes(int64_t n) { return sizeof(GammaWs) + size_t(cdiv(n, kTile)) * 4 * sizeof(double) + 256; }
 

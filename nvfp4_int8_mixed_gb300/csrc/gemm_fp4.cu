@@ -12,17 +12,18 @@
 //                 no tcgen05 int8 kind, and its warp-level int8 MMA runs at
 //                 ~150 TOP/s, far below the FP4 pipe.)
 //
-// Structure: persistent, warp-specialized CTA of 6 warps over 128 x BN
-// output tiles, K in steps of 256 (128 bytes of codes per row):
-//   warp 0      TMA producer: A/B code tiles (128B swizzle) and the
+// Structure: persistent, warp-specialized CTA of 10 warps over 128 x 256
+// output tiles, K in steps of KB bytes of codes per row (2*KB elements):
+//   warp 0      TMA producer: A/B code tiles (KB-byte swizzle) and the
 //               scale-factor atoms into a STAGES-deep shared-memory ring;
 //   warp 1      TMEM owner and MMA issuer: tcgen05.cp of the scale atoms
-//               into TMEM, tcgen05.mma kind::mxf4nvf4 scale_vec::4X into a
-//               double-buffered TMEM accumulator, tcgen05.commit to free
-//               stages and publish finished tiles;
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane
-//               quarter per warp, one output row per thread), scale, bias,
-//               GELU, residual, store -- overlapping the next tile's MMAs.
+//               into per-stage TMEM columns, tcgen05.mma kind::mxf4nvf4
+//               scale_vec::4X (128 x 256 x 64 per instruction) into the TMEM
+//               accumulator, tcgen05.commit to free stages and publish tiles;
+//   warps 2..9  epilogue: two warps per TMEM lane quarter, 128 columns each.
+//               They pull the whole accumulator into registers, release TMEM
+//               at once (the next tile's MMAs start), then scale, add bias,
+//               GELU, add residual and store from registers.
 // Every mbarrier wait is bounded; on expiry the CTA records an error in the
 // device error word, drains its own copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -35,33 +36,38 @@ namespace sixbit {
 namespace {
 
 constexpr int BM = 128;
-constexpr int kKB = 128;                 // bytes of packed codes per row per K step (256 elements)
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;            // producer, MMA, 8 epilogue warps
+constexpr int kEpiThreads = 256;
 constexpr uint32_t kSpinCap = 1u << 22;  // polls of a bounded mbarrier wait
 constexpr uint32_t kTmemCols = 512;
 
-template <int BN, int MODE, int STAGES>
+template <int BN, int MODE, int STAGES, int KB>
 struct Cfg {
-  static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
+  static_assert(BN == 256, "epilogue assumes 256-column tiles");
+  static_assert(KB == 64 || KB == 128, "K step of 64 or 128 bytes per row");
+  static constexpr int kMmaK = KB / 32;                    // MMAs (K = 64 elements) per stage
   static constexpr int kPlanes = MODE == 0 ? 1 : 3;
   static constexpr int kRT = BN / 128;                     // 128-row scale tiles of W per N tile
-  static constexpr int kA = BM * kKB;                      // one A plane tile
-  static constexpr int kB = BN * kKB;
-  static constexpr int kSFA = MODE == 0 ? 2048 : 0;        // 4 atoms of 512 bytes
-  static constexpr int kSFB = 2048 * kRT;
+  static constexpr int kA = BM * KB;                       // one A plane tile
+  static constexpr int kB = BN * KB;
+  static constexpr int kSFA = MODE == 0 ? 512 * kMmaK : 0; // one 512-byte atom per MMA
+  static constexpr int kSFB = 512 * kMmaK * kRT;
   static constexpr int offB = kPlanes * kA;
   static constexpr int offSFA = offB + kB;
   static constexpr int offSFB = offSFA + kSFA;
-  static constexpr int kStage = offSFB + kSFB;             // multiple of 1024
+  static constexpr int kStage = offSFB + kSFB;
+  static_assert(kStage % 1024 == 0, "stages stay 1024-byte aligned");
   static constexpr uint32_t kTx = kStage;                  // bytes landed per stage
-  // TMEM columns
-  static constexpr int kSfStride = (MODE == 0 ? 16 : 0) + 16 * kRT;
-  static constexpr int kNAcc = (2 * BN + STAGES * kSfStride + 12 <= int(kTmemCols)) ? 2 : 1;
-  static constexpr int kSfBase = kNAcc * BN;
+  // TMEM columns: accumulator [0, BN), then per-stage scale columns, then
+  // the three constant digit-scale atoms (mode 1).
+  static constexpr int kSfaCols = MODE == 0 ? 4 * kMmaK : 0;
+  static constexpr int kSfStride = kSfaCols + 4 * kMmaK * kRT;
+  static constexpr int kSfBase = BN;
   static constexpr int kConstCol = kSfBase + STAGES * kSfStride;
   static_assert(kConstCol + 12 <= int(kTmemCols), "TMEM budget");
   static constexpr int kExtra = 2048;                      // constant digit-scale atoms + barriers
   static constexpr size_t kSmem = size_t(STAGES) * kStage + kExtra + 1024;
+  static_assert(kSmem <= 232448, "shared memory budget");
 };
 
 // ------------------------------------------------------------- PTX wrappers
@@ -141,11 +147,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128
-// bytes, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
-  return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) | (uint64_t(1) << 46) |
-         (uint64_t(2) << 61);
+// Shared-memory matrix descriptor, K-major, KB-byte swizzle: rows of KB
+// bytes, 8-row groups 8*KB bytes apart (layout code 2 = 128B, 4 = 64B).
+template <int KB>
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) {
+  constexpr uint64_t layout = KB == 128 ? 2 : 4;
+  return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t((8 * KB) >> 4) << 32) |
+         (uint64_t(1) << 46) | (layout << 61);
 }
 // Descriptor of a 512-byte scale atom: 8-row core matrices of 16-byte rows, 128 bytes apart.
 __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
@@ -157,9 +165,14 @@ __host__ __device__ constexpr uint32_t idesc_fp4(int n) {
   return (1u << 7) | (1u << 10) | (uint32_t(n >> 3) << 17) | (uint32_t(BM >> 4) << 24);
 }
 
+// tanh-form GELU, 0.5 x (1 + tanh(u)) with u = sqrt(2/pi) (x + 0.044715 x^3),
+// written as x / (1 + exp(-2u)) (the same function).  exp and the division
+// use the hardware approximations (ex2.approx, rcp.approx: ~1e-6 relative);
+// the IEEE reciprocal's special-case path made this epilogue slower than the
+// tile's MMAs.  Large negative u gives exp = inf and a result of -0.
 __device__ __forceinline__ float gelu_tanh(float x) {
   const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
-  return 0.5f * x * (1.f + tanhf(u));
+  return __fdividef(x, 1.f + __expf(-2.f * u));
 }
 
 struct Params {
@@ -177,36 +190,38 @@ struct Params {
   int* err;
 };
 
-template <int BN, int MODE, int STAGES>
+template <int BN, int MODE, int STAGES, int KB>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                     const Params p) {
-  using C = Cfg<BN, MODE, STAGES>;
+  using C = Cfg<BN, MODE, STAGES, KB>;
   if (p.pred && *p.pred == 0) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* extra = smem + size_t(STAGES) * C::kStage;
   uint8_t* const_sfa = extra;                                    // 3 x 512 bytes (mode 1)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(extra + 1536);    // full[S] empty[S] tfull[2] tempty[2] drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(extra + 1536);    // full[S] empty[S] tfull tempty drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * uint32_t(s); };
   auto empty_bar = [&](int s) { return bar0 + 8u * uint32_t(STAGES + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * uint32_t(2 * STAGES + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * uint32_t(2 * STAGES + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8u * uint32_t(2 * STAGES + 4);
+  const uint32_t tfull_bar = bar0 + 8u * uint32_t(2 * STAGES);
+  const uint32_t tempty_bar = bar0 + 8u * uint32_t(2 * STAGES + 1);
+  const uint32_t drain_bar = bar0 + 8u * uint32_t(2 * STAGES + 2);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(tfull_bar(a), 1); mbar_init(tempty_bar(a), 128); }
+    mbar_init(tfull_bar, 1);
+    mbar_init(tempty_bar, kEpiThreads);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    prefetch_tmap(&tmA); prefetch_tmap(&tmB); prefetch_tmap(&tmB);
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
     if (MODE == 0) prefetch_tmap(&tmSFA);
     prefetch_tmap(&tmSFB);
   }
@@ -247,14 +262,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t fb = full_bar(stage);
         mbar_expect_tx(fb, C::kTx);
         if (MODE == 0) {
-          tma_load_2d(smem_u32(sb), &tmA, kt * kKB, mt * BM, fb);
-          tma_load_3d(smem_u32(sb + C::offSFA), &tmSFA, 0, kt * 4, mt, fb);
+          tma_load_2d(smem_u32(sb), &tmA, kt * KB, mt * BM, fb);
+          tma_load_3d(smem_u32(sb + C::offSFA), &tmSFA, 0, kt * C::kMmaK, mt, fb);
         } else {
 #pragma unroll
-          for (int pl = 0; pl < 3; ++pl) tma_load_3d(smem_u32(sb + pl * C::kA), &tmA, kt * kKB, mt * BM, pl, fb);
+          for (int pl = 0; pl < 3; ++pl) tma_load_3d(smem_u32(sb + pl * C::kA), &tmA, kt * KB, mt * BM, pl, fb);
         }
-        tma_load_2d(smem_u32(sb + C::offB), &tmB, kt * kKB, nt * BN, fb);
-        tma_load_3d(smem_u32(sb + C::offSFB), &tmSFB, 0, kt * 4, nt * C::kRT, fb);
+        tma_load_2d(smem_u32(sb + C::offB), &tmB, kt * KB, nt * BN, fb);
+        tma_load_3d(smem_u32(sb + C::offSFB), &tmSFB, 0, kt * C::kMmaK, nt * C::kRT, fb);
         issued |= 1u << stage;
         last_par = (last_par & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -271,39 +286,43 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int pl = 0; pl < 3; ++pl) tc_cp_sf(tmem + C::kConstCol + 4 * pl, desc_sf(smem_u32(const_sfa + 512 * pl)));
     }
-    int stage = 0, acc = 0;
+    // Descriptors of stage 0; stage s adds s * kStage bytes (>> 4) to the start address field.
+    const uint64_t adesc_s0 = desc_kmajor<KB>(smem_u32(smem));
+    const uint64_t bdesc_s0 = desc_kmajor<KB>(smem_u32(smem + C::offB));
+    const uint64_t sfa_s0 = desc_sf(smem_u32(smem + C::offSFA));
+    const uint64_t sfb_s0 = desc_sf(smem_u32(smem + C::offSFB));
+    int stage = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-      if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) { fail(); ok = false; break; }
+      // the epilogue has pulled the previous tile out of TMEM
+      if (!mbar_wait(tempty_bar, acc_phase ^ 1u, abort_flag)) { fail(); ok = false; break; }
       tc_fence_after();
-      const uint32_t d_tmem = tmem + uint32_t(acc * BN);
       for (int kt = 0; kt < p.KT; ++kt) {
         if (!mbar_wait(full_bar(stage), phase, abort_flag)) { fail(); ok = false; break; }
         tc_fence_after();
-        uint8_t* sb = smem + size_t(stage) * C::kStage;
+        const uint64_t soff = uint64_t((stage * C::kStage) >> 4);
         const uint32_t sfa_t = tmem + uint32_t(C::kSfBase + stage * C::kSfStride);
-        const uint32_t sfb_t = sfa_t + (MODE == 0 ? 16u : 0u);
+        const uint32_t sfb_t = sfa_t + uint32_t(C::kSfaCols);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (MODE == 0) tc_cp_sf(sfa_t + 4 * j, desc_sf(smem_u32(sb + C::offSFA + 512 * j)));
+        for (int j = 0; j < C::kMmaK; ++j) {
+          if (MODE == 0) tc_cp_sf(sfa_t + 4 * j, sfa_s0 + soff + uint64_t((512 * j) >> 4));
 #pragma unroll
           for (int r = 0; r < C::kRT; ++r)
-            tc_cp_sf(sfb_t + 4 * (C::kRT * j + r), desc_sf(smem_u32(sb + C::offSFB + 512 * (4 * r + j))));
+            tc_cp_sf(sfb_t + 4 * (C::kRT * j + r), sfb_s0 + soff + uint64_t((512 * (C::kMmaK * r + j)) >> 4));
         }
-        const uint64_t bdesc0 = desc_sw128(smem_u32(sb + C::offB));
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint64_t bdesc = bdesc0 + uint64_t((32 * j) >> 4);
+        for (int j = 0; j < C::kMmaK; ++j) {
+          const uint64_t bdesc = bdesc_s0 + soff + uint64_t((32 * j) >> 4);
           const uint32_t sfb = sfb_t + 4 * C::kRT * j;
           if (MODE == 0) {
-            const uint64_t adesc = desc_sw128(smem_u32(sb)) + uint64_t((32 * j) >> 4);
-            tc_mma_fp4(d_tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb, (kt | j) != 0);
+            const uint64_t adesc = adesc_s0 + soff + uint64_t((32 * j) >> 4);
+            tc_mma_fp4(tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb, (kt | j) != 0);
           } else {
 #pragma unroll
             for (int pl = 0; pl < 3; ++pl) {
-              const uint64_t adesc = desc_sw128(smem_u32(sb + pl * C::kA)) + uint64_t((32 * j) >> 4);
-              tc_mma_fp4(d_tmem, adesc, bdesc, idesc, tmem + C::kConstCol + 4 * pl, sfb, (kt | j | pl) != 0);
+              const uint64_t adesc = adesc_s0 + soff + uint64_t((pl * C::kA + 32 * j) >> 4);
+              tc_mma_fp4(tmem, adesc, bdesc, idesc, tmem + C::kConstCol + 4 * pl, sfb, (kt | j | pl) != 0);
             }
           }
         }
@@ -311,40 +330,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
-      tc_commit(tfull_bar(acc));
-      if (C::kNAcc == 2) { acc ^= 1; if (acc == 0) acc_phase ^= 1u; }
-      else acc_phase ^= 1u;
+      tc_commit(tfull_bar);
+      acc_phase ^= 1u;
     }
     // all MMAs issued by this thread complete before TMEM is released
     tc_commit(drain_bar);
     mbar_wait(drain_bar, 0, nullptr);
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;                      // TMEM lane quarter of this warp
+    const int q = warp & 3;                      // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;            // columns [128*half, 128*half + 128)
     const int row = q * 32 + lane;
-    int acc = 0;
     uint32_t acc_phase = 0;
     const float gw = *p.g_w;
     const float gscale = MODE == 0 ? __fmul_rn(*p.g_a, gw) : gw;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       const int mt = tile / p.NT, nt = tile - mt * p.NT;
-      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) { fail(); break; }
+      if (!mbar_wait(tfull_bar, acc_phase, abort_flag)) { fail(); break; }
       tc_fence_after();
+      uint32_t r0[32], r1[32], r2[32], r3[32];
+      const uint32_t taddr = tmem + uint32_t(half * 128) + (uint32_t(q * 32) << 16);
+      __syncwarp();
+      tmem_ld32(taddr, r0);
+      tmem_ld32(taddr + 32, r1);
+      tmem_ld32(taddr + 64, r2);
+      tmem_ld32(taddr + 96, r3);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(tempty_bar);                   // TMEM is free: the next tile's MMAs may start
+      acc_phase ^= 1u;
       const int m = mt * BM + row;
-      const bool row_ok = m < p.M;
-      const float scale = MODE == 0 ? gscale : (row_ok ? __fmul_rn(p.row_scale[m], gw) : 0.f);
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        __syncwarp();
-        tmem_ld32(tmem + uint32_t(acc * BN + c * 32) + (uint32_t(q * 32) << 16), r);
-        tmem_ld_wait();
-        const int n0 = nt * BN + c * 32;
-        if (!row_ok || n0 >= p.N) continue;
+      if (m >= p.M) continue;
+      const float scale = MODE == 0 ? gscale : __fmul_rn(p.row_scale[m], gw);
+      const int nbase = nt * BN + half * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t* rc = c == 0 ? r0 : (c == 1 ? r1 : (c == 2 ? r2 : r3));
+        const int n0 = nbase + c * 32;
+        if (n0 >= p.N) break;
+        const int cols = (p.N - n0) < 32 ? (p.N - n0) : 32;   // 16 or 32 (N % 16 == 0)
         float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(__uint_as_float(r[i]), scale);
-        const int cols = (p.N - n0) < 32 ? (p.N - n0) : 32;   // 16 or 32 (N % 16 == 0)
+        for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(__uint_as_float(rc[i]), scale);
         if (p.bias) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -397,10 +424,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
-      if (C::kNAcc == 2) { acc ^= 1; if (acc == 0) acc_phase ^= 1u; }
-      else acc_phase ^= 1u;
     }
   }
   tc_fence_before();
@@ -433,45 +456,46 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int MODE, int STAGES>
+template <int BN, int MODE, int STAGES, int KB>
 int run(const GemmCall& c, int num_sms, cudaStream_t s) {
-  using Cf = Cfg<BN, MODE, STAGES>;
+  using Cf = Cfg<BN, MODE, STAGES, KB>;
+  constexpr CUtensorMapSwizzle kSw = KB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   const int64_t kb = c.K / 2;                       // bytes of codes per row
   const int64_t natoms = c.K / 64;                  // 512-byte scale atoms per 128-row tile
   CUtensorMap tA, tB, tSA, tSB;
   bool ok = true;
   if (MODE == 0) {
     uint64_t d[2] = {uint64_t(kb), uint64_t(c.M)}, st[1] = {uint64_t(kb)};
-    uint32_t b[2] = {uint32_t(kKB), uint32_t(BM)};
-    ok &= make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.a, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    uint32_t b[2] = {uint32_t(KB), uint32_t(BM)};
+    ok &= make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.a, d, st, b, kSw);
     uint64_t d2[3] = {128, uint64_t(natoms), uint64_t(cdiv(c.M, 128))}, st2[2] = {512, uint64_t(natoms) * 512};
-    uint32_t b2[3] = {128, 4, 1};
+    uint32_t b2[3] = {128, uint32_t(Cf::kMmaK), 1};
     ok &= make_map(&tSA, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, c.a_sf, d2, st2, b2, CU_TENSOR_MAP_SWIZZLE_NONE);
   } else {
     uint64_t d[3] = {uint64_t(kb), uint64_t(c.M), 3}, st[2] = {uint64_t(kb), uint64_t(kb) * uint64_t(c.M)};
-    uint32_t b[3] = {uint32_t(kKB), uint32_t(BM), 1};
-    ok &= make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c.a, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    uint32_t b[3] = {uint32_t(KB), uint32_t(BM), 1};
+    ok &= make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c.a, d, st, b, kSw);
     tSA = tA;   // unused in mode 1
   }
   {
     uint64_t d[2] = {uint64_t(kb), uint64_t(c.N)}, st[1] = {uint64_t(kb)};
-    uint32_t b[2] = {uint32_t(kKB), uint32_t(BN)};
-    ok &= make_map(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.w, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    uint32_t b[2] = {uint32_t(KB), uint32_t(BN)};
+    ok &= make_map(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.w, d, st, b, kSw);
     uint64_t d2[3] = {128, uint64_t(natoms), uint64_t(cdiv(c.N, 128))}, st2[2] = {512, uint64_t(natoms) * 512};
-    uint32_t b2[3] = {128, 4, uint32_t(Cf::kRT)};
+    uint32_t b2[3] = {128, uint32_t(Cf::kMmaK), uint32_t(Cf::kRT)};
     ok &= make_map(&tSB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, c.w_sf, d2, st2, b2, CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   if (!ok) return kELaunch;
   Params p;
   p.M = int(c.M); p.N = int(c.N); p.K = int(c.K);
-  p.KT = int(cdiv(c.K, 256));
+  p.KT = int(cdiv(c.K / 2, KB));
   p.MT = int(cdiv(c.M, BM));
   p.NT = int(cdiv(c.N, BN));
   p.g_a = c.g_a; p.row_scale = c.row_scale; p.g_w = c.g_w;
   p.bias = static_cast<const uint16_t*>(c.bias);
   p.residual = static_cast<const uint16_t*>(c.residual);
   p.ldr = c.ldr; p.y = c.y; p.ldy = c.ldy; p.out_bf16 = c.out_bf16; p.gelu = c.gelu; p.pred = c.pred; p.err = c.err;
-  auto kern = gemm_fp4_kernel<BN, MODE, STAGES>;
+  auto kern = gemm_fp4_kernel<BN, MODE, STAGES, KB>;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cf::kSmem)) != cudaSuccess)
@@ -487,8 +511,10 @@ int run(const GemmCall& c, int num_sms, cudaStream_t s) {
 }  // namespace
 
 int launch_gemm_fp4(const GemmCall& c, int num_sms, cudaStream_t s) {
-  if (c.mode == 0) return run<128, 0, 5>(c, num_sms, s);
-  return run<128, 1, 3>(c, num_sms, s);
+  // Measured on GB300: W4A4 prefers 128-byte K steps (fewer, larger stages),
+  // W4A8 (three MMAs per stage already) prefers more, smaller stages.
+  if (c.mode == 0) return run<256, 0, 4, 128>(c, num_sms, s);
+  return run<256, 1, 5, 64>(c, num_sms, s);
 }
 
 }  // namespace sixbit

@@ -18,53 +18,84 @@ namespace {
 
 constexpr int kThreads = 256;
 
-template <typename T> struct In;
-template <> struct In<uint16_t> {   // bf16 bits
-  __device__ static void load8(const uint16_t* p, float* f) {
-    uint4 v = ldg_nc_v4(p);
-    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x); f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
-    f[4] = bf16lo(v.z); f[5] = bf16hi(v.z); f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
-  }
-};
-template <> struct In<float> {
-  __device__ static void load8(const float* p, float* f) {
-    uint4 a = ldg_nc_v4(p), b = ldg_nc_v4(p + 4);
-    f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y); f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
-    f[4] = __uint_as_float(b.x); f[5] = __uint_as_float(b.y); f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
-  }
-};
-
 // ---------------------------------------------------------------- amax (a1)
-// One warp per row: row max |x| (optional) and the tensor max via an atomic
-// max on the float bits (values are >= 0, so the bit order is the value order).
+// |x| maxima through bit patterns: for x >= 0 the IEEE bit order is the value
+// order, so |x| = bits & ~sign and the max is an unsigned max (two bf16 per
+// 32-bit word with a halfword max).  NaN inputs are not supported.
+__device__ __forceinline__ uint32_t absmax_word(uint32_t acc, uint32_t w, uint16_t) {
+  return __vmaxu2(acc, w & 0x7FFF7FFFu);
+}
+__device__ __forceinline__ uint32_t absmax_word(uint32_t acc, uint32_t w, float) {
+  return max(acc, w & 0x7FFFFFFFu);
+}
+__device__ __forceinline__ float absmax_value(uint32_t acc, uint16_t) {
+  return __uint_as_float(max(acc & 0xFFFFu, acc >> 16) << 16);
+}
+__device__ __forceinline__ float absmax_value(uint32_t acc, float) { return __uint_as_float(acc); }
+
+// Contiguous tensor: every thread keeps 8 independent 16-byte loads in
+// flight; one atomic max per CTA.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) amax_flat_kernel(const T* __restrict__ x, int64_t nvec16, float* amax_out) {
+  __shared__ uint32_t red[kThreads / 32];
+  constexpr int kU = 8;
+  uint32_t acc = 0;
+  const uint4* p = reinterpret_cast<const uint4*>(x);
+  const int64_t stride = int64_t(gridDim.x) * kThreads;
+  int64_t i = int64_t(blockIdx.x) * kThreads + threadIdx.x;
+  for (; i + (kU - 1) * stride < nvec16; i += kU * stride) {
+    uint4 v[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) v[u] = ldg_nc_v4(p + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      acc = absmax_word(acc, v[u].x, T()); acc = absmax_word(acc, v[u].y, T());
+      acc = absmax_word(acc, v[u].z, T()); acc = absmax_word(acc, v[u].w, T());
+    }
+  }
+  for (; i < nvec16; i += stride) {
+    const uint4 v = ldg_nc_v4(p + i);
+    acc = absmax_word(acc, v.x, T()); acc = absmax_word(acc, v.y, T());
+    acc = absmax_word(acc, v.z, T()); acc = absmax_word(acc, v.w, T());
+  }
+  float m = warp_max(absmax_value(acc, T()));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = __float_as_uint(m);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t b = 0;
+    for (int w = 0; w < kThreads / 32; ++w) b = max(b, red[w]);
+    atomic_max_nonneg(amax_out, __uint_as_float(b));
+  }
+}
+
+// Strided rows and/or per-row maxima: one warp per row, 8 vectors of 16
+// bytes per lane in flight.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) amax_rows_kernel(const T* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
                                                              float* amax_out, float* row_amax_out) {
+  constexpr int kE = 16 / sizeof(T);          // elements per 16-byte vector
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
+  const int64_t nvec = K / kE;
   float tmax = 0.f;
-  const int64_t nvec = K / 8;
   for (int64_t m = warp; m < M; m += nwarps) {
-    const T* row = x + m * ldx;
-    float rmax = 0.f;
-    int64_t j = lane;
-    for (; j + 96 < nvec; j += 128) {          // 4 vectors in flight per lane
-      float f[4][8];
+    const uint4* row = reinterpret_cast<const uint4*>(x + m * ldx);
+    uint32_t acc = 0;
+    for (int64_t j0 = 0; j0 < nvec; j0 += 8 * 32) {
+      uint4 v[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) In<T>::load8(row + (j + 32 * u) * 8, f[u]);
+      for (int u = 0; u < 8; ++u) {
+        const int64_t j = j0 + u * 32 + lane;
+        v[u] = j < nvec ? ldg_nc_v4(row + j) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) rmax = fmaxf(rmax, fabsf(f[u][e]));
+      for (int u = 0; u < 8; ++u) {
+        acc = absmax_word(acc, v[u].x, T()); acc = absmax_word(acc, v[u].y, T());
+        acc = absmax_word(acc, v[u].z, T()); acc = absmax_word(acc, v[u].w, T());
+      }
     }
-    for (; j < nvec; j += 32) {
-      float f[8];
-      In<T>::load8(row + j * 8, f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) rmax = fmaxf(rmax, fabsf(f[e]));
-    }
-    rmax = warp_max(rmax);
+    const float rmax = warp_max(absmax_value(acc, T()));
     if (row_amax_out && lane == 0) row_amax_out[m] = rmax;
     tmax = fmaxf(tmax, rmax);
   }
@@ -72,11 +103,32 @@ __global__ void __launch_bounds__(kThreads) amax_rows_kernel(const T* __restrict
 }
 
 // ------------------------------------------------------------ NVFP4 (a2/a4)
-// The tensor is walked as 64-element groups (4 scale blocks).  A warp takes
-// 4 groups per step: lanes 8j..8j+7 hold the 8 vectors of group j, a lane
-// pair holds one 16-element block.  Each lane writes its 8 codes as one
-// 32-bit word; lane 8j assembles the group's 4 scale bytes into one 32-bit
-// word of the swizzled scale buffer.
+// One warp per row.  A "chunk" is 256 consecutive elements: lane l holds
+// elements 8l..8l+7, a lane pair one 16-element scale block, lanes 8j..8j+7
+// one 64-element group (4 blocks).  Up to 8 chunks are loaded before any is
+// processed.  Each lane writes its 8 codes as one 32-bit word (128 bytes per
+// warp per chunk); lane 8j writes the group's 4 scale bytes as one 32-bit
+// word of the swizzled scale buffer.  Rows M..Mpad-1 get zero scales.
+template <typename T> struct Chunk;          // one lane's 8 elements of a 256-element chunk, raw
+template <> struct Chunk<uint16_t> {
+  uint4 v;
+  __device__ void load(const uint16_t* p) { v = ldg_nc_v4(p); }
+  __device__ void zero() { v = make_uint4(0, 0, 0, 0); }
+  __device__ void get(float* f) const {
+    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x); f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+    f[4] = bf16lo(v.z); f[5] = bf16hi(v.z); f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+  }
+};
+template <> struct Chunk<float> {
+  uint4 a, b;
+  __device__ void load(const float* p) { a = ldg_nc_v4(p); b = ldg_nc_v4(p + 4); }
+  __device__ void zero() { a = b = make_uint4(0, 0, 0, 0); }
+  __device__ void get(float* f) const {
+    f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y); f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
+    f[4] = __uint_as_float(b.x); f[5] = __uint_as_float(b.y); f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
+  }
+};
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(const T* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
                                                                const float* __restrict__ amax_ptr,
@@ -87,55 +139,48 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(const T* __restri
   const float g = (amax_t == 0.f) ? 1.f : __fdiv_rn(amax_t, 2688.f);
   if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
   const int lane = threadIdx.x & 31;
-  const int sub = lane >> 3, vec = lane & 7;
-  const int64_t gpr = K / 64;
-  const int64_t kc4 = K / 16;               // K % 64 == 0 -> already a multiple of 4
-  const int64_t total = Mpad * gpr;
+  const int64_t kc4 = K / 16;                 // K % 64 == 0 -> already a multiple of 4
+  const int nchunks = int((K + 255) / 256);
   const int64_t warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
-  constexpr int kU = 2;                     // warp steps unrolled (loads in flight)
-  for (int64_t G0 = warp * 4 * kU; G0 < total; G0 += nwarps * 4 * kU) {
-    float f[kU][8];
-    int64_t mm[kU], gg[kU];
+  for (int64_t m = warp; m < Mpad; m += nwarps) {
+    const bool row_ok = m < M;
+    const T* row = x + m * ldx;
+    for (int c0 = 0; c0 < nchunks; c0 += 8) {
+      Chunk<T> ch[8];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int64_t G = G0 + u * 4 + sub;
-      mm[u] = G / gpr;
-      gg[u] = G - mm[u] * gpr;
-      if (G < total && mm[u] < M) In<T>::load8(x + mm[u] * ldx + gg[u] * 64 + vec * 8, f[u]);
-      else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[u][e] = 0.f;
+      for (int u = 0; u < 8; ++u) {
+        const int64_t e0 = int64_t(c0 + u) * 256 + lane * 8;
+        if (row_ok && e0 < K) ch[u].load(row + e0);
+        else ch[u].zero();
       }
-    }
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int64_t G = G0 + u * 4 + sub;
-      float am = 0.f;
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u;
+        if (c >= nchunks) break;                // warp-uniform
+        const int64_t e0 = int64_t(c) * 256 + lane * 8;
+        float f[8];
+        ch[u].get(f);
+        float am = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(f[u][e]));
-      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));        // block of 16 = lane pair
-      const float s = (amax_t == 0.f) ? 0.f : __fdiv_rn(__fmul_rn(am, 448.f), amax_t);
-      const uint32_t sb = e4m3_encode(s);
-      const float d = __fmul_rn(e4m3_decode(sb), g);
-      uint32_t w = 0;
-      if (d != 0.f) {
-        const float r = __frcp_rn(d);
+        for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(f[e]));
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));      // 16-element block = lane pair
+        const float s = (amax_t == 0.f) ? 0.f : __fdiv_rn(__fmul_rn(am, 448.f), amax_t);
+        const uint32_t sb = e4m3_encode(s);
+        const float d = __fmul_rn(e4m3_decode(sb), g);
+        uint32_t w = 0;
+        if (d != 0.f) {
+          const float r = __frcp_rn(d);
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          w |= e2m1x2(__fmul_rn(f[u][2 * e], r), __fmul_rn(f[u][2 * e + 1], r)) << (8 * e);
-      }
-      // scale bytes of blocks 0..3 of this group live in lanes 8j, 8j+2, 8j+4, 8j+6
-      const uint32_t s0 = __shfl_sync(0xffffffffu, sb, (lane & ~7) + 0);
-      const uint32_t s1 = __shfl_sync(0xffffffffu, sb, (lane & ~7) + 2);
-      const uint32_t s2 = __shfl_sync(0xffffffffu, sb, (lane & ~7) + 4);
-      const uint32_t s3 = __shfl_sync(0xffffffffu, sb, (lane & ~7) + 6);
-      if (G < total) {
-        const int64_t m = mm[u], grp = gg[u];
-        if (m < M) *reinterpret_cast<uint32_t*>(codes + m * (K / 2) + grp * 32 + vec * 4) = w;
-        if (vec == 0) {
-          const uint32_t word = (m < M) ? (s0 | (s1 << 8) | (s2 << 16) | (s3 << 24)) : 0u;
-          *reinterpret_cast<uint32_t*>(sf + sf_offset(m, grp * 4, kc4)) = word;
+          for (int e = 0; e < 4; ++e)
+            w |= e2m1x2(__fmul_rn(f[2 * e], r), __fmul_rn(f[2 * e + 1], r)) << (8 * e);
+        }
+        // the group's 4 scale bytes sit in lanes 8j, 8j+2, 8j+4, 8j+6: gather them in lane 8j
+        uint32_t word = sb | (__shfl_down_sync(0xffffffffu, sb, 2) << 8);
+        word |= __shfl_down_sync(0xffffffffu, word, 4) << 16;
+        if (e0 < K) {
+          if (row_ok) *reinterpret_cast<uint32_t*>(codes + m * (K / 2) + e0 / 2) = w;
+          if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset(m, e0 / 16, kc4)) = row_ok ? word : 0u;
         }
       }
     }
@@ -148,77 +193,106 @@ __device__ __forceinline__ uint32_t digit_code(int d) {    // integer in [-4, 4]
   return mag | (d < 0 ? 8u : 0u);
 }
 
-// One warp per row.  Pass 1 finds the row amax (unless given); pass 2
-// re-reads the row (an L2 hit) and writes codes and/or digit planes.
-__global__ void __launch_bounds__(kThreads) int8_quant_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
-                                                              const float* __restrict__ row_amax_in,
-                                                              int8_t* __restrict__ q, uint8_t* __restrict__ planes,
-                                                              float* __restrict__ row_scale, const uint8_t* pred) {
+// Digit split of an INT8 code q in [-128, 127] (entry q & 0xFF):
+// byte 0 = E2M1 code of a, byte 1 = of b, byte 2 = of c, q = 64a + 8b + c,
+// c = q mod 8 in [-3, 4], b likewise for (q - c)/8, a the rest.
+__device__ __forceinline__ uint32_t digit_entry(int q) {
+  const int c = ((q + 3) & 7) - 3;
+  const int q1 = (q - c) >> 3;                 // exact: q - c is a multiple of 8
+  const int b = ((q1 + 3) & 7) - 3;
+  const int a = (q1 - b) >> 3;
+  return digit_code(a) | (digit_code(b) << 8) | (digit_code(c) << 16);
+}
+
+// WPR warps per row, NVL 16-byte vectors (8 bf16) per lane: the whole row
+// stays in registers between the amax reduction and the encode, so the input
+// is read from HBM once.  Vector v of the row sits in warp v / (32*NVL) of
+// the row's group, register slot (v / 32) % NVL, lane v % 32.  CTAs of 4
+// warps take 4 / WPR rows per step.
+// Encode: v = clamp(x * inv, +-127) rounded to nearest even by adding
+// 1.5 * 2^23 (the low byte of the sum's bits is then q as a two's complement
+// byte); the digit planes come from a 256-entry shared table.
+template <int NVL, int WPR>
+__global__ void __launch_bounds__(128) int8_quant_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
+                                                         const float* __restrict__ row_amax_in,
+                                                         int8_t* __restrict__ q, uint8_t* __restrict__ planes,
+                                                         float* __restrict__ row_scale, const uint8_t* pred) {
   if (pred && *pred == 0) return;
-  const int lane = threadIdx.x & 31;
-  const int64_t warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-  const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
+  constexpr int RPC = 4 / WPR;
+  __shared__ float red[4];
+  __shared__ uint32_t lut[256];
+  for (int i = threadIdx.x; i < 256; i += 128) lut[i] = digit_entry(int(int8_t(uint8_t(i))));
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rloc = warp / WPR, wpart = warp % WPR;
   const int64_t nvec = K / 8;
   const int64_t plane_stride = M * (K / 2);
-  for (int64_t m = warp; m < M; m += nwarps) {
+  constexpr float kMagic = 12582912.0f;        // 1.5 * 2^23
+  for (int64_t m0 = int64_t(blockIdx.x) * RPC; m0 < M; m0 += int64_t(gridDim.x) * RPC) {
+    const int64_t m = m0 + rloc;
+    const bool row_ok = m < M;
     const uint16_t* row = x + m * ldx;
+    uint4 v[NVL];
+#pragma unroll
+    for (int i = 0; i < NVL; ++i) {
+      const int64_t vi = int64_t(wpart * NVL + i) * 32 + lane;
+      v[i] = (row_ok && vi < nvec) ? ldg_nc_v4(row + vi * 8) : make_uint4(0, 0, 0, 0);
+    }
     float amax;
     if (row_amax_in) {
-      amax = row_amax_in[m];
+      amax = row_ok ? row_amax_in[m] : 0.f;
     } else {
-      float rmax = 0.f;
-      int64_t j = lane;
-      for (; j + 96 < nvec; j += 128) {
-        float f[4][8];
+      uint32_t acc = 0;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) In<uint16_t>::load8(row + (j + 32 * u) * 8, f[u]);
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) rmax = fmaxf(rmax, fabsf(f[u][e]));
+      for (int i = 0; i < NVL; ++i) {
+        acc = __vmaxu2(acc, v[i].x & 0x7FFF7FFFu); acc = __vmaxu2(acc, v[i].y & 0x7FFF7FFFu);
+        acc = __vmaxu2(acc, v[i].z & 0x7FFF7FFFu); acc = __vmaxu2(acc, v[i].w & 0x7FFF7FFFu);
       }
-      for (; j < nvec; j += 32) {
-        float f[8];
-        In<uint16_t>::load8(row + j * 8, f);
+      amax = warp_max(__uint_as_float(max(acc & 0xFFFFu, acc >> 16) << 16));
+      if (WPR > 1) {
+        if (lane == 0) red[warp] = amax;
+        __syncthreads();
 #pragma unroll
-        for (int e = 0; e < 8; ++e) rmax = fmaxf(rmax, fabsf(f[e]));
+        for (int w = 0; w < WPR; ++w) amax = fmaxf(amax, red[rloc * WPR + w]);
+        __syncthreads();
       }
-      amax = warp_max(rmax);
     }
+    if (!row_ok) continue;                     // uniform per row group (after the barriers)
     const bool nz = amax > 0.f;
     const float inv = nz ? __fdiv_rn(127.f, amax) : 0.f;
-    if (lane == 0) row_scale[m] = nz ? __fdiv_rn(amax, 127.f) : 0.f;
-    for (int64_t j = lane; j < nvec; j += 32) {
-      float f[8];
-      In<uint16_t>::load8(row + j * 8, f);
-      int qi[8];
+    if (lane == 0 && wpart == 0) row_scale[m] = nz ? __fdiv_rn(amax, 127.f) : 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        int v = __float2int_rn(__fmul_rn(f[e], inv));
-        qi[e] = nz ? max(-127, min(127, v)) : 0;
+    for (int i = 0; i < NVL; ++i) {
+      const int64_t vi = int64_t(wpart * NVL + i) * 32 + lane;
+      if (vi >= nvec) continue;
+      const uint32_t* pw = &v[i].x;
+      uint32_t qb[8];                          // bits of (v + magic): low byte = q
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float lo = fminf(fmaxf(__fmul_rn(bf16lo(pw[e]), inv), -127.f), 127.f);
+        const float hi = fminf(fmaxf(__fmul_rn(bf16hi(pw[e]), inv), -127.f), 127.f);
+        qb[2 * e] = __float_as_uint(__fadd_rn(lo, kMagic));
+        qb[2 * e + 1] = __float_as_uint(__fadd_rn(hi, kMagic));
       }
       if (q) {
         uint2 w;
-        w.x = (qi[0] & 0xFF) | ((qi[1] & 0xFF) << 8) | ((qi[2] & 0xFF) << 16) | (uint32_t(qi[3] & 0xFF) << 24);
-        w.y = (qi[4] & 0xFF) | ((qi[5] & 0xFF) << 8) | ((qi[6] & 0xFF) << 16) | (uint32_t(qi[7] & 0xFF) << 24);
-        *reinterpret_cast<uint2*>(q + m * K + j * 8) = w;
+        w.x = __byte_perm(__byte_perm(qb[0], qb[1], 0x0040), __byte_perm(qb[2], qb[3], 0x0040), 0x5410);
+        w.y = __byte_perm(__byte_perm(qb[4], qb[5], 0x0040), __byte_perm(qb[6], qb[7], 0x0040), 0x5410);
+        *reinterpret_cast<uint2*>(q + m * K + vi * 8) = w;
       }
       if (planes) {
-        uint32_t pa = 0, pb = 0, pc = 0;
+        // pair elements (2j, 2j+1): byte k of p[j] = digit-k codes, low nibble element 2j
+        uint32_t p[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int c = ((qi[e] + 3) & 7) - 3;          // q mod 8 in [-3, 4]
-          const int q1 = (qi[e] - c) >> 3;              // exact: q - c is a multiple of 8
-          const int b = ((q1 + 3) & 7) - 3;
-          const int a = (q1 - b) >> 3;                  // in [-2, 2]
-          pa |= digit_code(a) << (4 * e);
-          pb |= digit_code(b) << (4 * e);
-          pc |= digit_code(c) << (4 * e);
-        }
-        uint8_t* base = planes + m * (K / 2) + j * 4;
-        *reinterpret_cast<uint32_t*>(base) = pa;
-        *reinterpret_cast<uint32_t*>(base + plane_stride) = pb;
-        *reinterpret_cast<uint32_t*>(base + 2 * plane_stride) = pc;
+        for (int j = 0; j < 4; ++j) p[j] = lut[qb[2 * j] & 0xFFu] | (lut[qb[2 * j + 1] & 0xFFu] << 4);
+        const uint32_t x01 = __byte_perm(p[0], p[1], 0x5140);   // a01 a23 b01 b23
+        const uint32_t x23 = __byte_perm(p[2], p[3], 0x5140);   // a45 a67 b45 b67
+        const uint32_t c01 = __byte_perm(p[0], p[1], 0x0062);   // c01 c23
+        const uint32_t c23 = __byte_perm(p[2], p[3], 0x0062);   // c45 c67
+        uint8_t* base = planes + m * (K / 2) + vi * 4;
+        *reinterpret_cast<uint32_t*>(base) = __byte_perm(x01, x23, 0x5410);
+        *reinterpret_cast<uint32_t*>(base + plane_stride) = __byte_perm(x01, x23, 0x7632);
+        *reinterpret_cast<uint32_t*>(base + 2 * plane_stride) = __byte_perm(c01, c23, 0x5410);
       }
     }
   }
@@ -235,19 +309,29 @@ int grid_for(int64_t work_items, int per_block, int num_sms, int waves = 8) {
 int launch_amax(const void* x, int dtype, int64_t M, int64_t K, int64_t ldx, float* amax_out, float* row_amax_out,
                 int num_sms, cudaStream_t s) {
   if (amax_out && cudaMemsetAsync(amax_out, 0, sizeof(float), s) != cudaSuccess) return kELaunch;
-  const int grid = grid_for(M, kThreads / 32, num_sms);
-  if (dtype == 1)
-    amax_rows_kernel<uint16_t><<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), M, K, ldx, amax_out, row_amax_out);
-  else
-    amax_rows_kernel<float><<<grid, kThreads, 0, s>>>(static_cast<const float*>(x), M, K, ldx, amax_out, row_amax_out);
+  const int esz = dtype == 1 ? 2 : 4;
+  const bool flat = !row_amax_out && ldx == K && (M * K * esz) % 16 == 0;
+  if (flat) {
+    const int64_t nvec16 = M * K * esz / 16;
+    const int grid = grid_for(nvec16, kThreads * 8, num_sms, 8);
+    if (dtype == 1)
+      amax_flat_kernel<uint16_t><<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), nvec16, amax_out);
+    else
+      amax_flat_kernel<float><<<grid, kThreads, 0, s>>>(static_cast<const float*>(x), nvec16, amax_out);
+  } else {
+    const int grid = grid_for(M, kThreads / 32, num_sms, 16);
+    if (dtype == 1)
+      amax_rows_kernel<uint16_t><<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), M, K, ldx, amax_out, row_amax_out);
+    else
+      amax_rows_kernel<float><<<grid, kThreads, 0, s>>>(static_cast<const float*>(x), M, K, ldx, amax_out, row_amax_out);
+  }
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 
 int launch_nvfp4_quant(const void* x, int dtype, int64_t M, int64_t K, int64_t ldx, const float* amax,
                        uint8_t* codes, uint8_t* sf, float* g_out, const uint8_t* pred, int num_sms, cudaStream_t s) {
   const int64_t Mpad = cdiv(M, 128) * 128;
-  const int64_t warps_needed = cdiv(Mpad * (K / 64), 8);
-  const int grid = grid_for(warps_needed, kThreads / 32, num_sms);
+  const int grid = grid_for(Mpad, kThreads / 32, num_sms, 16);
   if (dtype == 1)
     nvfp4_quant_kernel<uint16_t><<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), M, K, ldx, amax, codes, sf,
                                                            g_out, pred, Mpad);
@@ -259,9 +343,17 @@ int launch_nvfp4_quant(const void* x, int dtype, int64_t M, int64_t K, int64_t l
 
 int launch_int8_quant(const void* x, int64_t M, int64_t K, int64_t ldx, const float* row_amax_in, int8_t* q,
                       uint8_t* planes, float* row_scale, const uint8_t* pred, int num_sms, cudaStream_t s) {
-  const int grid = grid_for(M, kThreads / 32, num_sms);
-  int8_quant_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), M, K, ldx, row_amax_in, q, planes,
-                                              row_scale, pred);
+  auto xs = static_cast<const uint16_t*>(x);
+  // rows per CTA step = 4 / warps-per-row
+  if (K <= 2048) {
+    int8_quant_kernel<8, 1><<<grid_for(M, 4, num_sms, 16), 128, 0, s>>>(xs, M, K, ldx, row_amax_in, q, planes, row_scale, pred);
+  } else if (K <= 4096) {
+    int8_quant_kernel<16, 1><<<grid_for(M, 4, num_sms, 12), 128, 0, s>>>(xs, M, K, ldx, row_amax_in, q, planes, row_scale, pred);
+  } else if (K <= 8192) {
+    int8_quant_kernel<16, 2><<<grid_for(M, 2, num_sms, 12), 128, 0, s>>>(xs, M, K, ldx, row_amax_in, q, planes, row_scale, pred);
+  } else {
+    int8_quant_kernel<16, 4><<<grid_for(M, 1, num_sms, 12), 128, 0, s>>>(xs, M, K, ldx, row_amax_in, q, planes, row_scale, pred);
+  }
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 

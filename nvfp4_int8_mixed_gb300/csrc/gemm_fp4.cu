@@ -41,17 +41,29 @@ constexpr int kEpiThreads = 256;
 constexpr uint32_t kSpinCap = 1u << 22;  // polls of a bounded mbarrier wait
 constexpr uint32_t kTmemCols = 512;
 
-template <int BN, int MODE, int STAGES, int KB>
+#ifndef W4A4_NC
+#define W4A4_NC 2        // chunks of 64 bytes per stage (128 K elements)
+#define W4A4_STAGES 4
+#endif
+#ifndef W4A8_NC
+#define W4A8_NC 1
+#define W4A8_STAGES 5
+#endif
+
+template <int BN, int MODE, int STAGES, int KB, int NC>
 struct Cfg {
   static_assert(BN == 256, "epilogue assumes 256-column tiles");
-  static_assert(KB == 64 || KB == 128, "K step of 64 or 128 bytes per row");
-  static constexpr int kMmaK = KB / 32;                    // MMAs (K = 64 elements) per stage
+  static_assert(KB == 64 || KB == 128, "K chunk of 64 or 128 bytes per row");
+  static constexpr int kMmaK = KB / 32;                    // MMAs (K = 64 elements) per chunk
+  static constexpr int kAtoms = kMmaK * NC;                // 512-byte scale atoms per 128 rows per stage
   static constexpr int kPlanes = MODE == 0 ? 1 : 3;
   static constexpr int kRT = BN / 128;                     // 128-row scale tiles of W per N tile
-  static constexpr int kA = BM * KB;                       // one A plane tile
-  static constexpr int kB = BN * KB;
-  static constexpr int kSFA = MODE == 0 ? 512 * kMmaK : 0; // one 512-byte atom per MMA
-  static constexpr int kSFB = 512 * kMmaK * kRT;
+  static constexpr int kChunkA = BM * KB;                  // one chunk of one A plane
+  static constexpr int kChunkB = BN * KB;
+  static constexpr int kA = kChunkA * NC;                  // one A plane, all chunks of a stage
+  static constexpr int kB = kChunkB * NC;
+  static constexpr int kSFA = MODE == 0 ? 512 * kAtoms : 0;
+  static constexpr int kSFB = 512 * kAtoms * kRT;
   static constexpr int offB = kPlanes * kA;
   static constexpr int offSFA = offB + kB;
   static constexpr int offSFB = offSFA + kSFA;
@@ -60,8 +72,8 @@ struct Cfg {
   static constexpr uint32_t kTx = kStage;                  // bytes landed per stage
   // TMEM columns: accumulator [0, BN), then per-stage scale columns, then
   // the three constant digit-scale atoms (mode 1).
-  static constexpr int kSfaCols = MODE == 0 ? 4 * kMmaK : 0;
-  static constexpr int kSfStride = kSfaCols + 4 * kMmaK * kRT;
+  static constexpr int kSfaCols = MODE == 0 ? 4 * kAtoms : 0;
+  static constexpr int kSfStride = kSfaCols + 4 * kAtoms * kRT;
   static constexpr int kSfBase = BN;
   static constexpr int kConstCol = kSfBase + STAGES * kSfStride;
   static_assert(kConstCol + 12 <= int(kTmemCols), "TMEM budget");
@@ -111,6 +123,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm,
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
           dst),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, int c2, int c3,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
@@ -186,16 +206,17 @@ struct Params {
   void* y;
   int64_t ldy;
   int out_bf16, gelu;
+  int chunked;               // 1: K chunk maps (one op per operand per stage); 0: 2-D maps, one chunk per stage
   const uint8_t* pred;
   int* err;
 };
 
-template <int BN, int MODE, int STAGES, int KB>
+template <int BN, int MODE, int STAGES, int KB, int NC>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                     const Params p) {
-  using C = Cfg<BN, MODE, STAGES, KB>;
+  using C = Cfg<BN, MODE, STAGES, KB, NC>;
   if (p.pred && *p.pred == 0) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -261,15 +282,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* sb = smem + size_t(stage) * C::kStage;
         const uint32_t fb = full_bar(stage);
         mbar_expect_tx(fb, C::kTx);
-        if (MODE == 0) {
-          tma_load_2d(smem_u32(sb), &tmA, kt * KB, mt * BM, fb);
-          tma_load_3d(smem_u32(sb + C::offSFA), &tmSFA, 0, kt * C::kMmaK, mt, fb);
+        if (p.chunked) {
+          // one op per operand: NC chunks of KB bytes (and all three planes in mode 1)
+          if (MODE == 0) tma_load_3d(smem_u32(sb), &tmA, 0, mt * BM, kt * NC, fb);
+          else tma_load_4d(smem_u32(sb), &tmA, 0, mt * BM, kt * NC, 0, fb);
+          tma_load_3d(smem_u32(sb + C::offB), &tmB, 0, nt * BN, kt * NC, fb);
         } else {
+          if (MODE == 0) {
+            tma_load_2d(smem_u32(sb), &tmA, kt * KB, mt * BM, fb);
+          } else {
 #pragma unroll
-          for (int pl = 0; pl < 3; ++pl) tma_load_3d(smem_u32(sb + pl * C::kA), &tmA, kt * KB, mt * BM, pl, fb);
+            for (int pl = 0; pl < 3; ++pl) tma_load_3d(smem_u32(sb + pl * C::kA), &tmA, kt * KB, mt * BM, pl, fb);
+          }
+          tma_load_2d(smem_u32(sb + C::offB), &tmB, kt * KB, nt * BN, fb);
         }
-        tma_load_2d(smem_u32(sb + C::offB), &tmB, kt * KB, nt * BN, fb);
-        tma_load_3d(smem_u32(sb + C::offSFB), &tmSFB, 0, kt * C::kMmaK, nt * C::kRT, fb);
+        if (MODE == 0) tma_load_3d(smem_u32(sb + C::offSFA), &tmSFA, 0, kt * C::kAtoms, mt, fb);
+        tma_load_3d(smem_u32(sb + C::offSFB), &tmSFB, 0, kt * C::kAtoms, nt * C::kRT, fb);
         issued |= 1u << stage;
         last_par = (last_par & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -305,24 +333,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sfa_t = tmem + uint32_t(C::kSfBase + stage * C::kSfStride);
         const uint32_t sfb_t = sfa_t + uint32_t(C::kSfaCols);
 #pragma unroll
-        for (int j = 0; j < C::kMmaK; ++j) {
-          if (MODE == 0) tc_cp_sf(sfa_t + 4 * j, sfa_s0 + soff + uint64_t((512 * j) >> 4));
+        for (int a = 0; a < C::kAtoms; ++a) {
+          if (MODE == 0) tc_cp_sf(sfa_t + 4 * a, sfa_s0 + soff + uint64_t((512 * a) >> 4));
 #pragma unroll
           for (int r = 0; r < C::kRT; ++r)
-            tc_cp_sf(sfb_t + 4 * (C::kRT * j + r), sfb_s0 + soff + uint64_t((512 * (C::kMmaK * r + j)) >> 4));
+            tc_cp_sf(sfb_t + 4 * (C::kRT * a + r), sfb_s0 + soff + uint64_t((512 * (C::kAtoms * r + a)) >> 4));
         }
 #pragma unroll
-        for (int j = 0; j < C::kMmaK; ++j) {
-          const uint64_t bdesc = bdesc_s0 + soff + uint64_t((32 * j) >> 4);
-          const uint32_t sfb = sfb_t + 4 * C::kRT * j;
-          if (MODE == 0) {
-            const uint64_t adesc = adesc_s0 + soff + uint64_t((32 * j) >> 4);
-            tc_mma_fp4(tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb, (kt | j) != 0);
-          } else {
+        for (int c = 0; c < NC; ++c) {
 #pragma unroll
-            for (int pl = 0; pl < 3; ++pl) {
-              const uint64_t adesc = adesc_s0 + soff + uint64_t((pl * C::kA + 32 * j) >> 4);
-              tc_mma_fp4(tmem, adesc, bdesc, idesc, tmem + C::kConstCol + 4 * pl, sfb, (kt | j | pl) != 0);
+          for (int j = 0; j < C::kMmaK; ++j) {
+            const int a = c * C::kMmaK + j;            // MMA index within the stage = scale atom index
+            const uint64_t bdesc = bdesc_s0 + soff + uint64_t((c * C::kChunkB + 32 * j) >> 4);
+            const uint32_t sfb = sfb_t + 4 * C::kRT * a;
+            if (MODE == 0) {
+              const uint64_t adesc = adesc_s0 + soff + uint64_t((c * C::kChunkA + 32 * j) >> 4);
+              tc_mma_fp4(tmem, adesc, bdesc, idesc, sfa_t + 4 * a, sfb, (kt | a) != 0);
+            } else {
+#pragma unroll
+              for (int pl = 0; pl < 3; ++pl) {
+                const uint64_t adesc = adesc_s0 + soff + uint64_t((pl * C::kA + c * C::kChunkA + 32 * j) >> 4);
+                tc_mma_fp4(tmem, adesc, bdesc, idesc, tmem + C::kConstCol + 4 * pl, sfb, (kt | a | pl) != 0);
+              }
             }
           }
         }
@@ -451,51 +483,78 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base
               const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle sw) {
   auto fn = encode_fn();
   if (!fn) return false;
-  uint32_t es[3] = {1, 1, 1};
+  uint32_t es[5] = {1, 1, 1, 1, 1};   // one per dimension, up to rank 5
   return fn(m, dt, rank, const_cast<void*>(base), dims, strides_bytes, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int MODE, int STAGES, int KB>
+template <int BN, int MODE, int STAGES, int KB, int NC>
 int run(const GemmCall& c, int num_sms, cudaStream_t s) {
-  using Cf = Cfg<BN, MODE, STAGES, KB>;
+  using Cf = Cfg<BN, MODE, STAGES, KB, NC>;
   constexpr CUtensorMapSwizzle kSw = KB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   const int64_t kb = c.K / 2;                       // bytes of codes per row
   const int64_t natoms = c.K / 64;                  // 512-byte scale atoms per 128-row tile
+  // Chunked maps view each row as K/2/KB chunks of KB bytes (chunk index is
+  // the outer box dimension, so a box lands as NC consecutive [rows][KB]
+  // tiles); this needs KB to divide K/2, else a chunk would run into the
+  // next row instead of reading the zero fill.
+  const bool chunked = kb % KB == 0;
+  if (!chunked && NC != 1) return kEShape;
+  const int64_t nch = kb / KB;
   CUtensorMap tA, tB, tSA, tSB;
   bool ok = true;
   if (MODE == 0) {
-    uint64_t d[2] = {uint64_t(kb), uint64_t(c.M)}, st[1] = {uint64_t(kb)};
-    uint32_t b[2] = {uint32_t(KB), uint32_t(BM)};
-    ok &= make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.a, d, st, b, kSw);
+    if (chunked) {
+      uint64_t d[3] = {uint64_t(KB), uint64_t(c.M), uint64_t(nch)}, st[2] = {uint64_t(kb), uint64_t(KB)};
+      uint32_t b[3] = {uint32_t(KB), uint32_t(BM), uint32_t(NC)};
+      ok &= make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c.a, d, st, b, kSw);
+    } else {
+      uint64_t d[2] = {uint64_t(kb), uint64_t(c.M)}, st[1] = {uint64_t(kb)};
+      uint32_t b[2] = {uint32_t(KB), uint32_t(BM)};
+      ok &= make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.a, d, st, b, kSw);
+    }
     uint64_t d2[3] = {128, uint64_t(natoms), uint64_t(cdiv(c.M, 128))}, st2[2] = {512, uint64_t(natoms) * 512};
-    uint32_t b2[3] = {128, uint32_t(Cf::kMmaK), 1};
+    uint32_t b2[3] = {128, uint32_t(Cf::kAtoms), 1};
     ok &= make_map(&tSA, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, c.a_sf, d2, st2, b2, CU_TENSOR_MAP_SWIZZLE_NONE);
   } else {
-    uint64_t d[3] = {uint64_t(kb), uint64_t(c.M), 3}, st[2] = {uint64_t(kb), uint64_t(kb) * uint64_t(c.M)};
-    uint32_t b[3] = {uint32_t(KB), uint32_t(BM), 1};
-    ok &= make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c.a, d, st, b, kSw);
+    if (chunked) {
+      uint64_t d[4] = {uint64_t(KB), uint64_t(c.M), uint64_t(nch), 3};
+      uint64_t st[3] = {uint64_t(kb), uint64_t(KB), uint64_t(kb) * uint64_t(c.M)};
+      uint32_t b[4] = {uint32_t(KB), uint32_t(BM), uint32_t(NC), 3};
+      ok &= make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, c.a, d, st, b, kSw);
+    } else {
+      uint64_t d[3] = {uint64_t(kb), uint64_t(c.M), 3}, st[2] = {uint64_t(kb), uint64_t(kb) * uint64_t(c.M)};
+      uint32_t b[3] = {uint32_t(KB), uint32_t(BM), 1};
+      ok &= make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c.a, d, st, b, kSw);
+    }
     tSA = tA;   // unused in mode 1
   }
-  {
+  if (chunked) {
+    uint64_t d[3] = {uint64_t(KB), uint64_t(c.N), uint64_t(nch)}, st[2] = {uint64_t(kb), uint64_t(KB)};
+    uint32_t b[3] = {uint32_t(KB), uint32_t(BN), uint32_t(NC)};
+    ok &= make_map(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c.w, d, st, b, kSw);
+  } else {
     uint64_t d[2] = {uint64_t(kb), uint64_t(c.N)}, st[1] = {uint64_t(kb)};
     uint32_t b[2] = {uint32_t(KB), uint32_t(BN)};
     ok &= make_map(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.w, d, st, b, kSw);
+  }
+  {
     uint64_t d2[3] = {128, uint64_t(natoms), uint64_t(cdiv(c.N, 128))}, st2[2] = {512, uint64_t(natoms) * 512};
-    uint32_t b2[3] = {128, uint32_t(Cf::kMmaK), uint32_t(Cf::kRT)};
+    uint32_t b2[3] = {128, uint32_t(Cf::kAtoms), uint32_t(Cf::kRT)};
     ok &= make_map(&tSB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, c.w_sf, d2, st2, b2, CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   if (!ok) return kELaunch;
   Params p;
   p.M = int(c.M); p.N = int(c.N); p.K = int(c.K);
-  p.KT = int(cdiv(c.K / 2, KB));
+  p.KT = int(chunked ? cdiv(nch, NC) : cdiv(kb, KB));
   p.MT = int(cdiv(c.M, BM));
   p.NT = int(cdiv(c.N, BN));
   p.g_a = c.g_a; p.row_scale = c.row_scale; p.g_w = c.g_w;
   p.bias = static_cast<const uint16_t*>(c.bias);
   p.residual = static_cast<const uint16_t*>(c.residual);
   p.ldr = c.ldr; p.y = c.y; p.ldy = c.ldy; p.out_bf16 = c.out_bf16; p.gelu = c.gelu; p.pred = c.pred; p.err = c.err;
-  auto kern = gemm_fp4_kernel<BN, MODE, STAGES, KB>;
+  p.chunked = chunked ? 1 : 0;
+  auto kern = gemm_fp4_kernel<BN, MODE, STAGES, KB, NC>;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cf::kSmem)) != cudaSuccess)
@@ -513,8 +572,12 @@ int run(const GemmCall& c, int num_sms, cudaStream_t s) {
 int launch_gemm_fp4(const GemmCall& c, int num_sms, cudaStream_t s) {
   // Measured on GB300: W4A4 prefers 128-byte K steps (fewer, larger stages),
   // W4A8 (three MMAs per stage already) prefers more, smaller stages.
-  if (c.mode == 0) return run<256, 0, 4, 128>(c, num_sms, s);
-  return run<256, 1, 5, 64>(c, num_sms, s);
+  // K % 128 == 0: chunked maps, several 64-byte chunks per stage, one TMA
+  // op per operand (the per-op cost, not bandwidth, bounded smaller stages).
+  // Otherwise one chunk per stage through 2-D maps.
+  const bool chunked = (c.K / 2) % 64 == 0;
+  if (c.mode == 0) return chunked ? run<256, 0, W4A4_STAGES, 64, W4A4_NC>(c, num_sms, s) : run<256, 0, 4, 128, 1>(c, num_sms, s);
+  return chunked ? run<256, 1, W4A8_STAGES, 64, W4A8_NC>(c, num_sms, s) : run<256, 1, 5, 64, 1>(c, num_sms, s);
 }
 
 }  // namespace sixbit

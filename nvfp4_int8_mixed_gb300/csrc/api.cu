@@ -70,7 +70,7 @@ int sixbit_amax_bf16(const void* x, int64_t M, int64_t K, int64_t ldx, float* am
   int sms;
   if (device_setup(&sms, nullptr) != kOk) return kELaunch;
   if (M == 0) return amax_out ? (cudaMemsetAsync(amax_out, 0, 4, cs(stream)) == cudaSuccess ? kOk : kELaunch) : kOk;
-  return launch_amax(x, SIXBIT_BF16, M, K, ldx, amax_out, row_amax_out, sms, cs(stream));
+  return launch_amax(x, SIXBIT_BF16, M, K, ldx, amax_out, row_amax_out, nullptr, sms, cs(stream));
 }
 
 int sixbit_quantize_act_nvfp4(const void* x, int64_t M, int64_t K, int64_t ldx, const float* amax_in, uint8_t* codes,
@@ -84,7 +84,7 @@ int sixbit_quantize_act_nvfp4(const void* x, int64_t M, int64_t K, int64_t ldx, 
   const float* amax = amax_in;
   if (!amax) {
     float* wamax = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsAmaxOffset);
-    int rc = launch_amax(x, SIXBIT_BF16, M, K, ldx, wamax, nullptr, sms, cs(stream));
+    int rc = launch_amax(x, SIXBIT_BF16, M, K, ldx, wamax, nullptr, pred, sms, cs(stream));
     if (rc != kOk) return rc;
     amax = wamax;
   }
@@ -100,7 +100,7 @@ int sixbit_quantize_weight_nvfp4(const void* w, int dtype, int64_t N, int64_t K,
   int sms;
   if (device_setup(&sms, nullptr) != kOk) return kELaunch;
   float* wamax = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsAmaxOffset);
-  int rc = launch_amax(w, dtype, N, K, K, wamax, nullptr, sms, cs(stream));
+  int rc = launch_amax(w, dtype, N, K, K, wamax, nullptr, nullptr, sms, cs(stream));
   if (rc != kOk) return rc;
   return launch_nvfp4_quant(w, dtype, N, K, K, wamax, codes, sf, g_out, nullptr, sms, cs(stream));
 }

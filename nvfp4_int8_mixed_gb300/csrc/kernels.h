@@ -7,7 +7,7 @@
 namespace sixbit {
 
 int launch_amax(const void* x, int dtype, int64_t M, int64_t K, int64_t ldx, float* amax_out, float* row_amax_out,
-                int num_sms, cudaStream_t s);
+                const uint8_t* pred, int num_sms, cudaStream_t s);
 int launch_nvfp4_quant(const void* x, int dtype, int64_t M, int64_t K, int64_t ldx, const float* amax,
                        uint8_t* codes, uint8_t* sf, float* g_out, const uint8_t* pred, int num_sms, cudaStream_t s);
 int launch_int8_quant(const void* x, int64_t M, int64_t K, int64_t ldx, const float* row_amax_in, int8_t* q,

@@ -36,7 +36,9 @@ __device__ __forceinline__ float absmax_value(uint32_t acc, float) { return __ui
 // Contiguous tensor: every thread keeps 8 independent 16-byte loads in
 // flight; one atomic max per CTA.
 template <typename T>
-__global__ void __launch_bounds__(kThreads) amax_flat_kernel(const T* __restrict__ x, int64_t nvec16, float* amax_out) {
+__global__ void __launch_bounds__(kThreads) amax_flat_kernel(const T* __restrict__ x, int64_t nvec16, float* amax_out,
+                                                             const uint8_t* pred) {
+  if (pred && *pred == 0) return;
   __shared__ uint32_t red[kThreads / 32];
   constexpr int kU = 8;
   uint32_t acc = 0;
@@ -72,7 +74,8 @@ __global__ void __launch_bounds__(kThreads) amax_flat_kernel(const T* __restrict
 // bytes per lane in flight.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) amax_rows_kernel(const T* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
-                                                             float* amax_out, float* row_amax_out) {
+                                                             float* amax_out, float* row_amax_out, const uint8_t* pred) {
+  if (pred && *pred == 0) return;
   constexpr int kE = 16 / sizeof(T);          // elements per 16-byte vector
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
@@ -307,7 +310,7 @@ int grid_for(int64_t work_items, int per_block, int num_sms, int waves = 8) {
 }  // namespace
 
 int launch_amax(const void* x, int dtype, int64_t M, int64_t K, int64_t ldx, float* amax_out, float* row_amax_out,
-                int num_sms, cudaStream_t s) {
+                const uint8_t* pred, int num_sms, cudaStream_t s) {
   if (amax_out && cudaMemsetAsync(amax_out, 0, sizeof(float), s) != cudaSuccess) return kELaunch;
   const int esz = dtype == 1 ? 2 : 4;
   const bool flat = !row_amax_out && ldx == K && (M * K * esz) % 16 == 0;
@@ -315,15 +318,15 @@ int launch_amax(const void* x, int dtype, int64_t M, int64_t K, int64_t ldx, flo
     const int64_t nvec16 = M * K * esz / 16;
     const int grid = grid_for(nvec16, kThreads * 8, num_sms, 8);
     if (dtype == 1)
-      amax_flat_kernel<uint16_t><<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), nvec16, amax_out);
+      amax_flat_kernel<uint16_t><<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), nvec16, amax_out, pred);
     else
-      amax_flat_kernel<float><<<grid, kThreads, 0, s>>>(static_cast<const float*>(x), nvec16, amax_out);
+      amax_flat_kernel<float><<<grid, kThreads, 0, s>>>(static_cast<const float*>(x), nvec16, amax_out, pred);
   } else {
     const int grid = grid_for(M, kThreads / 32, num_sms, 16);
     if (dtype == 1)
-      amax_rows_kernel<uint16_t><<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), M, K, ldx, amax_out, row_amax_out);
+      amax_rows_kernel<uint16_t><<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), M, K, ldx, amax_out, row_amax_out, pred);
     else
-      amax_rows_kernel<float><<<grid, kThreads, 0, s>>>(static_cast<const float*>(x), M, K, ldx, amax_out, row_amax_out);
+      amax_rows_kernel<float><<<grid, kThreads, 0, s>>>(static_cast<const float*>(x), M, K, ldx, amax_out, row_amax_out, pred);
   }
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }

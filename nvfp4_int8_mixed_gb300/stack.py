@@ -1,0 +1,189 @@
+"""Synthetic DiT block stack driven through the sixbit C ABI, with DMPQ and TDC.
+
+Block (the linear layers of a video-DiT block; token mixing omitted):
+    h1 = LN(x); qkv = QL(h1); x1 = x + QL(qkv[:, 2H:3H]); h2 = LN(x1);
+    u = GELU(QL(h2)); out = x1 + QL(u)
+QL quantizes its input to NVFP4 (W4A4) or INT8 (W4A8) as the layer's DMPQ
+flag says.  6Bit-Diffusion (thelatestinai.com page, Figure 2): DMPQ picks
+each layer's activation bits from the block's Gamma at the previous step;
+TDC skips a block whose update barely changed and reuses in + Delta.
+
+Every decision stays on the device.  At the start of a step DMPQ writes one
+gate byte per (layer, format); the TDC kernel of a block clears the block's
+gates when it skips it; every kernel of the block reads its gate (`pred`)
+and exits at once when it is 0.  One step is captured once as a CUDA graph
+and replayed; only the block-0 input and the step counter are written
+between replays.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import (block_gamma, dmpq_assign, layernorm, qlinear_w4a4, qlinear_w4a8, quantize_act_int8,
+               quantize_act_nvfp4, quantize_weight_nvfp4, sf_bytes, tdc_decide_and_apply)
+
+LN_EPS = 1e-5
+LAYERS = ("qkv", "out", "up", "down")
+
+
+class DiTStack:
+    """n_blocks blocks of hidden size H and FFN size F over M tokens.
+
+    weights: list (per block) of dicts qkv [3H,H], out [H,H], up [F,H], down [H,F]
+    (float32 numpy or torch); alpha, beta: per-layer predictor lines (4 per
+    block, layer order qkv, out, up, down); tau: DMPQ threshold; tau_tdc,
+    max_skip: TDC rule (max_skip = 0 disables skipping).
+    """
+
+    def __init__(self, weights, alpha, beta, M: int, H: int, F: int, tau: float, tau_tdc: float = 0.05,
+                 max_skip: int = 1, device=None):
+        self.dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        dev = self.dev
+        self.nb, self.M, self.H, self.F = len(weights), M, H, F
+        self.tau, self.tau_tdc, self.max_skip = float(tau), float(tau_tdc), int(max_skip)
+        nl = 4 * self.nb
+        to_t = lambda a: torch.as_tensor(np.asarray(a, np.float32)).to(dev)
+        self.alpha, self.beta = to_t(alpha), to_t(beta)
+        self.layer_block = torch.arange(self.nb, dtype=torch.int32, device=dev).repeat_interleave(4)
+        self.wq = []
+        for b in weights:
+            self.wq.append({k: quantize_weight_nvfp4(torch.as_tensor(b[k]).to(dev, torch.float32).contiguous())
+                            for k in LAYERS})
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.x_in = torch.zeros((M, H), **bf)
+        self.buf = [torch.zeros((M, H), **bf), torch.zeros((M, H), **bf)]
+        self.h1 = torch.empty((M, H), **bf)
+        self.qkv = torch.empty((M, 3 * H), **bf)
+        self.x1 = torch.empty((M, H), **bf)
+        self.h2 = torch.empty((M, H), **bf)
+        self.u = torch.empty((M, F), **bf)
+        kmax = max(H, F)
+        self.codes = torch.empty(M * kmax // 2, dtype=torch.uint8, device=dev)
+        self.sf = torch.empty(sf_bytes(M, kmax), dtype=torch.uint8, device=dev)
+        self.g = torch.empty(1, dtype=torch.float32, device=dev)
+        self.planes = torch.empty(3 * M * kmax // 2, dtype=torch.uint8, device=dev)
+        self.rs = torch.empty(M, dtype=torch.float32, device=dev)
+        self.amax = torch.empty(1, dtype=torch.float32, device=dev)
+        self.row_amax = torch.empty(M, dtype=torch.float32, device=dev)
+        # decisions and TDC cache
+        self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.use_nvfp4 = torch.zeros(nl, dtype=torch.uint8, device=dev)
+        self.gates = torch.zeros((nl, 2), dtype=torch.uint8, device=dev)
+        self.gamma = torch.zeros(self.nb, dtype=torch.float32, device=dev)
+        self.delta = [torch.zeros((M, H), **bf) for _ in range(self.nb)]
+        self.r2 = torch.full((self.nb,), float("inf"), dtype=torch.float32, device=dev)
+        self.state = torch.zeros((self.nb, 2), dtype=torch.int32, device=dev)
+        self.cflag = torch.ones(self.nb, dtype=torch.uint8, device=dev)
+        self.graph = None
+        self.out = self.buf[(self.nb - 1) % 2]
+
+    # ------------------------------------------------------------ one step
+    def _ql(self, x, wq, gate_nv, gate_i8, out, amax_in=None, row_amax_in=None, residual=None, gelu=False):
+        M, K = x.shape
+        codes = self.codes[:M * K // 2].view(M, K // 2)
+        sf = self.sf[:sf_bytes(M, K)]
+        planes = self.planes[:3 * M * K // 2].view(3, M, K // 2)
+        quantize_act_nvfp4(x, amax_in=amax_in, pred=gate_nv, out=(codes, sf, self.g))
+        qlinear_w4a4(codes, sf, self.g, *wq, residual=residual, gelu=gelu, out=out, pred=gate_nv)
+        quantize_act_int8(x, row_amax=row_amax_in, want_q=False, pred=gate_i8, out=(None, planes, self.rs))
+        qlinear_w4a8(planes, self.rs, *wq, residual=residual, gelu=gelu, out=out, pred=gate_i8)
+
+    def enqueue_step(self):
+        """Enqueue one denoising step on the current stream (graph-capturable)."""
+        H = self.H
+        dmpq_assign(self.gamma, self.alpha, self.beta, self.layer_block, self.tau, self.step_dev,
+                    use_nvfp4=self.use_nvfp4, gates=self.gates)
+        h = self.x_in
+        for l in range(self.nb):
+            out = self.buf[l % 2]
+            gates = self.gates[4 * l:4 * l + 4]
+            c = self.cflag[l:l + 1]
+            tdc_decide_and_apply(h, self.delta[l], self.r2[l:l + 1], self.tau_tdc, self.max_skip, self.state[l],
+                                 c, out, gates=gates)
+            g = lambda i, f: gates[i, f:f + 1]
+            layernorm(h, LN_EPS, out=self.h1, amax_out=self.amax, row_amax_out=self.row_amax, pred=c)
+            self._ql(self.h1, self.wq[l]["qkv"], g(0, 0), g(0, 1), self.qkv, amax_in=self.amax,
+                     row_amax_in=self.row_amax)
+            v = self.qkv[:, 2 * H:3 * H]
+            self._ql(v, self.wq[l]["out"], g(1, 0), g(1, 1), self.x1, residual=h)
+            layernorm(self.x1, LN_EPS, out=self.h2, amax_out=self.amax, row_amax_out=self.row_amax, pred=c)
+            self._ql(self.h2, self.wq[l]["up"], g(2, 0), g(2, 1), self.u, amax_in=self.amax,
+                     row_amax_in=self.row_amax, gelu=True)
+            self._ql(self.u, self.wq[l]["down"], g(3, 0), g(3, 1), out, residual=self.x1)
+            block_gamma(h, out, delta=self.delta[l], gamma_out=self.gamma[l:l + 1], r2_out=self.r2[l:l + 1],
+                        tdc_state=self.state[l], computed=c)
+            h = out
+        self.out = h
+
+    def capture(self):
+        """Warm up once (kernel attributes, scratch) and capture one step as a CUDA graph."""
+        snap = self._snapshot()
+        self.enqueue_step()
+        torch.cuda.synchronize()
+        self._restore(snap)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.enqueue_step()
+        torch.cuda.synchronize()
+
+    def _snapshot(self):
+        return [t.clone() for t in (self.gamma, self.r2, self.state, self.cflag, self.use_nvfp4, self.gates)] + \
+               [d.clone() for d in self.delta]
+
+    def _restore(self, snap):
+        for t, s in zip((self.gamma, self.r2, self.state, self.cflag, self.use_nvfp4, self.gates), snap[:6]):
+            t.copy_(s)
+        for d, s in zip(self.delta, snap[6:]):
+            d.copy_(s)
+
+    def reset(self):
+        self.gamma.zero_()
+        self.r2.fill_(float("inf"))
+        self.state.zero_()
+        self.cflag.fill_(1)
+        self.use_nvfp4.zero_()
+        self.gates.zero_()
+        for d in self.delta:
+            d.zero_()
+
+    def run(self, xs, record=False):
+        """Run every step with block-0 inputs xs (list of bf16 [M,H] device tensors).
+
+        Returns the last block's output of every step (clones) and, with
+        record=True, per-step decisions: flags [steps, layers], skips
+        [steps, blocks], gamma, r2 and the TDC counters after the step.
+        """
+        if self.graph is None:
+            self.capture()
+        outs, log = [], dict(flags=[], skips=[], gamma=[], r2=[], state=[])
+        for t, x in enumerate(xs):
+            self.x_in.copy_(x)
+            self.step_dev.fill_(t)
+            self.graph.replay()
+            outs.append(self.out.clone())
+            if record:
+                log["flags"].append(self.use_nvfp4.clone())
+                log["skips"].append(1 - self.cflag)
+                log["gamma"].append(self.gamma.clone())
+                log["r2"].append(self.r2.clone())
+                log["state"].append(self.state.clone())
+        return outs, log
+
+
+def calibrate_tau(stack: DiTStack, xs, frac: float = 0.6) -> float:
+    """DMPQ threshold from an all-INT8 run: the `frac` quantile of the
+    predictions alpha * Gamma_{t-1} + beta over (layer, step >= 1)."""
+    tau0, tdc0 = stack.tau, stack.max_skip
+    stack.tau, stack.max_skip = float("-inf"), 0
+    stack.graph = None
+    stack.reset()
+    _, log = stack.run(xs, record=True)
+    g = torch.stack(log["gamma"][:-1]).cpu().numpy()                # Gamma_{t-1} for t = 1..T-1
+    lb = stack.layer_block.cpu().numpy()
+    a, b = stack.alpha.cpu().numpy(), stack.beta.cpu().numpy()
+    p = (a[None, :] * g[:, lb]).astype(np.float32) + b[None, :]
+    stack.tau, stack.max_skip = tau0, tdc0
+    stack.graph = None
+    stack.reset()
+    return float(np.float32(np.quantile(p.astype(np.float64), frac)))

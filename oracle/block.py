@@ -70,11 +70,12 @@ def block_forward(x_bits, wq_block, flags):
 
 
 def run_stack(x_steps, wq_blocks, alpha, beta, tau, tau_tdc, max_skip=1, use_tdc=True,
-              forced_flags=None):
+              forced_flags=None, forced_skips=None):
     """Run every step.  Returns dict(outputs, flags[t], skips[t], gammas[t], r2[t]).
 
-    forced_flags (optional) [steps][layers] replaces DMPQ's decisions
-    (teacher forcing for parity checks of a free-running device stack).
+    forced_flags (optional) [steps][layers] replaces DMPQ's decisions and
+    forced_skips (optional) [steps][blocks] replaces TDC's (teacher forcing
+    for parity checks of a free-running device stack).
     """
     nb = len(wq_blocks)
     layer_block = np.repeat(np.arange(nb), 4)
@@ -91,7 +92,10 @@ def run_stack(x_steps, wq_blocks, alpha, beta, tau, tau_tdc, max_skip=1, use_tdc
         h = x
         for l in range(nb):
             c = caches[l]
-            skip = use_tdc and tdc.decide(c, tau_tdc, max_skip)
+            if forced_skips is not None:
+                skip = bool(forced_skips[t][l])
+            else:
+                skip = use_tdc and tdc.decide(c, tau_tdc, max_skip)
             if skip:
                 out = tdc.apply(h, c.delta)
                 tdc.after_skip(c)

@@ -1,0 +1,80 @@
+"""GPU parity of the DiT block stack with DMPQ and TDC (reduced config-4
+shape) against the oracle.
+
+Decisions are checked as decisions: the device's DMPQ flags must equal the
+oracle's rule applied to the device's own Gamma of the previous step, and
+its TDC skips the oracle's rule applied to the device's counters and r2.
+Outputs are compared against the oracle run under the same decisions
+(teacher forcing): relative L2 <= 2e-3 per step."""
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+from oracle import block as o_block, codecs, dmpq as o_dmpq, tdc as o_tdc
+from tests.helpers import dev_bf16, host, host_bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(tau_tdc, max_skip, nb=3, M=300, H=256, F=512, steps=6, seed=7):
+    from nvfp4_int8_mixed_gb300.stack import DiTStack, calibrate_tau
+    st = synthetic.stack_setup(seed, nb, H, F)
+    xs = synthetic.stack_inputs(st["noise_seed"], M, H, steps)
+    xs_dev = [dev_bf16(x) for x in xs]
+    stack = DiTStack(st["blocks"], st["alpha"], st["beta"], M, H, F, tau=0.0, tau_tdc=tau_tdc, max_skip=max_skip)
+    tau = calibrate_tau(stack, xs_dev)
+    stack.tau = tau
+    outs, log = stack.run(xs_dev, record=True)
+    torch.cuda.synchronize()
+    rec = {k: [host(v) for v in vs] for k, vs in log.items()}
+    return st, xs, tau, [host_bf16_bits(o) for o in outs], rec
+
+
+@pytest.mark.parametrize("tau_tdc,max_skip", [(0.0, 1), (10.0, 1), (0.05, 1)])
+def test_stack_decisions_and_outputs(tau_tdc, max_skip):
+    st, xs, tau, outs, rec = _run(tau_tdc, max_skip)
+    nb = len(st["blocks"])
+    lb = np.repeat(np.arange(nb), 4)
+    steps = len(xs)
+    # DMPQ: the device's flags follow the rule on the device's previous Gamma
+    for t in range(steps):
+        g_prev = rec["gamma"][t - 1] if t > 0 else np.zeros(nb, np.float32)
+        ref = o_dmpq.assign(g_prev, st["alpha"], st["beta"], lb, np.float32(tau), t)
+        assert np.array_equal(rec["flags"][t], ref), t
+    # TDC: the device's skips follow the rule on its counters after the previous step
+    for t in range(steps):
+        for l in range(nb):
+            if t == 0:
+                want = False
+            else:
+                c = o_tdc.BlockCache(fresh_count=int(rec["state"][t - 1][l, 0]), consec=int(rec["state"][t - 1][l, 1]),
+                                     r2=np.float32(rec["r2"][t - 1][l]))
+                want = o_tdc.decide(c, tau_tdc, max_skip)
+            assert bool(rec["skips"][t][l]) == want, (t, l)
+    # outputs under the same decisions
+    wq = [{k: o_block.quantize_weights(v) for k, v in b.items()} for b in st["blocks"]]
+    ref = o_block.run_stack(xs, wq, st["alpha"], st["beta"], tau, tau_tdc, max_skip,
+                            forced_flags=rec["flags"], forced_skips=rec["skips"])
+    for t in range(steps):
+        g = codecs.bf16_to_f32(outs[t]).astype(np.float64)
+        r = codecs.bf16_to_f32(ref["outputs"][t]).astype(np.float64)
+        rel = np.linalg.norm(g - r) / np.linalg.norm(r)
+        assert rel <= 2e-3, (t, rel)
+        assert np.allclose(rec["gamma"][t], ref["gammas"][t], rtol=2e-3, atol=0), t
+    flags = np.array(rec["flags"][1:])
+    assert flags.any() and not flags.all()          # a real NVFP4 / INT8 mix after step 0
+    skips = np.array(rec["skips"])
+    if tau_tdc == 0.0:
+        assert not skips.any()
+    if tau_tdc == 10.0:
+        assert skips.any()
+
+
+def test_stack_graph_replay_is_deterministic():
+    _, _, _, outs1, rec1 = _run(10.0, 1, steps=4)
+    _, _, _, outs2, rec2 = _run(10.0, 1, steps=4)
+    for a, b in zip(outs1, outs2):
+        assert np.array_equal(a, b)
+    for a, b in zip(rec1["gamma"], rec2["gamma"]):
+        assert np.array_equal(a, b)

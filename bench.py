@@ -227,6 +227,81 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- DiT stack
+STACKS = {
+    "2b": dict(n_blocks=30, M=synthetic.M_2B, H=1920, F=7680, steps=50, seed=3),
+    "5b": dict(n_blocks=42, M=2 * synthetic.M_2B, H=3072, F=12288, steps=50, seed=4),   # CFG batch 2
+}
+
+
+def run_stack_bench(name: str, dev):
+    """Blocks/s of the synthetic DiT stack with DMPQ+TDC and with DMPQ only.
+
+    Weights N(0, 0.02) and the input drift x_t = x_{t-1} + sigma_t N(0,1)
+    (sigma 0.3 -> 0.01) are drawn on the device from a seeded torch
+    generator; (alpha, beta) ~ U(0.5,1.5) x U(0,0.01) per layer; tau is
+    calibrated for ~60% NVFP4 from an all-INT8 run; TDC threshold 0.05,
+    max_skip 1.  Timed: every step's graph replay plus its input copy."""
+    import torch
+    from nvfp4_int8_mixed_gb300.stack import DiTStack, calibrate_tau
+    c = STACKS[name]
+    nb, M, H, F, T = c["n_blocks"], c["M"], c["H"], c["F"], c["steps"]
+    gen = torch.Generator(device=dev).manual_seed(c["seed"])
+    weights = []
+    for _ in range(nb):
+        weights.append({k: (torch.randn(shape, generator=gen, device=dev) * 0.02)
+                        for k, shape in (("qkv", (3 * H, H)), ("out", (H, H)), ("up", (F, H)), ("down", (H, F)))})
+    rng = np.random.default_rng(c["seed"])
+    alpha = rng.uniform(0.5, 1.5, 4 * nb).astype(np.float32)
+    beta = rng.uniform(0.0, 0.01, 4 * nb).astype(np.float32)
+    x = torch.randn((M, H), generator=gen, device=dev)
+    xs = [x.to(torch.bfloat16)]
+    for t in range(1, T):
+        x = x + synthetic.drift_sigma(t, T) * torch.randn((M, H), generator=gen, device=dev)
+        xs.append(x.to(torch.bfloat16))
+    del x
+    stack = DiTStack(weights, alpha, beta, M, H, F, tau=0.0, tau_tdc=0.05, max_skip=1, device=dev)
+    del weights
+    torch.cuda.synchronize()
+    tau = calibrate_tau(stack, xs)
+    res = {"config": f"{nb} blocks, M={M}, H={H}, F={F}, {T} steps", "tau": tau}
+    for mode, max_skip in (("dmpq_tdc", 1), ("dmpq_only", 0)):
+        stack.tau, stack.max_skip = tau, max_skip
+        stack.graph = None
+        stack.reset()
+        stack.capture()
+        stack.reset()
+        skips = torch.zeros(nb, dtype=torch.int32, device=dev)
+        nv = torch.zeros(4 * nb, dtype=torch.int32, device=dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for t in range(T):
+            stack.x_in.copy_(xs[t])
+            stack.step_dev.fill_(t)
+            stack.graph.replay()
+            skips += (1 - stack.cflag).int()
+            nv += stack.use_nvfp4.int()
+        e1.record()
+        torch.cuda.synchronize()
+        sec = e0.elapsed_time(e1) / 1e3
+        res[mode] = {"blocks_per_s": nb * T / sec, "ms_per_step": sec / T * 1e3,
+                     "skipped_fraction": float(skips.sum()) / (nb * T),
+                     "nvfp4_fraction_after_step0": float(nv.sum()) / (4 * nb * (T - 1))}
+    # HBM footprint of the quantized stack vs a bf16 one (weights, TDC cache, block activations)
+    w_params = nb * (3 * H * H + H * H + 2 * F * H)
+    w_nvfp4 = sum(int(t.numel() * t.element_size()) for b in stack.wq for wl in b.values() for t in wl)
+    act = sum(int(t.numel() * t.element_size()) for t in (stack.x_in, *stack.buf, stack.h1, stack.qkv, stack.x1,
+                                                         stack.h2, stack.u, stack.codes, stack.sf, stack.planes))
+    cache = sum(int(d.numel() * d.element_size()) for d in stack.delta)
+    res["footprint_bytes"] = {"weights_nvfp4": w_nvfp4, "weights_bf16": 2 * w_params, "activations": act,
+                              "tdc_cache": cache,
+                              "weights_ratio_bf16_over_nvfp4": 2 * w_params / w_nvfp4}
+    del stack, xs
+    torch.cuda.empty_cache()
+    return res
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args):
     import torch
@@ -434,6 +509,10 @@ def run_ours(args):
     tf = {n: {"ms": mean_t[n] * 1e3, "TFLOP/s": flops_layer[[l["name"] for l in L].index(n.split("[")[1][:-1])]
                     / mean_t[n] / 1e12} for n in gemm_names}
 
+    stack_res = None
+    if rank == 0 and args.stack != "none":
+        stack_res = run_stack_bench(args.stack, dev)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         rows, cols = 64, 512
@@ -455,6 +534,7 @@ def run_ours(args):
                         "d2h_bytes_per_step": int(d2h)},
                 "gpu_launches": launches_per_step * args.steps,
                 "clocks": clocks, "roofline": roofline, "cpu_baseline": cpu,
+                "dit_stack": stack_res,
                 "per_kernel": {"gemm": tf, "bandwidth": bw, "dmpq_ms": mean_t["dmpq"] * 1e3,
                                "tdc_ms": mean_t["tdc"] * 1e3}}
         print(json.dumps(line), flush=True)
@@ -470,6 +550,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["2b", "5b"], default="2b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stack", choices=["2b", "5b", "none"], default="2b",
+                    help="DiT block stack measured after the GEMM-set step (blocks/s with DMPQ+TDC)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -9,6 +9,8 @@
 // All kernels are HBM-bound streaming passes: 16-byte vector loads issued
 // several at a time per thread, coalesced across the warp, grids sized as a
 // multiple of the SM count.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -112,24 +114,49 @@ __global__ void __launch_bounds__(kThreads) amax_rows_kernel(const T* __restrict
 // processed.  Each lane writes its 8 codes as one 32-bit word (128 bytes per
 // warp per chunk); lane 8j writes the group's 4 scale bytes as one 32-bit
 // word of the swizzled scale buffer.  Rows M..Mpad-1 get zero scales.
-template <typename T> struct Chunk;          // one lane's 8 elements of a 256-element chunk, raw
-template <> struct Chunk<uint16_t> {
-  uint4 v;
-  __device__ void load(const uint16_t* p) { v = ldg_nc_v4(p); }
-  __device__ void zero() { v = make_uint4(0, 0, 0, 0); }
-  __device__ void get(float* f) const {
-    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x); f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
-    f[4] = bf16lo(v.z); f[5] = bf16hi(v.z); f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+// One lane owns one 16-element scale block: the block amax, the E4M3 scale,
+// the reciprocal and the 16 codes are computed once per block (no lane pair
+// repeating the scale arithmetic).  A warp covers 32 consecutive blocks
+// (512 elements) of a row per step and keeps two steps of loads in flight.
+template <typename T> struct Block16;           // the raw 16 elements of one block
+template <> struct Block16<uint16_t> {
+  uint4 v[2];
+  __device__ void load(const uint16_t* p) { v[0] = ldg_v4(p); v[1] = ldg_v4(p + 8); }
+  __device__ void zero() { v[0] = v[1] = make_uint4(0, 0, 0, 0); }
+  __device__ float amax() const {
+    uint32_t a = 0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      a = __vmaxu2(a, v[i].x & 0x7FFF7FFFu); a = __vmaxu2(a, v[i].y & 0x7FFF7FFFu);
+      a = __vmaxu2(a, v[i].z & 0x7FFF7FFFu); a = __vmaxu2(a, v[i].w & 0x7FFF7FFFu);
+    }
+    return __uint_as_float(max(a & 0xFFFFu, a >> 16) << 16);
+  }
+  __device__ float at(int i) const {               // element i (compile-time i after unrolling)
+    const uint32_t* w = &v[i >> 3].x;
+    return (i & 1) ? bf16hi(w[(i & 7) >> 1]) : bf16lo(w[(i & 7) >> 1]);
   }
 };
-template <> struct Chunk<float> {
-  uint4 a, b;
-  __device__ void load(const float* p) { a = ldg_nc_v4(p); b = ldg_nc_v4(p + 4); }
-  __device__ void zero() { a = b = make_uint4(0, 0, 0, 0); }
-  __device__ void get(float* f) const {
-    f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y); f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
-    f[4] = __uint_as_float(b.x); f[5] = __uint_as_float(b.y); f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
+template <> struct Block16<float> {
+  uint4 v[4];
+  __device__ void load(const float* p) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = ldg_v4(p + 4 * i);
   }
+  __device__ void zero() {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = make_uint4(0, 0, 0, 0);
+  }
+  __device__ float amax() const {
+    uint32_t a = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      a = max(a, v[i].x & 0x7FFFFFFFu); a = max(a, v[i].y & 0x7FFFFFFFu);
+      a = max(a, v[i].z & 0x7FFFFFFFu); a = max(a, v[i].w & 0x7FFFFFFFu);
+    }
+    return __uint_as_float(a);
+  }
+  __device__ float at(int i) const { return __uint_as_float((&v[i >> 2].x)[i & 3]); }
 };
 
 template <typename T>
@@ -142,48 +169,46 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(const T* __restri
   const float g = (amax_t == 0.f) ? 1.f : __fdiv_rn(amax_t, 2688.f);
   if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
   const int lane = threadIdx.x & 31;
-  const int64_t kc4 = K / 16;                 // K % 64 == 0 -> already a multiple of 4
-  const int nchunks = int((K + 255) / 256);
+  const int64_t kc4 = K / 16;                 // K % 64 == 0 -> a multiple of 4
+  const int nblk = int(K / 16);
+  const int nspan = (nblk + 31) / 32;
   const int64_t warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
+  constexpr int kU = 2;
   for (int64_t m = warp; m < Mpad; m += nwarps) {
     const bool row_ok = m < M;
     const T* row = x + m * ldx;
-    for (int c0 = 0; c0 < nchunks; c0 += 8) {
-      Chunk<T> ch[8];
+    for (int sp0 = 0; sp0 < nspan; sp0 += kU) {
+      Block16<T> blk[kU];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int64_t e0 = int64_t(c0 + u) * 256 + lane * 8;
-        if (row_ok && e0 < K) ch[u].load(row + e0);
-        else ch[u].zero();
+      for (int u = 0; u < kU; ++u) {
+        const int b = (sp0 + u) * 32 + lane;
+        if (row_ok && b < nblk) blk[u].load(row + int64_t(b) * 16);
+        else blk[u].zero();
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int c = c0 + u;
-        if (c >= nchunks) break;                // warp-uniform
-        const int64_t e0 = int64_t(c) * 256 + lane * 8;
-        float f[8];
-        ch[u].get(f);
-        float am = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(f[e]));
-        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));      // 16-element block = lane pair
+      for (int u = 0; u < kU; ++u) {
+        if (sp0 + u >= nspan) break;          // warp-uniform
+        const int b = (sp0 + u) * 32 + lane;
+        const float am = blk[u].amax();
         const float s = (amax_t == 0.f) ? 0.f : __fdiv_rn(__fmul_rn(am, 448.f), amax_t);
         const uint32_t sb = e4m3_encode(s);
         const float d = __fmul_rn(e4m3_decode(sb), g);
-        uint32_t w = 0;
+        uint32_t w0 = 0, w1 = 0;
         if (d != 0.f) {
           const float r = __frcp_rn(d);
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w |= e2m1x2(__fmul_rn(f[2 * e], r), __fmul_rn(f[2 * e + 1], r)) << (8 * e);
+          for (int e = 0; e < 4; ++e) {
+            w0 |= e2m1x2(__fmul_rn(blk[u].at(2 * e), r), __fmul_rn(blk[u].at(2 * e + 1), r)) << (8 * e);
+            w1 |= e2m1x2(__fmul_rn(blk[u].at(8 + 2 * e), r), __fmul_rn(blk[u].at(9 + 2 * e), r)) << (8 * e);
+          }
         }
-        // the group's 4 scale bytes sit in lanes 8j, 8j+2, 8j+4, 8j+6: gather them in lane 8j
-        uint32_t word = sb | (__shfl_down_sync(0xffffffffu, sb, 2) << 8);
-        word |= __shfl_down_sync(0xffffffffu, word, 4) << 16;
-        if (e0 < K) {
-          if (row_ok) *reinterpret_cast<uint32_t*>(codes + m * (K / 2) + e0 / 2) = w;
-          if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset(m, e0 / 16, kc4)) = row_ok ? word : 0u;
+        // 4 consecutive blocks (lanes 4j..4j+3) form one 32-bit word of the swizzled scale buffer
+        uint32_t word = sb | (__shfl_down_sync(0xffffffffu, sb, 1) << 8);
+        word |= __shfl_down_sync(0xffffffffu, word, 2) << 16;
+        if (b < nblk) {
+          if (row_ok) *reinterpret_cast<uint2*>(codes + m * (K / 2) + int64_t(b) * 8) = make_uint2(w0, w1);
+          if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset(m, b, kc4)) = row_ok ? word : 0u;
         }
       }
     }
@@ -215,7 +240,10 @@ __device__ __forceinline__ uint32_t digit_entry(int q) {
 // Encode: v = clamp(x * inv, +-127) rounded to nearest even by adding
 // 1.5 * 2^23 (the low byte of the sum's bits is then q as a two's complement
 // byte); the digit planes come from a 256-entry shared table.
-template <int NVL, int WPR>
+// kClamp: a caller-given row amax may be below the true one, so x * inv is
+// clamped to +-127; with the kernel's own amax |x * inv| already rounds to
+// at most 127 and the clamp is skipped.
+template <int NVL, int WPR, bool kClamp>
 __global__ void __launch_bounds__(128) int8_quant_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
                                                          const float* __restrict__ row_amax_in,
                                                          int8_t* __restrict__ q, uint8_t* __restrict__ planes,
@@ -272,8 +300,11 @@ __global__ void __launch_bounds__(128) int8_quant_kernel(const uint16_t* __restr
       uint32_t qb[8];                          // bits of (v + magic): low byte = q
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float lo = fminf(fmaxf(__fmul_rn(bf16lo(pw[e]), inv), -127.f), 127.f);
-        const float hi = fminf(fmaxf(__fmul_rn(bf16hi(pw[e]), inv), -127.f), 127.f);
+        float lo = __fmul_rn(bf16lo(pw[e]), inv), hi = __fmul_rn(bf16hi(pw[e]), inv);
+        if (kClamp) {
+          lo = fminf(fmaxf(lo, -127.f), 127.f);
+          hi = fminf(fmaxf(hi, -127.f), 127.f);
+        }
         qb[2 * e] = __float_as_uint(__fadd_rn(lo, kMagic));
         qb[2 * e + 1] = __float_as_uint(__fadd_rn(hi, kMagic));
       }
@@ -348,15 +379,19 @@ int launch_int8_quant(const void* x, int64_t M, int64_t K, int64_t ldx, const fl
                       uint8_t* planes, float* row_scale, const uint8_t* pred, int num_sms, cudaStream_t s) {
   auto xs = static_cast<const uint16_t*>(x);
   // rows per CTA step = 4 / warps-per-row
-  if (K <= 2048) {
-    int8_quant_kernel<8, 1><<<grid_for(M, 4, num_sms, 16), 128, 0, s>>>(xs, M, K, ldx, row_amax_in, q, planes, row_scale, pred);
-  } else if (K <= 4096) {
-    int8_quant_kernel<16, 1><<<grid_for(M, 4, num_sms, 12), 128, 0, s>>>(xs, M, K, ldx, row_amax_in, q, planes, row_scale, pred);
-  } else if (K <= 8192) {
-    int8_quant_kernel<16, 2><<<grid_for(M, 2, num_sms, 12), 128, 0, s>>>(xs, M, K, ldx, row_amax_in, q, planes, row_scale, pred);
-  } else {
-    int8_quant_kernel<16, 4><<<grid_for(M, 1, num_sms, 12), 128, 0, s>>>(xs, M, K, ldx, row_amax_in, q, planes, row_scale, pred);
-  }
+  auto go = [&](auto clamp) {
+    constexpr bool C = decltype(clamp)::value;
+    if (K <= 2048)
+      int8_quant_kernel<8, 1, C><<<grid_for(M, 4, num_sms, 16), 128, 0, s>>>(xs, M, K, ldx, row_amax_in, q, planes, row_scale, pred);
+    else if (K <= 4096)
+      int8_quant_kernel<8, 2, C><<<grid_for(M, 2, num_sms, 16), 128, 0, s>>>(xs, M, K, ldx, row_amax_in, q, planes, row_scale, pred);
+    else if (K <= 8192)
+      int8_quant_kernel<8, 4, C><<<grid_for(M, 1, num_sms, 16), 128, 0, s>>>(xs, M, K, ldx, row_amax_in, q, planes, row_scale, pred);
+    else
+      int8_quant_kernel<16, 4, C><<<grid_for(M, 1, num_sms, 12), 128, 0, s>>>(xs, M, K, ldx, row_amax_in, q, planes, row_scale, pred);
+  };
+  if (row_amax_in) go(std::true_type{});
+  else go(std::false_type{});
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 

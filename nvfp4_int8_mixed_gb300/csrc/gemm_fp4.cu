@@ -12,18 +12,29 @@
 //                 no tcgen05 int8 kind, and its warp-level int8 MMA runs at
 //                 ~150 TOP/s, far below the FP4 pipe.)
 //
-// Structure: persistent, warp-specialized CTA of 10 warps over 128 x 256
+// Structure: persistent, warp-specialized CTA of 16 warps over 128 x 256
 // output tiles, K in steps of KB bytes of codes per row (2*KB elements):
 //   warp 0      TMA producer: A/B code tiles (KB-byte swizzle) and the
 //               scale-factor atoms into a STAGES-deep shared-memory ring;
-//   warp 1      TMEM owner and MMA issuer: tcgen05.cp of the scale atoms
-//               into per-stage TMEM columns, tcgen05.mma kind::mxf4nvf4
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::mxf4nvf4
 //               scale_vec::4X (128 x 256 x 64 per instruction) into the TMEM
 //               accumulator, tcgen05.commit to free stages and publish tiles;
-//   warps 2..9  epilogue: two warps per TMEM lane quarter, 128 columns each.
+//   warps 4..7  scale warps, one per TMEM lane quarter: move each stage's
+//               E4M3 scale atoms from shared memory into that stage's TMEM
+//               scale columns with tcgen05.st, in the layout a replicating
+//               tcgen05.cp (.32x128b.warpx4) produces;
+//   warps 8..15 epilogue: two warps per TMEM lane quarter, 128 columns each.
 //               They pull the whole accumulator into registers, release TMEM
 //               at once (the next tile's MMAs start), then scale, add bias,
 //               GELU, add residual and store from registers.
+// Only MMAs go through the tensor pipe's issue queue: on GB300 one thread
+// issues about one tcgen05.mma/tcgen05.cp per 25 ns, so moving the three
+// scale copies of each 128 x 256 x 64 MMA (66 ns of tensor work) to
+// tcgen05.st from other warps takes the issue queue off the critical path.
+// Registers: the CTA launches with 128 per thread; warpgroups 0-1 drop to
+// 72 and the epilogue warpgroups rise to 184 (setmaxnreg), which adds up to
+// exactly the launch allocation.  The host refuses to launch a build whose
+// launch register count is not 128 (the rise would never be granted).
 // Every mbarrier wait is bounded; on expiry the CTA records an error in the
 // device error word, drains its own copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -36,18 +47,21 @@ namespace sixbit {
 namespace {
 
 constexpr int BM = 128;
-constexpr int kThreads = 320;            // producer, MMA, 8 epilogue warps
+constexpr int kThreads = 512;            // 4 warpgroups: control, scales, 2 x epilogue
 constexpr int kEpiThreads = 256;
+constexpr int kLaunchRegs = 128;         // 65536 / kThreads
+constexpr int kLowRegs = 72, kHighRegs = 184;
+static_assert(2 * 128 * kLowRegs + 2 * 128 * kHighRegs == kThreads * kLaunchRegs, "register split");
 constexpr uint32_t kSpinCap = 1u << 22;  // polls of a bounded mbarrier wait
 constexpr uint32_t kTmemCols = 512;
 
 #ifndef W4A4_NC
 #define W4A4_NC 2        // chunks of 64 bytes per stage (128 K elements)
-#define W4A4_STAGES 4
+#define W4A4_STAGES 3
 #endif
 #ifndef W4A8_NC
 #define W4A8_NC 1
-#define W4A8_STAGES 5
+#define W4A8_STAGES 4
 #endif
 
 template <int BN, int MODE, int STAGES, int KB, int NC>
@@ -77,8 +91,9 @@ struct Cfg {
   static constexpr int kSfBase = BN;
   static constexpr int kConstCol = kSfBase + STAGES * kSfStride;
   static_assert(kConstCol + 12 <= int(kTmemCols), "TMEM budget");
+  static constexpr int kStaging = 8 * 4096;               // per epilogue warp: 32 rows x 128 bytes of output
   static constexpr int kExtra = 2048;                      // constant digit-scale atoms + barriers
-  static constexpr size_t kSmem = size_t(STAGES) * kStage + kExtra + 1024;
+  static constexpr size_t kSmem = size_t(STAGES) * kStage + kStaging + kExtra + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -133,6 +148,16 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* tm,
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(c0), "r"(c1), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
@@ -166,6 +191,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Scale atoms into TMEM, laid out as tcgen05.cp .32x128b.warpx4 would: lane
+// l of every lane quarter holds row l of each 512-byte atom (16 bytes, the
+// scales of rows l, 32+l, 64+l, 96+l) in 4 consecutive columns.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, uint4 a, uint4 b, uint4 c, uint4 d) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w), "r"(c.x), "r"(c.y), "r"(c.z),
+      "r"(c.w), "r"(d.x), "r"(d.y), "r"(d.z), "r"(d.w)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, uint4 a, uint4 b) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(a.x),
+               "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+template <int R>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R)); }
+template <int R>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R)); }
 
 // Shared-memory matrix descriptor, K-major, KB-byte swizzle: rows of KB
 // bytes, 8-row groups 8*KB bytes apart (layout code 2 = 128B, 4 = 64B).
@@ -215,36 +261,48 @@ template <int BN, int MODE, int STAGES, int KB, int NC>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                    const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmR,
                     const Params p) {
   using C = Cfg<BN, MODE, STAGES, KB, NC>;
   if (p.pred && *p.pred == 0) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* extra = smem + size_t(STAGES) * C::kStage;
+  uint8_t* staging = smem + size_t(STAGES) * C::kStage;          // 8 x 4 KB, 1024-byte aligned
+  uint8_t* extra = staging + C::kStaging;
   uint8_t* const_sfa = extra;                                    // 3 x 512 bytes (mode 1)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(extra + 1536);    // full[S] empty[S] tfull tempty drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 3);
+  // barriers: full[S] empty[S] sfready[S] tfull tempty drain resid[8]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(extra + 1536);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 3 + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * uint32_t(s); };
   auto empty_bar = [&](int s) { return bar0 + 8u * uint32_t(STAGES + s); };
-  const uint32_t tfull_bar = bar0 + 8u * uint32_t(2 * STAGES);
-  const uint32_t tempty_bar = bar0 + 8u * uint32_t(2 * STAGES + 1);
-  const uint32_t drain_bar = bar0 + 8u * uint32_t(2 * STAGES + 2);
+  auto sfready_bar = [&](int s) { return bar0 + 8u * uint32_t(2 * STAGES + s); };
+  const uint32_t tfull_bar = bar0 + 8u * uint32_t(3 * STAGES);
+  const uint32_t tempty_bar = bar0 + 8u * uint32_t(3 * STAGES + 1);
+  const uint32_t drain_bar = bar0 + 8u * uint32_t(3 * STAGES + 2);
+  auto resid_bar = [&](int w) { return bar0 + 8u * uint32_t(3 * STAGES + 3 + w); };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+      mbar_init(sfready_bar(s), 4);            // one arrival per scale warp
+    }
     mbar_init(tfull_bar, 1);
     mbar_init(tempty_bar, kEpiThreads);
     mbar_init(drain_bar, 1);
+    for (int w = 0; w < 8; ++w) mbar_init(resid_bar(w), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     if (MODE == 0) prefetch_tmap(&tmSFA);
     prefetch_tmap(&tmSFB);
+    if (p.out_bf16) prefetch_tmap(&tmY);
+    if (p.out_bf16 && p.residual) prefetch_tmap(&tmR);
   }
   if (MODE == 1) {
     // constant digit scales 64, 8, 1 as E4M3 bytes (0x68, 0x50, 0x38)
@@ -270,7 +328,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.err) atomicExch(p.err, int(kErrWaitTimeout));
   };
 
-  if (warp == 0 && lane == 0) {
+  // ------------------------------------------------------------ MMA issuer
+  auto mma_issuer = [&]() {
+    constexpr uint32_t idesc = idesc_fp4(BN);
+    if (MODE == 1) {
+#pragma unroll
+      for (int pl = 0; pl < 3; ++pl) tc_cp_sf(tmem + C::kConstCol + 4 * pl, desc_sf(smem_u32(const_sfa + 512 * pl)));
+    }
+    // Descriptors of stage 0; stage s adds s * kStage bytes (>> 4) to the start address field.
+    const uint64_t adesc_s0 = desc_kmajor<KB>(smem_u32(smem));
+    const uint64_t bdesc_s0 = desc_kmajor<KB>(smem_u32(smem + C::offB));
+    int stage = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      // the epilogue has pulled the previous tile out of TMEM
+      if (!mbar_wait(tempty_bar, acc_phase ^ 1u, abort_flag)) { fail(); ok = false; break; }
+      tc_fence_after();
+      for (int kt = 0; kt < p.KT; ++kt) {
+        // operands landed and the scale warps have written this stage's scales
+        if (!mbar_wait(sfready_bar(stage), phase, abort_flag)) { fail(); ok = false; break; }
+        tc_fence_after();
+        const uint64_t soff = uint64_t((stage * C::kStage) >> 4);
+        const uint32_t sfa_t = tmem + uint32_t(C::kSfBase + stage * C::kSfStride);
+        const uint32_t sfb_t = sfa_t + uint32_t(C::kSfaCols);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+#pragma unroll
+          for (int j = 0; j < C::kMmaK; ++j) {
+            const int a = c * C::kMmaK + j;            // MMA index within the stage = scale atom index
+            const uint64_t bdesc = bdesc_s0 + soff + uint64_t((c * C::kChunkB + 32 * j) >> 4);
+            const uint32_t sfb = sfb_t + 4 * C::kRT * a;
+            if (MODE == 0) {
+              const uint64_t adesc = adesc_s0 + soff + uint64_t((c * C::kChunkA + 32 * j) >> 4);
+              tc_mma_fp4(tmem, adesc, bdesc, idesc, sfa_t + 4 * a, sfb, (kt | a) != 0);
+            } else {
+#pragma unroll
+              for (int pl = 0; pl < 3; ++pl) {
+                const uint64_t adesc = adesc_s0 + soff + uint64_t((pl * C::kA + c * C::kChunkA + 32 * j) >> 4);
+                tc_mma_fp4(tmem, adesc, bdesc, idesc, tmem + C::kConstCol + 4 * pl, sfb, (kt | a | pl) != 0);
+              }
+            }
+          }
+        }
+        tc_commit(empty_bar(stage));
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      tc_commit(tfull_bar);
+      acc_phase ^= 1u;
+    }
+    // all MMAs issued by this thread complete before TMEM is released
+    tc_commit(drain_bar);
+    mbar_wait(drain_bar, 0, nullptr);
+  };
+
+  if (warp < 4) {
+    // Warpgroup 0: the producer and MMA threads (warps 2-3 idle).  The
+    // register drop is warpgroup-wide, so every lane executes it here.
+    regs_dec<kLowRegs>();
+    if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
     int stage = 0;
     uint32_t phase = 0, issued = 0, last_par = 0;
@@ -307,78 +424,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < STAGES; ++s)
         if (issued & (1u << s)) mbar_wait(full_bar(s), (last_par >> s) & 1u, nullptr);
     }
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = idesc_fp4(BN);
-    if (MODE == 1) {
-#pragma unroll
-      for (int pl = 0; pl < 3; ++pl) tc_cp_sf(tmem + C::kConstCol + 4 * pl, desc_sf(smem_u32(const_sfa + 512 * pl)));
+    } else if (warp == 1 && lane == 0) {
+      mma_issuer();
     }
-    // Descriptors of stage 0; stage s adds s * kStage bytes (>> 4) to the start address field.
-    const uint64_t adesc_s0 = desc_kmajor<KB>(smem_u32(smem));
-    const uint64_t bdesc_s0 = desc_kmajor<KB>(smem_u32(smem + C::offB));
-    const uint64_t sfa_s0 = desc_sf(smem_u32(smem + C::offSFA));
-    const uint64_t sfb_s0 = desc_sf(smem_u32(smem + C::offSFB));
+  } else if (warp < 8) {
+    regs_dec<kLowRegs>();
+    // ------------------------------------------------------------ scale warps
+    // Stage s's TMEM scale columns are free again once stage s is refilled:
+    // the producer waited for the MMAs that read them (empty barrier).
+    const int q = warp & 3;
+    const uint32_t lane_base = uint32_t(q * 32) << 16;
     int stage = 0;
-    uint32_t phase = 0, acc_phase = 0;
+    uint32_t phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-      // the epilogue has pulled the previous tile out of TMEM
-      if (!mbar_wait(tempty_bar, acc_phase ^ 1u, abort_flag)) { fail(); ok = false; break; }
-      tc_fence_after();
       for (int kt = 0; kt < p.KT; ++kt) {
-        if (!mbar_wait(full_bar(stage), phase, abort_flag)) { fail(); ok = false; break; }
-        tc_fence_after();
-        const uint64_t soff = uint64_t((stage * C::kStage) >> 4);
-        const uint32_t sfa_t = tmem + uint32_t(C::kSfBase + stage * C::kSfStride);
-        const uint32_t sfb_t = sfa_t + uint32_t(C::kSfaCols);
-#pragma unroll
-        for (int a = 0; a < C::kAtoms; ++a) {
-          if (MODE == 0) tc_cp_sf(sfa_t + 4 * a, sfa_s0 + soff + uint64_t((512 * a) >> 4));
-#pragma unroll
-          for (int r = 0; r < C::kRT; ++r)
-            tc_cp_sf(sfb_t + 4 * (C::kRT * a + r), sfb_s0 + soff + uint64_t((512 * (C::kAtoms * r + a)) >> 4));
+        // every lane waits (each acquires the landed bytes); the verdict is
+        // made warp-uniform so the .sync.aligned stores below never diverge
+        const bool landed = mbar_wait(full_bar(stage), phase, abort_flag);
+        if (!__all_sync(0xffffffffu, landed)) {
+          if (lane == 0) fail();
+          ok = false;
+          break;
         }
+        const uint8_t* sb = smem + size_t(stage) * C::kStage;
+        const uint32_t sfa_t = tmem + lane_base + uint32_t(C::kSfBase + stage * C::kSfStride);
+        const uint32_t sfb_t = sfa_t + uint32_t(C::kSfaCols);
+        if (MODE == 0) {
+          uint4 wa[C::kAtoms];
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-#pragma unroll
-          for (int j = 0; j < C::kMmaK; ++j) {
-            const int a = c * C::kMmaK + j;            // MMA index within the stage = scale atom index
-            const uint64_t bdesc = bdesc_s0 + soff + uint64_t((c * C::kChunkB + 32 * j) >> 4);
-            const uint32_t sfb = sfb_t + 4 * C::kRT * a;
-            if (MODE == 0) {
-              const uint64_t adesc = adesc_s0 + soff + uint64_t((c * C::kChunkA + 32 * j) >> 4);
-              tc_mma_fp4(tmem, adesc, bdesc, idesc, sfa_t + 4 * a, sfb, (kt | a) != 0);
-            } else {
-#pragma unroll
-              for (int pl = 0; pl < 3; ++pl) {
-                const uint64_t adesc = adesc_s0 + soff + uint64_t((pl * C::kA + c * C::kChunkA + 32 * j) >> 4);
-                tc_mma_fp4(tmem, adesc, bdesc, idesc, tmem + C::kConstCol + 4 * pl, sfb, (kt | a | pl) != 0);
-              }
-            }
+          for (int a = 0; a < C::kAtoms; ++a) wa[a] = *reinterpret_cast<const uint4*>(sb + C::offSFA + 512 * a + 16 * lane);
+          if constexpr (C::kAtoms == 4) {
+            tmem_st16(sfa_t, wa[0], wa[1], wa[2], wa[3]);
+          } else {
+            tmem_st8(sfa_t, wa[0], wa[1]);
           }
         }
-        tc_commit(empty_bar(stage));
+#pragma unroll
+        for (int g = 0; g < C::kAtoms / 2; ++g) {   // K steps 2g, 2g+1; row tiles 0, 1 of each
+          const uint8_t* b0 = sb + C::offSFB + 16 * lane;
+          const uint4 w00 = *reinterpret_cast<const uint4*>(b0 + 512 * (2 * g));
+          const uint4 w01 = *reinterpret_cast<const uint4*>(b0 + 512 * (C::kAtoms + 2 * g));
+          const uint4 w10 = *reinterpret_cast<const uint4*>(b0 + 512 * (2 * g + 1));
+          const uint4 w11 = *reinterpret_cast<const uint4*>(b0 + 512 * (C::kAtoms + 2 * g + 1));
+          tmem_st16(sfb_t + 16 * g, w00, w01, w10, w11);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sfready_bar(stage));
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
-      if (!ok) break;
-      tc_commit(tfull_bar);
-      acc_phase ^= 1u;
     }
-    // all MMAs issued by this thread complete before TMEM is released
-    tc_commit(drain_bar);
-    mbar_wait(drain_bar, 0, nullptr);
-  } else if (warp >= 2) {
+  } else {
+    regs_inc<kHighRegs>();
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                      // TMEM lane quarter this warp may access
-    const int half = (warp - 2) >> 2;            // columns [128*half, 128*half + 128)
+    const int ew = warp - 8;                     // epilogue warp 0..7
+    const int half = ew >> 2;                    // columns [128*half, 128*half + 128)
     const int row = q * 32 + lane;
-    uint32_t acc_phase = 0;
+    // bf16 output leaves through this warp's staging block: 32 rows x 64
+    // columns (128 bytes a row, 16-byte chunk j of row r at j ^ (r % 8), the
+    // TMA 128-byte swizzle), written by one TMA store per 64 columns.
+    uint8_t* stg = staging + ew * 4096;
+    const uint32_t stg_s = smem_u32(stg);
+    const uint32_t rbar = resid_bar(ew);
+    uint32_t acc_phase = 0, r_phase = 0;
+    bool ok = true;
     const float gw = *p.g_w;
     const float gscale = MODE == 0 ? __fmul_rn(*p.g_a, gw) : gw;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
       const int mt = tile / p.NT, nt = tile - mt * p.NT;
-      if (!mbar_wait(tfull_bar, acc_phase, abort_flag)) { fail(); break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar, acc_phase, abort_flag))) {   // warp-uniform verdict
+        if (lane == 0) fail();
+        break;
+      }
       tc_fence_after();
       uint32_t r0[32], r1[32], r2[32], r3[32];
       const uint32_t taddr = tmem + uint32_t(half * 128) + (uint32_t(q * 32) << 16);
@@ -391,63 +511,124 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(tempty_bar);                   // TMEM is free: the next tile's MMAs may start
       acc_phase ^= 1u;
-      const int m = mt * BM + row;
-      if (m >= p.M) continue;
-      const float scale = MODE == 0 ? gscale : __fmul_rn(p.row_scale[m], gw);
+      const int m0 = mt * BM + q * 32;           // first row of this warp's block
+      const int m = m0 + lane;
       const int nbase = nt * BN + half * 128;
+      if (p.out_bf16) {
+        const float scale = MODE == 0 ? gscale : (m < p.M ? __fmul_rn(p.row_scale[m], gw) : 0.f);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t* rc = c == 0 ? r0 : (c == 1 ? r1 : (c == 2 ? r2 : r3));
-        const int n0 = nbase + c * 32;
-        if (n0 >= p.N) break;
-        const int cols = (p.N - n0) < 32 ? (p.N - n0) : 32;   // 16 or 32 (N % 16 == 0)
-        float v[32];
+        for (int k = 0; k < 2; ++k) {
+          const int n0 = nbase + 64 * k;
+          if (n0 >= p.N) break;
+          if (lane == 0) bulk_wait_read0();      // the previous store has read the block
+          __syncwarp();
+          if (p.residual) {
+            if (lane == 0) {
+              mbar_expect_tx(rbar, 4096);
+              tma_load_2d(stg_s, &tmR, n0, m0, rbar);   // rows >= M and columns >= N read as 0
+            }
+            if (!__all_sync(0xffffffffu, mbar_wait(rbar, r_phase, abort_flag))) {
+              if (lane == 0) fail();
+              ok = false;
+              break;
+            }
+            r_phase ^= 1u;
+          }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(__uint_as_float(rc[i]), scale);
-        if (p.bias) {
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t* rc = k == 0 ? (h == 0 ? r0 : r1) : (h == 0 ? r2 : r3);
+            const int nc = n0 + 32 * h;
+            float v[32];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if (8 * i >= cols) break;
-            const uint4 b = *reinterpret_cast<const uint4*>(p.bias + n0 + 8 * i);
-            const uint32_t* pb = &b.x;
+            for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(__uint_as_float(rc[i]), scale);
+            if (p.bias && nc < p.N) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              v[8 * i + 2 * e] = __fadd_rn(v[8 * i + 2 * e], bf16lo(pb[e]));
-              v[8 * i + 2 * e + 1] = __fadd_rn(v[8 * i + 2 * e + 1], bf16hi(pb[e]));
+              for (int i = 0; i < 4; ++i) {
+                if (nc + 8 * i >= p.N) break;
+                const uint4 b = *reinterpret_cast<const uint4*>(p.bias + nc + 8 * i);
+                const uint32_t* pb = &b.x;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  v[8 * i + 2 * e] = __fadd_rn(v[8 * i + 2 * e], bf16lo(pb[e]));
+                  v[8 * i + 2 * e + 1] = __fadd_rn(v[8 * i + 2 * e + 1], bf16hi(pb[e]));
+                }
+              }
+            }
+            if (p.gelu) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int j = 4 * h + i;           // 16-byte chunk of the 128-byte row
+              uint4* slot = reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4));
+              if (p.residual) {
+                const uint4 rr = *slot;
+                const uint32_t* pr = &rr.x;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  v[8 * i + 2 * e] = __fadd_rn(v[8 * i + 2 * e], bf16lo(pr[e]));
+                  v[8 * i + 2 * e + 1] = __fadd_rn(v[8 * i + 2 * e + 1], bf16hi(pr[e]));
+                }
+              }
+              uint4 w;
+              w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+              w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+              w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+              w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+              *slot = w;
             }
           }
+          fence_async_smem();                    // generic writes -> visible to the TMA store
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmY, stg_s, n0, m0);   // rows >= M and columns >= N are not written
+            bulk_commit();
+          }
         }
-        if (p.gelu) {
+      } else {
+        if (m >= p.M) continue;
+        const float scale = MODE == 0 ? gscale : __fmul_rn(p.row_scale[m], gw);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
-        }
-        if (p.residual) {
-          const uint16_t* rp = p.residual + int64_t(m) * p.ldr + n0;
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t* rc = c == 0 ? r0 : (c == 1 ? r1 : (c == 2 ? r2 : r3));
+          const int n0 = nbase + c * 32;
+          if (n0 >= p.N) break;
+          const int cols = (p.N - n0) < 32 ? (p.N - n0) : 32;   // 16 or 32 (N % 16 == 0)
+          float v[32];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if (8 * i >= cols) break;
-            const uint4 b = *reinterpret_cast<const uint4*>(rp + 8 * i);
-            const uint32_t* pb = &b.x;
+          for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(__uint_as_float(rc[i]), scale);
+          if (p.bias) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              v[8 * i + 2 * e] = __fadd_rn(v[8 * i + 2 * e], bf16lo(pb[e]));
-              v[8 * i + 2 * e + 1] = __fadd_rn(v[8 * i + 2 * e + 1], bf16hi(pb[e]));
+            for (int i = 0; i < 4; ++i) {
+              if (8 * i >= cols) break;
+              const uint4 b = *reinterpret_cast<const uint4*>(p.bias + n0 + 8 * i);
+              const uint32_t* pb = &b.x;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                v[8 * i + 2 * e] = __fadd_rn(v[8 * i + 2 * e], bf16lo(pb[e]));
+                v[8 * i + 2 * e + 1] = __fadd_rn(v[8 * i + 2 * e + 1], bf16hi(pb[e]));
+              }
             }
           }
-        }
-        if (p.out_bf16) {
-          uint16_t* yp = static_cast<uint16_t*>(p.y) + int64_t(m) * p.ldy + n0;
+          if (p.gelu) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if (8 * i >= cols) break;
-            uint4 w;
-            w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
-            w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
-            w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
-            w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
-            *reinterpret_cast<uint4*>(yp + 8 * i) = w;
+            for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
           }
-        } else {
+          if (p.residual) {
+            const uint16_t* rp = p.residual + int64_t(m) * p.ldr + n0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if (8 * i >= cols) break;
+              const uint4 b = *reinterpret_cast<const uint4*>(rp + 8 * i);
+              const uint32_t* pb = &b.x;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                v[8 * i + 2 * e] = __fadd_rn(v[8 * i + 2 * e], bf16lo(pb[e]));
+                v[8 * i + 2 * e + 1] = __fadd_rn(v[8 * i + 2 * e + 1], bf16hi(pb[e]));
+              }
+            }
+          }
           float* yp = static_cast<float*>(p.y) + int64_t(m) * p.ldy + n0;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -457,6 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (lane == 0) bulk_wait0();                 // this warp's output stores are complete
   }
   tc_fence_before();
   __syncthreads();
@@ -543,6 +725,17 @@ int run(const GemmCall& c, int num_sms, cudaStream_t s) {
     uint32_t b2[3] = {128, uint32_t(Cf::kAtoms), uint32_t(Cf::kRT)};
     ok &= make_map(&tSB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, c.w_sf, d2, st2, b2, CU_TENSOR_MAP_SWIZZLE_NONE);
   }
+  // bf16 output (and residual) through 32-row x 64-column boxes, 128-byte swizzle
+  CUtensorMap tY = tB, tR = tB;
+  if (c.out_bf16) {
+    uint64_t d[2] = {uint64_t(c.N), uint64_t(c.M)}, st[1] = {uint64_t(c.ldy) * 2};
+    uint32_t b[2] = {64, 32};
+    ok &= make_map(&tY, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, c.y, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (c.residual) {
+      uint64_t dr[2] = {uint64_t(c.N), uint64_t(c.M)}, sr[1] = {uint64_t(c.ldr) * 2};
+      ok &= make_map(&tR, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, c.residual, dr, sr, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+  }
   if (!ok) return kELaunch;
   Params p;
   p.M = int(c.M); p.N = int(c.N); p.K = int(c.K);
@@ -557,13 +750,18 @@ int run(const GemmCall& c, int num_sms, cudaStream_t s) {
   auto kern = gemm_fp4_kernel<BN, MODE, STAGES, KB, NC>;
   static bool attr_set = false;
   if (!attr_set) {
+    // The register split (setmaxnreg) assumes exactly kLaunchRegs per thread
+    // at launch; any other allocation would leave the epilogue's request
+    // unsatisfiable, so such a build is refused here.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs != kLaunchRegs) return kELaunch;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cf::kSmem)) != cudaSuccess)
       return kELaunch;
     attr_set = true;
   }
   const int tiles = p.MT * p.NT;
   const int grid = tiles < num_sms ? tiles : num_sms;
-  kern<<<grid, kThreads, Cf::kSmem, s>>>(tA, tB, tSA, tSB, p);
+  kern<<<grid, kThreads, Cf::kSmem, s>>>(tA, tB, tSA, tSB, tY, tR, p);
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 
@@ -576,8 +774,8 @@ int launch_gemm_fp4(const GemmCall& c, int num_sms, cudaStream_t s) {
   // op per operand (the per-op cost, not bandwidth, bounded smaller stages).
   // Otherwise one chunk per stage through 2-D maps.
   const bool chunked = (c.K / 2) % 64 == 0;
-  if (c.mode == 0) return chunked ? run<256, 0, W4A4_STAGES, 64, W4A4_NC>(c, num_sms, s) : run<256, 0, 4, 128, 1>(c, num_sms, s);
-  return chunked ? run<256, 1, W4A8_STAGES, 64, W4A8_NC>(c, num_sms, s) : run<256, 1, 5, 64, 1>(c, num_sms, s);
+  if (c.mode == 0) return chunked ? run<256, 0, W4A4_STAGES, 64, W4A4_NC>(c, num_sms, s) : run<256, 0, 3, 128, 1>(c, num_sms, s);
+  return chunked ? run<256, 1, W4A8_STAGES, 64, W4A8_NC>(c, num_sms, s) : run<256, 1, 4, 64, 1>(c, num_sms, s);
 }
 
 }  // namespace sixbit

@@ -55,25 +55,32 @@ static_assert(2 * 128 * kLowRegs + 2 * 128 * kHighRegs == kThreads * kLaunchRegs
 constexpr uint32_t kSpinCap = 1u << 22;  // polls of a bounded mbarrier wait
 constexpr uint32_t kTmemCols = 512;
 
+#ifndef GEMM_PAIR
+#define GEMM_PAIR false  // true: CTA pairs with cta_group::2 MMAs (256 x 256 tiles)
+#endif
 #ifndef W4A4_NC
 #define W4A4_NC 2        // chunks of 64 bytes per stage (128 K elements)
-#define W4A4_STAGES 3
+#define W4A4_STAGES (GEMM_PAIR ? 5 : 3)
 #endif
 #ifndef W4A8_NC
 #define W4A8_NC 1
-#define W4A8_STAGES 4
+#define W4A8_STAGES (GEMM_PAIR ? 5 : 4)
 #endif
 
-template <int BN, int MODE, int STAGES, int KB, int NC>
+template <int BN, int MODE, int STAGES, int KB, int NC, bool PAIR>
 struct Cfg {
   static_assert(BN == 256, "epilogue assumes 256-column tiles");
+  // PAIR: a cluster of two CTAs computes a 256 x BN tile with cta_group::2
+  // MMAs; each CTA holds its own 128 rows of A and BN/2 rows of W.
+  static constexpr int kTileM = PAIR ? 2 * BM : BM;
+  static constexpr int kBRows = PAIR ? BN / 2 : BN;
   static_assert(KB == 64 || KB == 128, "K chunk of 64 or 128 bytes per row");
   static constexpr int kMmaK = KB / 32;                    // MMAs (K = 64 elements) per chunk
   static constexpr int kAtoms = kMmaK * NC;                // 512-byte scale atoms per 128 rows per stage
   static constexpr int kPlanes = MODE == 0 ? 1 : 3;
   static constexpr int kRT = BN / 128;                     // 128-row scale tiles of W per N tile
   static constexpr int kChunkA = BM * KB;                  // one chunk of one A plane
-  static constexpr int kChunkB = BN * KB;
+  static constexpr int kChunkB = kBRows * KB;
   static constexpr int kA = kChunkA * NC;                  // one A plane, all chunks of a stage
   static constexpr int kB = kChunkB * NC;
   static constexpr int kSFA = MODE == 0 ? 512 * kAtoms : 0;
@@ -83,16 +90,19 @@ struct Cfg {
   static constexpr int offSFB = offSFA + kSFA;
   static constexpr int kStage = offSFB + kSFB;
   static_assert(kStage % 1024 == 0, "stages stay 1024-byte aligned");
-  static constexpr uint32_t kTx = kStage;                  // bytes landed per stage
+  static constexpr uint32_t kTxA = kPlanes * kA;           // bytes landed per stage, by producer
+  static constexpr uint32_t kTxB = kB;
+  static constexpr uint32_t kTxS = kSFA + kSFB;
   // TMEM columns: accumulator [0, BN), then per-stage scale columns, then
-  // the three constant digit-scale atoms (mode 1).
+  // the three constant digit-scale atoms (mode 1).  Each CTA of a pair holds
+  // the scales of its own A rows and of all BN rows of W.
   static constexpr int kSfaCols = MODE == 0 ? 4 * kAtoms : 0;
   static constexpr int kSfStride = kSfaCols + 4 * kAtoms * kRT;
   static constexpr int kSfBase = BN;
   static constexpr int kConstCol = kSfBase + STAGES * kSfStride;
   static_assert(kConstCol + 12 <= int(kTmemCols), "TMEM budget");
   static constexpr int kStaging = 8 * 4096;               // per epilogue warp: 32 rows x 128 bytes of output
-  static constexpr int kExtra = 2048;                      // constant digit-scale atoms + barriers
+  static constexpr int kExtra = 1024;                      // barriers, TMEM address, abort flag
   static constexpr size_t kSmem = size_t(STAGES) * kStage + kStaging + kExtra + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
 };
@@ -118,10 +128,21 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: false when the cap expired or another role aborted.
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false when the cap expired or another role aborted.  CL:
+// the barrier also receives arrivals from the other CTA of a pair.
+template <bool CL = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   for (uint32_t i = 0; i < kSpinCap; ++i) {
-    if (mbar_try(bar, parity)) return true;
+    if (CL ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
     if ((i & 255u) == 255u && abort_flag && *abort_flag) return false;
   }
   return false;
@@ -164,21 +185,61 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+// Commit of this thread's MMAs to a barrier of this CTA only.
+template <bool PAIR>
+__device__ __forceinline__ void tc_commit_local(uint32_t bar) {
+  if constexpr (PAIR)
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+  else
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
-// 512-byte scale atom (32 rows x 16 bytes) -> 4 TMEM columns, replicated to
-// the four lane quarters; the MMA reads row r's scales from column r/32.
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
+template <bool PAIR>
 __device__ __forceinline__ void tc_mma_fp4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
                                            uint32_t sfb, uint32_t accum) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(accum), "r"(sfa), "r"(sfb)
-      : "memory");
+  if constexpr (PAIR)
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accum), "r"(sfa), "r"(sfb)
+        : "memory");
+  else
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accum), "r"(sfa), "r"(sfb)
+        : "memory");
+}
+// Commit of this thread's MMAs to a barrier; in a pair, to the barrier at the
+// same offset in both CTAs.
+template <bool PAIR>
+__device__ __forceinline__ void tc_commit_all(uint32_t bar) {
+  if constexpr (PAIR)
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                     bar),
+                 "h"(uint16_t(3))
+                 : "memory");
+  else
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
@@ -207,6 +268,9 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, uint4 a, uint4 b) {
                "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
                : "memory");
 }
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t w) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%1,%1,%1};" ::"r"(taddr), "r"(w) : "memory");
+}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 template <int R>
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R)); }
@@ -221,14 +285,10 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) {
   return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t((8 * KB) >> 4) << 32) |
          (uint64_t(1) << 46) | (layout << 61);
 }
-// Descriptor of a 512-byte scale atom: 8-row core matrices of 16-byte rows, 128 bytes apart.
-__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
-  return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(128 >> 4) << 32) | (uint64_t(1) << 46);
-}
 // Instruction descriptor, kind::mxf4nvf4: A, B = E2M1, K-major, dense,
-// UE4M3 scales, M = 128, N = n.
-__host__ __device__ constexpr uint32_t idesc_fp4(int n) {
-  return (1u << 7) | (1u << 10) | (uint32_t(n >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+// UE4M3 scales, M = m (128, or 256 for a CTA pair), N = n.
+__host__ __device__ constexpr uint32_t idesc_fp4(int m, int n) {
+  return (1u << 7) | (1u << 10) | (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
 }
 
 // tanh-form GELU, 0.5 x (1 + tanh(u)) with u = sqrt(2/pi) (x + 0.044715 x^3),
@@ -257,25 +317,25 @@ struct Params {
   int* err;
 };
 
-template <int BN, int MODE, int STAGES, int KB, int NC>
+template <int BN, int MODE, int STAGES, int KB, int NC, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                     const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmR,
                     const Params p) {
-  using C = Cfg<BN, MODE, STAGES, KB, NC>;
-  if (p.pred && *p.pred == 0) return;
+  using C = Cfg<BN, MODE, STAGES, KB, NC, PAIR>;
+  if (p.pred && *p.pred == 0) return;          // both CTAs of a pair read the same gate
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* staging = smem + size_t(STAGES) * C::kStage;          // 8 x 4 KB, 1024-byte aligned
   uint8_t* extra = staging + C::kStaging;
-  uint8_t* const_sfa = extra;                                    // 3 x 512 bytes (mode 1)
   // barriers: full[S] empty[S] sfready[S] tfull tempty drain resid[8]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(extra + 1536);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(extra);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 3 + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;              // 0: the CTA that issues the MMAs
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * uint32_t(s); };
   auto empty_bar = [&](int s) { return bar0 + 8u * uint32_t(STAGES + s); };
@@ -284,15 +344,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tempty_bar = bar0 + 8u * uint32_t(3 * STAGES + 1);
   const uint32_t drain_bar = bar0 + 8u * uint32_t(3 * STAGES + 2);
   auto resid_bar = [&](int w) { return bar0 + 8u * uint32_t(3 * STAGES + 3 + w); };
+  // Arrival on a barrier of the issuing CTA (rank 0): local, or across the pair.
+  auto arrive_leader = [&](uint32_t bar) {
+    if constexpr (PAIR) mbar_arrive_remote(map_rank(bar, 0));
+    else mbar_arrive(bar);
+  };
+  constexpr int kCtas = PAIR ? 2 : 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), 3);               // the A, W and scale producers
       mbar_init(empty_bar(s), 1);
-      mbar_init(sfready_bar(s), 4);            // one arrival per scale warp
+      mbar_init(sfready_bar(s), 4 * kCtas);    // one arrival per scale warp of the pair
     }
     mbar_init(tfull_bar, 1);
-    mbar_init(tempty_bar, kEpiThreads);
+    mbar_init(tempty_bar, 8 * kCtas);          // one arrival per epilogue warp of the pair
     mbar_init(drain_bar, 1);
     for (int w = 0; w < 8; ++w) mbar_init(resid_bar(w), 1);
     *abort_flag = 0;
@@ -304,50 +370,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.out_bf16) prefetch_tmap(&tmY);
     if (p.out_bf16 && p.residual) prefetch_tmap(&tmR);
   }
-  if (MODE == 1) {
-    // constant digit scales 64, 8, 1 as E4M3 bytes (0x68, 0x50, 0x38)
-    for (int i = threadIdx.x; i < 3 * 128; i += kThreads) {
-      const uint32_t b = i < 128 ? 0x68u : (i < 256 ? 0x50u : 0x38u);
-      reinterpret_cast<uint32_t*>(const_sfa)[i] = b * 0x01010101u;
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(kTmemCols));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    if constexpr (PAIR) {
+      // one allocation for the pair: warp 1 of both CTAs takes part
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(kTmemCols));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(kTmemCols));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();          // both CTAs' barriers and TMEM exist before any cross traffic
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int ntiles = p.MT * p.NT;
 
   auto fail = [&]() {
     *abort_flag = 1;
+    if constexpr (PAIR) st_cluster_u32(map_rank(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u), 1u);
     if (p.err) atomicExch(p.err, int(kErrWaitTimeout));
   };
 
   // ------------------------------------------------------------ MMA issuer
   auto mma_issuer = [&]() {
-    constexpr uint32_t idesc = idesc_fp4(BN);
-    if (MODE == 1) {
-#pragma unroll
-      for (int pl = 0; pl < 3; ++pl) tc_cp_sf(tmem + C::kConstCol + 4 * pl, desc_sf(smem_u32(const_sfa + 512 * pl)));
-    }
+    constexpr uint32_t idesc = idesc_fp4(C::kTileM, BN);
     // Descriptors of stage 0; stage s adds s * kStage bytes (>> 4) to the start address field.
     const uint64_t adesc_s0 = desc_kmajor<KB>(smem_u32(smem));
     const uint64_t bdesc_s0 = desc_kmajor<KB>(smem_u32(smem + C::offB));
     int stage = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-      // the epilogue has pulled the previous tile out of TMEM
-      if (!mbar_wait(tempty_bar, acc_phase ^ 1u, abort_flag)) { fail(); ok = false; break; }
+    for (int tile = blockIdx.x / kCtas; tile < ntiles && ok; tile += gridDim.x / kCtas) {
+      // the epilogue warps (of both CTAs) have pulled the previous tile out of TMEM
+      if (!mbar_wait<PAIR>(tempty_bar, acc_phase ^ 1u, abort_flag)) { fail(); ok = false; break; }
       tc_fence_after();
       for (int kt = 0; kt < p.KT; ++kt) {
-        // operands landed and the scale warps have written this stage's scales
-        if (!mbar_wait(sfready_bar(stage), phase, abort_flag)) { fail(); ok = false; break; }
+        // the stage landed and the scale warps (of both CTAs) have written its scales
+        if (!mbar_wait<PAIR>(sfready_bar(stage), phase, abort_flag)) { fail(); ok = false; break; }
         tc_fence_after();
         const uint64_t soff = uint64_t((stage * C::kStage) >> 4);
         const uint32_t sfa_t = tmem + uint32_t(C::kSfBase + stage * C::kSfStride);
@@ -361,25 +424,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sfb = sfb_t + 4 * C::kRT * a;
             if (MODE == 0) {
               const uint64_t adesc = adesc_s0 + soff + uint64_t((c * C::kChunkA + 32 * j) >> 4);
-              tc_mma_fp4(tmem, adesc, bdesc, idesc, sfa_t + 4 * a, sfb, (kt | a) != 0);
+              tc_mma_fp4<PAIR>(tmem, adesc, bdesc, idesc, sfa_t + 4 * a, sfb, (kt | a) != 0);
             } else {
 #pragma unroll
               for (int pl = 0; pl < 3; ++pl) {
                 const uint64_t adesc = adesc_s0 + soff + uint64_t((pl * C::kA + c * C::kChunkA + 32 * j) >> 4);
-                tc_mma_fp4(tmem, adesc, bdesc, idesc, tmem + C::kConstCol + 4 * pl, sfb, (kt | a | pl) != 0);
+                tc_mma_fp4<PAIR>(tmem, adesc, bdesc, idesc, tmem + C::kConstCol + 4 * pl, sfb, (kt | a | pl) != 0);
               }
             }
           }
         }
-        tc_commit(empty_bar(stage));
+        tc_commit_all<PAIR>(empty_bar(stage));       // frees the stage in both CTAs
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
-      tc_commit(tfull_bar);
+      tc_commit_all<PAIR>(tfull_bar);
       acc_phase ^= 1u;
     }
     // all MMAs issued by this thread complete before TMEM is released
-    tc_commit(drain_bar);
+    tc_commit_local<PAIR>(drain_bar);
     mbar_wait(drain_bar, 0, nullptr);
   };
 
@@ -387,57 +450,74 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Warpgroup 0: the producer and MMA threads (warps 2-3 idle).  The
     // register drop is warpgroup-wide, so every lane executes it here.
     regs_dec<kLowRegs>();
-    if (warp == 0 && lane == 0) {
-    // ------------------------------------------------------------ producer
-    int stage = 0;
-    uint32_t phase = 0, issued = 0, last_par = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-      const int mt = tile / p.NT, nt = tile - mt * p.NT;
-      for (int kt = 0; kt < p.KT; ++kt) {
-        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { fail(); ok = false; break; }
-        uint8_t* sb = smem + size_t(stage) * C::kStage;
-        const uint32_t fb = full_bar(stage);
-        mbar_expect_tx(fb, C::kTx);
-        if (p.chunked) {
-          // one op per operand: NC chunks of KB bytes (and all three planes in mode 1)
-          if (MODE == 0) tma_load_3d(smem_u32(sb), &tmA, 0, mt * BM, kt * NC, fb);
-          else tma_load_4d(smem_u32(sb), &tmA, 0, mt * BM, kt * NC, 0, fb);
-          tma_load_3d(smem_u32(sb + C::offB), &tmB, 0, nt * BN, kt * NC, fb);
-        } else {
-          if (MODE == 0) {
-            tma_load_2d(smem_u32(sb), &tmA, kt * KB, mt * BM, fb);
-          } else {
+    if ((warp == 0 || warp == 2 || warp == 3) && lane == 0) {
+      // ---------------------------------------------------------- producers
+      // warp 0 loads A (codes or the three digit planes), warp 2 loads W,
+      // warp 3 the scale atoms: a single thread issues about one TMA op per
+      // 75 ns plus ~150 ns per stage, which one producer for all four ops
+      // of a stage could not keep ahead of the stage's MMAs.
+      const int role = warp == 0 ? 0 : (warp == 2 ? 1 : 2);
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, last_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x / kCtas; tile < ntiles && ok; tile += gridDim.x / kCtas) {
+        const int mt = tile / p.NT, nt = tile - mt * p.NT;
+        const int arow = mt * C::kTileM + int(rank) * BM;          // this CTA's A rows
+        const int brow = nt * BN + int(rank) * C::kBRows;          // this CTA's W rows
+        for (int kt = 0; kt < p.KT; ++kt) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { fail(); ok = false; break; }
+          uint8_t* sb = smem + size_t(stage) * C::kStage;
+          const uint32_t fb = full_bar(stage);
+          if (role == 0) {
+            mbar_expect_tx(fb, C::kTxA);
+            if (p.chunked) {
+              if (MODE == 0) tma_load_3d(smem_u32(sb), &tmA, 0, arow, kt * NC, fb);
+              else tma_load_4d(smem_u32(sb), &tmA, 0, arow, kt * NC, 0, fb);   // all three planes
+            } else if (MODE == 0) {
+              tma_load_2d(smem_u32(sb), &tmA, kt * KB, arow, fb);
+            } else {
 #pragma unroll
-            for (int pl = 0; pl < 3; ++pl) tma_load_3d(smem_u32(sb + pl * C::kA), &tmA, kt * KB, mt * BM, pl, fb);
+              for (int pl = 0; pl < 3; ++pl) tma_load_3d(smem_u32(sb + pl * C::kA), &tmA, kt * KB, arow, pl, fb);
+            }
+          } else if (role == 1) {
+            mbar_expect_tx(fb, C::kTxB);
+            if (p.chunked) tma_load_3d(smem_u32(sb + C::offB), &tmB, 0, brow, kt * NC, fb);
+            else tma_load_2d(smem_u32(sb + C::offB), &tmB, kt * KB, brow, fb);
+          } else {
+            mbar_expect_tx(fb, C::kTxS);
+            if (MODE == 0) tma_load_3d(smem_u32(sb + C::offSFA), &tmSFA, 0, kt * C::kAtoms, arow / BM, fb);
+            tma_load_3d(smem_u32(sb + C::offSFB), &tmSFB, 0, kt * C::kAtoms, nt * C::kRT, fb);
           }
-          tma_load_2d(smem_u32(sb + C::offB), &tmB, kt * KB, nt * BN, fb);
+          issued |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        if (MODE == 0) tma_load_3d(smem_u32(sb + C::offSFA), &tmSFA, 0, kt * C::kAtoms, mt, fb);
-        tma_load_3d(smem_u32(sb + C::offSFB), &tmSFB, 0, kt * C::kAtoms, nt * C::kRT, fb);
-        issued |= 1u << stage;
-        last_par = (last_par & ~(1u << stage)) | (phase << stage);
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
-    }
-    if (!ok) {   // let the copies already issued land before the CTA exits
-      for (int s = 0; s < STAGES; ++s)
-        if (issued & (1u << s)) mbar_wait(full_bar(s), (last_par >> s) & 1u, nullptr);
-    }
-    } else if (warp == 1 && lane == 0) {
+      if (!ok) {   // let the copies already issued land before the CTA exits
+        for (int s = 0; s < STAGES; ++s)
+          if (issued & (1u << s)) mbar_wait(full_bar(s), (last_par >> s) & 1u, nullptr);
+      }
+    } else if (warp == 1 && lane == 0 && rank == 0) {
       mma_issuer();
     }
   } else if (warp < 8) {
     regs_dec<kLowRegs>();
     // ------------------------------------------------------------ scale warps
     // Stage s's TMEM scale columns are free again once stage s is refilled:
-    // the producer waited for the MMAs that read them (empty barrier).
+    // the producers waited for the MMAs that read them (empty barrier).
     const int q = warp & 3;
     const uint32_t lane_base = uint32_t(q * 32) << 16;
+    if (MODE == 1) {
+      // constant digit scales 64, 8, 1 (E4M3 0x68, 0x50, 0x38) for every row and K block
+      const uint32_t cb = tmem + lane_base + uint32_t(C::kConstCol);
+      tmem_st4(cb, 0x68686868u);
+      tmem_st4(cb + 4, 0x50505050u);
+      tmem_st4(cb + 8, 0x38383838u);
+    }
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+    for (int tile = blockIdx.x / kCtas; tile < ntiles && ok; tile += gridDim.x / kCtas) {
       for (int kt = 0; kt < p.KT; ++kt) {
         // every lane waits (each acquires the landed bytes); the verdict is
         // made warp-uniform so the .sync.aligned stores below never diverge
@@ -472,10 +552,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(sfready_bar(stage));
+        if (lane == 0) arrive_leader(sfready_bar(stage));
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
+    tmem_st_wait();                              // nothing of this warp is in flight at teardown
   } else {
     regs_inc<kHighRegs>();
     // ------------------------------------------------------------ epilogue
@@ -493,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     const float gw = *p.g_w;
     const float gscale = MODE == 0 ? __fmul_rn(*p.g_a, gw) : gw;
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+    for (int tile = blockIdx.x / kCtas; tile < ntiles && ok; tile += gridDim.x / kCtas) {
       const int mt = tile / p.NT, nt = tile - mt * p.NT;
       if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar, acc_phase, abort_flag))) {   // warp-uniform verdict
         if (lane == 0) fail();
@@ -509,9 +590,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(taddr + 96, r3);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(tempty_bar);                   // TMEM is free: the next tile's MMAs may start
+      __syncwarp();
+      if (lane == 0) arrive_leader(tempty_bar);  // TMEM is free: the next tile's MMAs may start
       acc_phase ^= 1u;
-      const int m0 = mt * BM + q * 32;           // first row of this warp's block
+      const int m0 = mt * C::kTileM + int(rank) * BM + q * 32;   // first row of this warp's block
       const int m = m0 + lane;
       const int nbase = nt * BN + half * 128;
       if (p.out_bf16) {
@@ -642,9 +724,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();          // the leader's MMAs into this CTA's TMEM are complete
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    if constexpr (PAIR)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
   }
 }
 
@@ -670,9 +756,9 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int MODE, int STAGES, int KB, int NC>
+template <int BN, int MODE, int STAGES, int KB, int NC, bool PAIR>
 int run(const GemmCall& c, int num_sms, cudaStream_t s) {
-  using Cf = Cfg<BN, MODE, STAGES, KB, NC>;
+  using Cf = Cfg<BN, MODE, STAGES, KB, NC, PAIR>;
   constexpr CUtensorMapSwizzle kSw = KB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   const int64_t kb = c.K / 2;                       // bytes of codes per row
   const int64_t natoms = c.K / 64;                  // 512-byte scale atoms per 128-row tile
@@ -695,9 +781,6 @@ int run(const GemmCall& c, int num_sms, cudaStream_t s) {
       uint32_t b[2] = {uint32_t(KB), uint32_t(BM)};
       ok &= make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.a, d, st, b, kSw);
     }
-    uint64_t d2[3] = {128, uint64_t(natoms), uint64_t(cdiv(c.M, 128))}, st2[2] = {512, uint64_t(natoms) * 512};
-    uint32_t b2[3] = {128, uint32_t(Cf::kAtoms), 1};
-    ok &= make_map(&tSA, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, c.a_sf, d2, st2, b2, CU_TENSOR_MAP_SWIZZLE_NONE);
   } else {
     if (chunked) {
       uint64_t d[4] = {uint64_t(KB), uint64_t(c.M), uint64_t(nch), 3};
@@ -709,21 +792,27 @@ int run(const GemmCall& c, int num_sms, cudaStream_t s) {
       uint32_t b[3] = {uint32_t(KB), uint32_t(BM), 1};
       ok &= make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c.a, d, st, b, kSw);
     }
-    tSA = tA;   // unused in mode 1
   }
   if (chunked) {
     uint64_t d[3] = {uint64_t(KB), uint64_t(c.N), uint64_t(nch)}, st[2] = {uint64_t(kb), uint64_t(KB)};
-    uint32_t b[3] = {uint32_t(KB), uint32_t(BN), uint32_t(NC)};
+    uint32_t b[3] = {uint32_t(KB), uint32_t(Cf::kBRows), uint32_t(NC)};
     ok &= make_map(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c.w, d, st, b, kSw);
   } else {
     uint64_t d[2] = {uint64_t(kb), uint64_t(c.N)}, st[1] = {uint64_t(kb)};
-    uint32_t b[2] = {uint32_t(KB), uint32_t(BN)};
+    uint32_t b[2] = {uint32_t(KB), uint32_t(Cf::kBRows)};
     ok &= make_map(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.w, d, st, b, kSw);
   }
   {
+    // scale atoms: [row tile][K step][128 x u32]; a box brings kAtoms K steps of one (A) or kRT (W) row tiles
     uint64_t d2[3] = {128, uint64_t(natoms), uint64_t(cdiv(c.N, 128))}, st2[2] = {512, uint64_t(natoms) * 512};
     uint32_t b2[3] = {128, uint32_t(Cf::kAtoms), uint32_t(Cf::kRT)};
     ok &= make_map(&tSB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, c.w_sf, d2, st2, b2, CU_TENSOR_MAP_SWIZZLE_NONE);
+    tSA = tSB;   // unused in mode 1
+    if (MODE == 0) {
+      uint64_t d3[3] = {128, uint64_t(natoms), uint64_t(cdiv(c.M, 128))};
+      uint32_t b3[3] = {128, uint32_t(Cf::kAtoms), 1};
+      ok &= make_map(&tSA, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, c.a_sf, d3, st2, b3, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
   }
   // bf16 output (and residual) through 32-row x 64-column boxes, 128-byte swizzle
   CUtensorMap tY = tB, tR = tB;
@@ -740,14 +829,15 @@ int run(const GemmCall& c, int num_sms, cudaStream_t s) {
   Params p;
   p.M = int(c.M); p.N = int(c.N); p.K = int(c.K);
   p.KT = int(chunked ? cdiv(nch, NC) : cdiv(kb, KB));
-  p.MT = int(cdiv(c.M, BM));
+  p.MT = int(cdiv(c.M, Cf::kTileM));
   p.NT = int(cdiv(c.N, BN));
   p.g_a = c.g_a; p.row_scale = c.row_scale; p.g_w = c.g_w;
   p.bias = static_cast<const uint16_t*>(c.bias);
   p.residual = static_cast<const uint16_t*>(c.residual);
   p.ldr = c.ldr; p.y = c.y; p.ldy = c.ldy; p.out_bf16 = c.out_bf16; p.gelu = c.gelu; p.pred = c.pred; p.err = c.err;
   p.chunked = chunked ? 1 : 0;
-  auto kern = gemm_fp4_kernel<BN, MODE, STAGES, KB, NC>;
+
+  auto kern = gemm_fp4_kernel<BN, MODE, STAGES, KB, NC, PAIR>;
   static bool attr_set = false;
   if (!attr_set) {
     // The register split (setmaxnreg) assumes exactly kLaunchRegs per thread
@@ -760,8 +850,29 @@ int run(const GemmCall& c, int num_sms, cudaStream_t s) {
     attr_set = true;
   }
   const int tiles = p.MT * p.NT;
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  kern<<<grid, kThreads, Cf::kSmem, s>>>(tA, tB, tSA, tSB, tY, tR, p);
+  constexpr int kCtas = PAIR ? 2 : 1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCtas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cf::kSmem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // persistent grid: as many CTA pairs (or CTAs) as can be resident at once
+  static int resident = 0;
+  if (resident == 0) {
+    cfg.gridDim = dim3(kCtas * (num_sms / kCtas));
+    int n = 0;
+    if (PAIR && cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) resident = n;
+    else resident = num_sms / kCtas;
+  }
+  const int units = tiles < resident ? tiles : resident;
+  cfg.gridDim = dim3(kCtas * units);
+  if (cudaLaunchKernelEx(&cfg, kern, tA, tB, tSA, tSB, tY, tR, p) != cudaSuccess) return kELaunch;
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 
@@ -774,8 +885,11 @@ int launch_gemm_fp4(const GemmCall& c, int num_sms, cudaStream_t s) {
   // op per operand (the per-op cost, not bandwidth, bounded smaller stages).
   // Otherwise one chunk per stage through 2-D maps.
   const bool chunked = (c.K / 2) % 64 == 0;
-  if (c.mode == 0) return chunked ? run<256, 0, W4A4_STAGES, 64, W4A4_NC>(c, num_sms, s) : run<256, 0, 3, 128, 1>(c, num_sms, s);
-  return chunked ? run<256, 1, W4A8_STAGES, 64, W4A8_NC>(c, num_sms, s) : run<256, 1, 4, 64, 1>(c, num_sms, s);
+  if (c.mode == 0)
+    return chunked ? run<256, 0, W4A4_STAGES, 64, W4A4_NC, GEMM_PAIR>(c, num_sms, s)
+                   : run<256, 0, GEMM_PAIR ? 5 : 3, 128, 1, GEMM_PAIR>(c, num_sms, s);
+  return chunked ? run<256, 1, W4A8_STAGES, 64, W4A8_NC, GEMM_PAIR>(c, num_sms, s)
+                 : run<256, 1, W4A8_STAGES, 64, 1, GEMM_PAIR>(c, num_sms, s);
 }
 
 }  // namespace sixbit

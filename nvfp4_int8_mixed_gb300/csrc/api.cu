@@ -170,7 +170,7 @@ int sixbit_block_gamma(const void* in, const void* out, int64_t n, void* delta, 
   if (!aligned16(in) || !aligned16(out) || (delta && !aligned16(delta)) || !aligned16(ws)) return kEAlign;
   int sms;
   if (device_setup(&sms, nullptr) != kOk) return kELaunch;
-  return launch_block_gamma(in, out, n, delta, gamma_out, r2_out, tdc_state, computed, ws, cs(stream));
+  return launch_block_gamma(in, out, n, delta, gamma_out, r2_out, tdc_state, computed, ws, sms, cs(stream));
 }
 
 int sixbit_block_gamma_noalloc(const void* in, const void* out, int64_t n, void* delta, float* gamma_out,
@@ -178,7 +178,9 @@ int sixbit_block_gamma_noalloc(const void* in, const void* out, int64_t n, void*
   if (!in || !out || !gamma_out || n <= 0) return kEInval;
   if (n > block_gamma_noalloc_max_elems()) return kEShape;
   if (!aligned16(in) || !aligned16(out) || (delta && !aligned16(delta))) return kEAlign;
-  return launch_block_gamma_noalloc(in, out, n, delta, gamma_out, r2_out, tdc_state, computed, cs(stream));
+  int sms;
+  if (device_setup(&sms, nullptr) != kOk) return kELaunch;
+  return launch_block_gamma_noalloc(in, out, n, delta, gamma_out, r2_out, tdc_state, computed, sms, cs(stream));
 }
 
 int sixbit_dmpq_assign(const float* gamma, const float* alpha, const float* beta, const int32_t* layer_block,

@@ -16,8 +16,10 @@ namespace sixbit {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTile = 16384;                  // elements per CTA of the Gamma pass
-constexpr int kVecPerThread = kTile / (8 * kThreads);   // 8 x 16-byte vectors
+constexpr int kTile = 8192;                   // elements per tile of the Gamma pass
+constexpr int kVecPerThread = kTile / (8 * kThreads);   // 4 x 16-byte vectors per operand
+constexpr int kGammaCtasPerSm = 3;
+constexpr int kGammaMaxCtas = 1024;           // bounds the partials (and so the scratch)
 
 struct GammaWs {                              // layout of the scratch buffer
   unsigned int counter;                       // CTAs finished (reset by the last one)
@@ -46,74 +48,74 @@ __device__ __forceinline__ void block_sum4(float v[4], float (*sm)[4]) {
 //   d = f32(out) - f32(in); S1 += |d|; S0 += |in|;
 //   if computed: D_new = bf16(d) (stored over D_old); if r2 wanted:
 //   e = f32(D_new) - f32(D_old); Sd += e*e; So += D_old^2.
-// CTA partials go to scratch as float64; the last CTA sums them in tile
-// order, writes Gamma / r2 and advances the TDC counters.
-__global__ void __launch_bounds__(kThreads) gamma_kernel(const uint16_t* __restrict__ xin, const uint16_t* __restrict__ xout,
-                                                         int64_t n, uint16_t* delta, float* gamma_out, float* r2_out,
-                                                         int32_t* tdc_state, const uint8_t* computed_ptr,
-                                                         GammaWs* ws, double* partials) {
+// Persistent CTAs walk the tiles t = blockIdx, blockIdx + grid, ...; each
+// CTA's partials go to scratch as float64 and the last CTA sums them in CTA
+// order, writes Gamma / r2 and advances the TDC counters.  The grid depends
+// only on n and the SM count, so the sums are deterministic.  Three CTAs per
+// SM (<= 80 registers a thread): while some compute, the others' loads are
+// in flight.
+__global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_kernel(
+    const uint16_t* __restrict__ xin, const uint16_t* __restrict__ xout, int64_t n, uint16_t* delta, float* gamma_out,
+    float* r2_out, int32_t* tdc_state, const uint8_t* computed_ptr, GammaWs* ws, double* partials) {
   __shared__ float sm[kThreads / 32][4];
   __shared__ bool is_last;
   const bool computed = computed_ptr ? (*computed_ptr != 0) : true;
   const bool do_delta = computed && delta != nullptr;
   const bool do_r2 = do_delta && r2_out != nullptr && (tdc_state ? tdc_state[0] >= 1 : true);
-  const int64_t base = int64_t(blockIdx.x) * kTile;
+  const int64_t ntiles = cdiv(n, kTile);
   float s1 = 0.f, s0 = 0.f, sd = 0.f, so = 0.f;
-  uint4 vi[kVecPerThread], vo[kVecPerThread], vd[kVecPerThread];
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t base = t * kTile;
+    uint4 vi[kVecPerThread], vo[kVecPerThread], vd[kVecPerThread];
 #pragma unroll
-  for (int i = 0; i < kVecPerThread; ++i) {
-    const int64_t idx = base + (int64_t(i) * kThreads + threadIdx.x) * 8;
-    if (idx + 8 <= n) {
-      vi[i] = ldg_nc_v4(xin + idx);
-      vo[i] = ldg_nc_v4(xout + idx);
-      if (do_r2) vd[i] = ldg_v4(delta + idx);
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < kVecPerThread; ++i) {
-    const int64_t idx = base + (int64_t(i) * kThreads + threadIdx.x) * 8;
-    if (idx >= n) continue;
-    float fi[8], fo[8], fd[8];
-    int cnt = 8;
-    if (idx + 8 <= n) {
-      const uint32_t* a = &vi[i].x;
-      const uint32_t* b = &vo[i].x;
-      const uint32_t* c = &vd[i].x;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        fi[2 * e] = bf16lo(a[e]); fi[2 * e + 1] = bf16hi(a[e]);
-        fo[2 * e] = bf16lo(b[e]); fo[2 * e + 1] = bf16hi(b[e]);
-        if (do_r2) { fd[2 * e] = bf16lo(c[e]); fd[2 * e + 1] = bf16hi(c[e]); }
-      }
-    } else {                                  // ragged tail (scalar)
-      cnt = int(n - idx);
-      for (int e = 0; e < 8; ++e) {
-        fi[e] = e < cnt ? bf16_to_f32(xin[idx + e]) : 0.f;
-        fo[e] = e < cnt ? bf16_to_f32(xout[idx + e]) : 0.f;
-        fd[e] = (e < cnt && do_r2) ? bf16_to_f32(delta[idx + e]) : 0.f;
+    for (int i = 0; i < kVecPerThread; ++i) {
+      const int64_t idx = base + (int64_t(i) * kThreads + threadIdx.x) * 8;
+      if (idx + 8 <= n) {
+        vi[i] = ldg_nc_v4(xin + idx);
+        vo[i] = ldg_nc_v4(xout + idx);
+        if (do_r2) vd[i] = ldg_v4(delta + idx);
       }
     }
-    uint16_t dn[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float d = __fsub_rn(fo[e], fi[e]);
-      s1 += fabsf(d);
-      s0 += fabsf(fi[e]);
-      dn[e] = f32_to_bf16(d);
-      if (do_r2) {
-        const float ee = __fsub_rn(bf16_to_f32(dn[e]), fd[e]);
-        sd = __fmaf_rn(ee, ee, sd);
-        so = __fmaf_rn(fd[e], fd[e], so);
-      }
-    }
-    if (do_delta) {
-      if (cnt == 8) {
+    for (int i = 0; i < kVecPerThread; ++i) {
+      const int64_t idx = base + (int64_t(i) * kThreads + threadIdx.x) * 8;
+      if (idx >= n) continue;
+      if (idx + 8 <= n) {
+        const uint32_t* a = &vi[i].x;
+        const uint32_t* b = &vo[i].x;
+        const uint32_t* c = &vd[i].x;
         uint4 w;
-        w.x = dn[0] | (uint32_t(dn[1]) << 16); w.y = dn[2] | (uint32_t(dn[3]) << 16);
-        w.z = dn[4] | (uint32_t(dn[5]) << 16); w.w = dn[6] | (uint32_t(dn[7]) << 16);
-        *reinterpret_cast<uint4*>(delta + idx) = w;
-      } else {
-        for (int e = 0; e < cnt; ++e) delta[idx + e] = dn[e];
+        uint32_t* pw = &w.x;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float i0 = bf16lo(a[e]), i1 = bf16hi(a[e]);
+          const float d0 = __fsub_rn(bf16lo(b[e]), i0), d1 = __fsub_rn(bf16hi(b[e]), i1);
+          s1 += fabsf(d0) + fabsf(d1);
+          s0 += fabsf(i0) + fabsf(i1);
+          pw[e] = pack_bf16x2(d0, d1);         // D_new: one rounding of the fp32 difference
+          if (do_r2) {
+            const float e0 = __fsub_rn(bf16lo(pw[e]), bf16lo(c[e])), e1 = __fsub_rn(bf16hi(pw[e]), bf16hi(c[e]));
+            sd = __fmaf_rn(e1, e1, __fmaf_rn(e0, e0, sd));
+            so = __fmaf_rn(bf16hi(c[e]), bf16hi(c[e]), __fmaf_rn(bf16lo(c[e]), bf16lo(c[e]), so));
+          }
+        }
+        if (do_delta) *reinterpret_cast<uint4*>(delta + idx) = w;
+      } else {                                  // ragged tail (scalar)
+        const int cnt = int(n - idx);
+        for (int e = 0; e < cnt; ++e) {
+          const float fi = bf16_to_f32(xin[idx + e]);
+          const float d = __fsub_rn(bf16_to_f32(xout[idx + e]), fi);
+          s1 += fabsf(d);
+          s0 += fabsf(fi);
+          const uint16_t dn = f32_to_bf16(d);
+          if (do_r2) {
+            const float fd = bf16_to_f32(delta[idx + e]);
+            const float ee = __fsub_rn(bf16_to_f32(dn), fd);
+            sd = __fmaf_rn(ee, ee, sd);
+            so = __fmaf_rn(fd, fd, so);
+          }
+          if (do_delta) delta[idx + e] = dn;
+        }
       }
     }
   }
@@ -267,8 +269,8 @@ __global__ void __launch_bounds__(kThreads) layernorm_kernel(const uint16_t* __r
 // array lives on every device that loads the library, until the process
 // exits, and bounds the tensor size to kNoAllocMaxElems.
 constexpr int64_t kNoAllocMaxElems = int64_t(1) << 27;                  // 134,217,728 elements
-constexpr int64_t kNoAllocMaxTiles = kNoAllocMaxElems / kTile;           // 8192 tiles
-constexpr size_t kNoAllocBytes = 256 + size_t(kNoAllocMaxTiles) * 4 * sizeof(double);   // 262,400 bytes
+constexpr size_t kNoAllocBytes = 262400;                                 // counter + partials of <= 8192 CTAs
+static_assert(kNoAllocBytes >= 256 + size_t(kGammaMaxCtas) * 4 * sizeof(double), "no-alloc scratch");
 static __device__ __align__(256) unsigned char g_gamma_scratch[kNoAllocBytes];
 
 namespace {
@@ -295,23 +297,34 @@ void* noalloc_scratch_for_current_device() {
 int64_t block_gamma_noalloc_max_elems() { return kNoAllocMaxElems; }
 
 int launch_block_gamma_noalloc(const void* xin, const void* xout, int64_t n, void* delta, float* gamma_out,
-                               float* r2_out, int32_t* tdc_state, const uint8_t* computed, cudaStream_t s) {
+                               float* r2_out, int32_t* tdc_state, const uint8_t* computed, int num_sms,
+                               cudaStream_t s) {
   if (n > kNoAllocMaxElems) return kEShape;
   void* scratch = noalloc_scratch_for_current_device();
   if (!scratch) return kELaunch;
   // The array keeps the previous call's contents: the CTA counter must start at 0.
   if (cudaMemsetAsync(scratch, 0, 256, s) != cudaSuccess) return kELaunch;
-  return launch_block_gamma(xin, xout, n, delta, gamma_out, r2_out, tdc_state, computed, scratch, s);
+  return launch_block_gamma(xin, xout, n, delta, gamma_out, r2_out, tdc_state, computed, scratch, num_sms, s);
 }
 
-size_t gamma_ws_bytes(int64_t n) { return sizeof(GammaWs) + size_t(cdiv(n, kTile)) * 4 * sizeof(double) + 256; }
+int gamma_grid(int64_t n, int num_sms) {
+  const int64_t tiles = cdiv(n, kTile);
+  int64_t g = int64_t(num_sms) * kGammaCtasPerSm;
+  if (g > kGammaMaxCtas) g = kGammaMaxCtas;
+  return int(tiles < g ? tiles : g);
+}
+
+size_t gamma_ws_bytes(int64_t n) {
+  const int64_t tiles = cdiv(n, kTile);
+  const int64_t ctas = tiles < kGammaMaxCtas ? tiles : kGammaMaxCtas;
+  return 256 + size_t(ctas) * 4 * sizeof(double);
+}
 
 int launch_block_gamma(const void* xin, const void* xout, int64_t n, void* delta, float* gamma_out, float* r2_out,
-                       int32_t* tdc_state, const uint8_t* computed, void* ws, cudaStream_t s) {
-  const int64_t tiles = cdiv(n, kTile);
+                       int32_t* tdc_state, const uint8_t* computed, void* ws, int num_sms, cudaStream_t s) {
   GammaWs* w = static_cast<GammaWs*>(ws);
   double* partials = reinterpret_cast<double*>(static_cast<char*>(ws) + 256);
-  gamma_kernel<<<unsigned(tiles), kThreads, 0, s>>>(static_cast<const uint16_t*>(xin), static_cast<const uint16_t*>(xout),
+  gamma_kernel<<<unsigned(gamma_grid(n, num_sms)), kThreads, 0, s>>>(static_cast<const uint16_t*>(xin), static_cast<const uint16_t*>(xout),
                                                     n, static_cast<uint16_t*>(delta), gamma_out, r2_out, tdc_state,
                                                     computed, w, partials);
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;

@@ -36,6 +36,22 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
   return r & 0xFFu;
 }
 
+// Eight floats -> eight E2M1 codes in one 32-bit word, element i in nibble i
+// (round to nearest even, saturating at 6).
+__device__ __forceinline__ uint32_t e2m1x8(float f0, float f1, float f2, float f3, float f4, float f5, float f6,
+                                           float f7) {
+  uint32_t r;
+  asm("{ .reg .b8 t0, t1, t2, t3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n"
+      " mov.b32 %0, {t0, t1, t2, t3}; }"
+      : "=r"(r)
+      : "f"(f0), "f"(f1), "f"(f2), "f"(f3), "f"(f4), "f"(f5), "f"(f6), "f"(f7));
+  return r;
+}
+
 // float >= 0 -> E4M3 byte, round to nearest even, saturate at 448.
 __device__ __forceinline__ uint32_t e4m3_encode(float x) {
   uint16_t r;

@@ -197,11 +197,11 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(const T* __restri
         uint32_t w0 = 0, w1 = 0;
         if (d != 0.f) {
           const float r = __frcp_rn(d);
+          float y[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            w0 |= e2m1x2(__fmul_rn(blk[u].at(2 * e), r), __fmul_rn(blk[u].at(2 * e + 1), r)) << (8 * e);
-            w1 |= e2m1x2(__fmul_rn(blk[u].at(8 + 2 * e), r), __fmul_rn(blk[u].at(9 + 2 * e), r)) << (8 * e);
-          }
+          for (int e = 0; e < 16; ++e) y[e] = __fmul_rn(blk[u].at(e), r);
+          w0 = e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
+          w1 = e2m1x8(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
         }
         // 4 consecutive blocks (lanes 4j..4j+3) form one 32-bit word of the swizzled scale buffer
         uint32_t word = sb | (__shfl_down_sync(0xffffffffu, sb, 1) << 8);

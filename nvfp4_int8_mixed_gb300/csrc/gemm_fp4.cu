@@ -58,10 +58,6 @@ constexpr uint32_t kTmemCols = 512;
 #ifndef GEMM_PAIR
 #define GEMM_PAIR false  // true: CTA pairs with cta_group::2 MMAs (256 x 256 tiles)
 #endif
-#ifndef W4A4_NC
-#define W4A4_NC 2        // chunks of 64 bytes per stage (128 K elements)
-#define W4A4_STAGES (GEMM_PAIR ? 5 : 3)
-#endif
 #ifndef W4A8_NC
 #define W4A8_NC 1
 #define W4A8_STAGES (GEMM_PAIR ? 5 : 4)
@@ -879,15 +875,13 @@ int run(const GemmCall& c, int num_sms, cudaStream_t s) {
 }  // namespace
 
 int launch_gemm_fp4(const GemmCall& c, int num_sms, cudaStream_t s) {
-  // Measured on GB300: W4A4 prefers 128-byte K steps (fewer, larger stages),
-  // W4A8 (three MMAs per stage already) prefers more, smaller stages.
-  // K % 128 == 0: chunked maps, several 64-byte chunks per stage, one TMA
-  // op per operand (the per-op cost, not bandwidth, bounded smaller stages).
-  // Otherwise one chunk per stage through 2-D maps.
+  // W4A8 (three MMAs per K step) keeps 64-byte K steps: three planes of
+  // 128-byte rows would leave room for only two stages.  K % 128 == 0:
+  // chunked maps, one TMA op per operand; otherwise 2-D maps.
   const bool chunked = (c.K / 2) % 64 == 0;
-  if (c.mode == 0)
-    return chunked ? run<256, 0, W4A4_STAGES, 64, W4A4_NC, GEMM_PAIR>(c, num_sms, s)
-                   : run<256, 0, GEMM_PAIR ? 5 : 3, 128, 1, GEMM_PAIR>(c, num_sms, s);
+  // W4A4: 128-byte K steps (a 128-byte box row per TMA row: 7-8% faster than
+  // two 64-byte chunks); the K tail past K/2 bytes reads as zeros.
+  if (c.mode == 0) return run<256, 0, GEMM_PAIR ? 5 : 3, 128, 1, GEMM_PAIR>(c, num_sms, s);
   return chunked ? run<256, 1, W4A8_STAGES, 64, W4A8_NC, GEMM_PAIR>(c, num_sms, s)
                  : run<256, 1, W4A8_STAGES, 64, 1, GEMM_PAIR>(c, num_sms, s);
 }

@@ -364,15 +364,19 @@ def run_ours(args):
     launches_per_step = 4 * 5 + 3      # amax + nvfp4 quant + w4a4 + int8 quant + w4a8 per layer; gamma, dmpq, tdc
     stream = torch.cuda.current_stream()
 
-    def step(evs=None):
+    def step(evs=None, inp=None):
+        """One pass of the path; `inp` (optional) is a set of device inputs
+        {x: [per layer], r: [per layer], bin, bout} to use instead of the defaults."""
         k = 0
-        for l in L:
+        for li, l in enumerate(L):
+            x = inp["x"][li] if inp else l["x"]
+            r = inp["r"][li] if inp else l["r"]
             ops = [
-                lambda: sb.quantize_act_nvfp4(l["x"], out=(l["codes"], l["sf"], l["ga"])),
-                lambda: sb.qlinear_w4a4(l["codes"], l["sf"], l["ga"], l["wc"], l["wsf"], l["gw"], residual=l["r"],
+                lambda: sb.quantize_act_nvfp4(x, out=(l["codes"], l["sf"], l["ga"])),
+                lambda: sb.qlinear_w4a4(l["codes"], l["sf"], l["ga"], l["wc"], l["wsf"], l["gw"], residual=r,
                                         gelu=l["gelu"], out=l["y4"]),
-                lambda: sb.quantize_act_int8(l["x"], out=(None, l["planes"], l["s"])),
-                lambda: sb.qlinear_w4a8(l["planes"], l["s"], l["wc"], l["wsf"], l["gw"], residual=l["r"],
+                lambda: sb.quantize_act_int8(x, out=(None, l["planes"], l["s"])),
+                lambda: sb.qlinear_w4a8(l["planes"], l["s"], l["wc"], l["wsf"], l["gw"], residual=r,
                                         gelu=l["gelu"], out=l["y8"]),
             ]
             for op in ops:
@@ -382,11 +386,12 @@ def run_ours(args):
                 if evs is not None:
                     evs[k][1].record(stream)
                 k += 1
+        b_in, b_out = (inp["bin"], inp["bout"]) if inp else (bin_, bout)
         tail = [
-            lambda: sb.block_gamma(bin_, bout, delta=bdelta, gamma_out=gamma_t[0:1], r2_out=gamma_t[1:2],
+            lambda: sb.block_gamma(b_in, b_out, delta=bdelta, gamma_out=gamma_t[0:1], r2_out=gamma_t[1:2],
                                    tdc_state=state),
             lambda: sb.dmpq_assign(gamma_t[0:1], alpha, beta, lbk, 0.1, step_t, use_nvfp4=flags, gates=gates),
-            lambda: sb.tdc_decide_and_apply(bin_, bdelta, gamma_t[1:2], 0.05, 1, state, cflag, tdc_out, gates=gates),
+            lambda: sb.tdc_decide_and_apply(b_in, bdelta, gamma_t[1:2], 0.05, 1, state, cflag, tdc_out, gates=gates),
         ]
         for op in tail:
             if evs is not None:
@@ -448,27 +453,64 @@ def run_ours(args):
     d2h = res_host.numel() + 8
     out_host = torch.empty(2, dtype=torch.float32).pin_memory()
 
-    def e2e_step():
-        for (ha, hr), l in zip(pinned, L):
-            l["x"].copy_(ha, non_blocking=True)
+    # Inputs are double-buffered on the device: while the compute stream runs
+    # step s on one set, two copy streams bring step s+1's inputs into the
+    # other.  Every step copies all of its inputs from pinned host memory and
+    # reads its decisions back inside the timed region; events order a set's
+    # copies after the step that last read it.
+    sets = [dict(x=[l["x"] for l in L], r=[l["r"] for l in L], bin=bin_, bout=bout),
+            dict(x=[torch.empty_like(l["x"]) for l in L],
+                 r=[torch.empty_like(l["r"]) if l["r"] is not None else None for l in L],
+                 bin=torch.empty_like(bin_), bout=torch.empty_like(bout))]
+    copy_streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    ready = [[torch.cuda.Event() for _ in copy_streams] for _ in sets]
+    free = [torch.cuda.Event() for _ in sets]
+
+    def load(si, after=None):
+        d = sets[si]
+        jobs = []
+        for li, (ha, hr) in enumerate(pinned):
+            jobs.append((d["x"][li], ha))
             if hr is not None:
-                l["r"].copy_(hr, non_blocking=True)
-        bin_.copy_(hb[0], non_blocking=True)
-        bout.copy_(hb[1], non_blocking=True)
-        step()
+                jobs.append((d["r"][li], hr))
+        jobs += [(d["bin"], hb[0]), (d["bout"], hb[1])]
+        load_bytes = [0] * len(copy_streams)
+        for cs in copy_streams:
+            cs.wait_event(free[si])                # the step that last read this set is done
+            if after is not None:
+                cs.wait_event(after)
+        for dst, src in sorted(jobs, key=lambda j: -j[1].numel()):
+            c = load_bytes.index(min(load_bytes))  # balance bytes over the copy streams
+            with torch.cuda.stream(copy_streams[c]):
+                dst.copy_(src, non_blocking=True)
+            load_bytes[c] += src.numel() * src.element_size()
+        for c, cs in enumerate(copy_streams):
+            ready[si][c].record(cs)
+
+    def e2e_step(s, last):
+        si = s % 2
+        for ev in ready[si]:
+            stream.wait_event(ev)
+        step(inp=sets[si])
+        free[si].record(stream)
         out_host.copy_(gamma_t[0:2], non_blocking=True)
         res_host[0:4].copy_(flags, non_blocking=True)
         res_host[4:8].copy_(gates.view(-1)[0:4], non_blocking=True)
         res_host[8:9].copy_(cflag, non_blocking=True)
+        if not last:
+            load((s + 1) % 2)
 
     e2e_steps = max(3, args.steps // 4)
-    e2e_step()
+    load(0)                                        # untimed warm-up of the pipeline
+    for s in range(2):
+        e2e_step(s, last=(s == 1))
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    load(0, after=e0)                              # the first step's copies are inside the timed region
+    for s in range(e2e_steps):
+        e2e_step(s, last=(s == e2e_steps - 1))
     e1.record(stream)
     barrier()
     e2e_elapsed = e0.elapsed_time(e1) / 1e3

@@ -241,7 +241,9 @@ def run_stack_bench(name: str, dev):
     (sigma 0.3 -> 0.01) are drawn on the device from a seeded torch
     generator; (alpha, beta) ~ U(0.5,1.5) x U(0,0.01) per layer; tau is
     calibrated for ~60% NVFP4 from an all-INT8 run; TDC threshold 0.05,
-    max_skip 1.  Timed: every step's graph replay plus its input copy."""
+    max_skip 1.  Also the PDR variant "pdr": max_skip 2 with a forced
+    computed step every 4th step.  Timed: every step's graph replay plus its
+    input copy."""
     import torch
     from nvfp4_int8_mixed_gb300.stack import DiTStack, calibrate_tau
     c = STACKS[name]
@@ -265,8 +267,8 @@ def run_stack_bench(name: str, dev):
     torch.cuda.synchronize()
     tau = calibrate_tau(stack, xs)
     res = {"config": f"{nb} blocks, M={M}, H={H}, F={F}, {T} steps", "tau": tau}
-    for mode, max_skip in (("dmpq_tdc", 1), ("dmpq_only", 0)):
-        stack.tau, stack.max_skip = tau, max_skip
+    for mode, max_skip, refresh in (("dmpq_tdc", 1, 0), ("dmpq_only", 0, 0), ("pdr_skip2_refresh4", 2, 4)):
+        stack.tau, stack.max_skip, stack.refresh_every = tau, max_skip, refresh
         stack.graph = None
         stack.reset()
         stack.capture()

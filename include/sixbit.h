@@ -187,12 +187,19 @@ int sixbit_dmpq_assign(const float* gamma, const float* alpha, const float* beta
 
 /* a9 -- TDC decision and reuse (Figure 2: skip from the updates of the two
  * preceding steps; "Abstract": skip invariant blocks).
- *   skip = tdc_state[0] >= 2 && r2[0] < f32(tau_tdc^2) && tdc_state[1] < max_skip
+ *   refresh = refresh_every > 0 && *step % refresh_every == 0
+ *   skip = !refresh && tdc_state[0] >= 2 && r2[0] < f32(tau_tdc^2)
+ *          && tdc_state[1] < max_skip
  * compute_out[0] = !skip.  If skip: out = bf16(f32(in) + f32(delta)) over n
  * elements and gates[0..n_gates) are cleared (so the block's kernels exit).
- * The counters are advanced by sixbit_block_gamma, not here. */
+ * The counters are advanced by sixbit_block_gamma, not here.
+ * max_skip > 1 and refresh_every > 0 are the PDR variants (Table 3 names
+ * "PDR" without defining it): consecutive reuses allowed, and a forced
+ * computed step every refresh_every steps.  refresh_every = 0: off (then
+ * step may be NULL); step: device int32, the denoising step index. */
 int sixbit_tdc_decide_and_apply(const void* in, const void* delta, int64_t n, const float* r2,
-                                float tau_tdc, int32_t max_skip, const int32_t* tdc_state,
+                                float tau_tdc, int32_t max_skip, int32_t refresh_every,
+                                const int32_t* step, const int32_t* tdc_state,
                                 uint8_t* compute_out, void* out, uint8_t* gates, int32_t n_gates,
                                 sixbit_stream_t stream);
 

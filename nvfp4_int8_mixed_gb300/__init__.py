@@ -42,7 +42,7 @@ _SIGS = {
     "sixbit_block_gamma": ([_P, _P, _I64, _P, _P, _P, _P, _P, _P, _P], _INT),
     "sixbit_block_gamma_noalloc": ([_P, _P, _I64, _P, _P, _P, _P, _P, _P], _INT),
     "sixbit_dmpq_assign": ([_P, _P, _P, _P, _I32, _F, _P, _P, _P, _P], _INT),
-    "sixbit_tdc_decide_and_apply": ([_P, _P, _I64, _P, _F, _I32, _P, _P, _P, _P, _I32, _P], _INT),
+    "sixbit_tdc_decide_and_apply": ([_P, _P, _I64, _P, _F, _I32, _I32, _P, _P, _P, _P, _P, _I32, _P], _INT),
     "sixbit_layernorm_bf16": ([_P, _I64, _I64, _I64, _F, _P, _I64, _P, _P, _P, _P], _INT),
     "sixbit_get_error": ([_P], _INT),
 }
@@ -232,13 +232,17 @@ def dmpq_assign(gamma, alpha, beta, layer_block, tau: float, step, use_nvfp4=Non
     return f
 
 
-def tdc_decide_and_apply(xin, delta, r2, tau_tdc: float, max_skip: int, tdc_state, compute_out, out, gates=None):
-    """a9: compute_out[0] = 1 if the block must run; on a skip out = in + Delta."""
+def tdc_decide_and_apply(xin, delta, r2, tau_tdc: float, max_skip: int, tdc_state, compute_out, out, gates=None,
+                         refresh_every: int = 0, step=None):
+    """a9: compute_out[0] = 1 if the block must run; on a skip out = in + Delta.
+    refresh_every > 0 (with step, a device int32) forces a computed step every
+    refresh_every steps."""
     n = xin.numel()
     _check("sixbit_tdc_decide_and_apply",
            lib().sixbit_tdc_decide_and_apply(_ptr(xin), _ptr(delta), n, _ptr(r2), float(tau_tdc), int(max_skip),
-                                             _ptr(tdc_state), _ptr(compute_out), _ptr(out), _ptr(gates),
-                                             gates.numel() if gates is not None else 0, _stream()))
+                                             int(refresh_every), _ptr(step), _ptr(tdc_state), _ptr(compute_out),
+                                             _ptr(out), _ptr(gates), gates.numel() if gates is not None else 0,
+                                             _stream()))
     return compute_out
 
 

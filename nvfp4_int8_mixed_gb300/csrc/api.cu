@@ -191,15 +191,17 @@ int sixbit_dmpq_assign(const float* gamma, const float* alpha, const float* beta
 }
 
 int sixbit_tdc_decide_and_apply(const void* in, const void* delta, int64_t n, const float* r2, float tau_tdc,
-                                int32_t max_skip, const int32_t* tdc_state, uint8_t* compute_out, void* out,
-                                uint8_t* gates, int32_t n_gates, sixbit_stream_t stream) {
+                                int32_t max_skip, int32_t refresh_every, const int32_t* step,
+                                const int32_t* tdc_state, uint8_t* compute_out, void* out, uint8_t* gates,
+                                int32_t n_gates, sixbit_stream_t stream) {
   if (!in || !delta || !r2 || !tdc_state || !compute_out || !out || n <= 0 || (gates && n_gates < 0)) return kEInval;
+  if (refresh_every < 0 || (refresh_every > 0 && !step)) return kEInval;
   if (!aligned16(in) || !aligned16(delta) || !aligned16(out)) return kEAlign;
   int sms;
   if (device_setup(&sms, nullptr) != kOk) return kELaunch;
   const float tau2 = tau_tdc * tau_tdc;   // float32 product, round to nearest
-  return launch_tdc(in, delta, n, r2, tau2, max_skip, tdc_state, compute_out, out, gates, gates ? n_gates : 0, sms,
-                    cs(stream));
+  return launch_tdc(in, delta, n, r2, tau2, max_skip, refresh_every, step, tdc_state, compute_out, out, gates,
+                    gates ? n_gates : 0, sms, cs(stream));
 }
 
 int sixbit_layernorm_bf16(const void* x, int64_t M, int64_t H, int64_t ldx, float eps, void* y, int64_t ldy,

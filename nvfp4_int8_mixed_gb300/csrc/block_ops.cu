@@ -174,12 +174,16 @@ __global__ void dmpq_kernel(const float* __restrict__ gamma, const float* __rest
 }
 
 // a9: every CTA evaluates the (read-only) decision; CTA 0 publishes it; on a
-// skip all CTAs write out = bf16(f32(in) + f32(delta)).
+// skip all CTAs write out = bf16(f32(in) + f32(delta)).  refresh_every > 0
+// (a periodic-refresh PDR variant) forces a computed step whenever
+// *step % refresh_every == 0.
 __global__ void __launch_bounds__(kThreads) tdc_kernel(const uint16_t* __restrict__ xin, const uint16_t* __restrict__ delta,
                                                        int64_t n, const float* r2, float tau2, int32_t max_skip,
+                                                       int32_t refresh_every, const int32_t* step,
                                                        const int32_t* tdc_state, uint8_t* compute_out,
                                                        uint16_t* __restrict__ out, uint8_t* gates, int32_t n_gates) {
-  const bool skip = tdc_state[0] >= 2 && *r2 < tau2 && tdc_state[1] < max_skip;
+  const bool refresh = refresh_every > 0 && (*step % refresh_every) == 0;
+  const bool skip = !refresh && tdc_state[0] >= 2 && *r2 < tau2 && tdc_state[1] < max_skip;
   if (blockIdx.x == 0) {
     if (threadIdx.x == 0) *compute_out = skip ? 0 : 1;
     if (skip && gates)
@@ -339,14 +343,14 @@ int launch_dmpq(const float* gamma, const float* alpha, const float* beta, const
 }
 
 int launch_tdc(const void* xin, const void* delta, int64_t n, const float* r2, float tau2, int32_t max_skip,
-               const int32_t* tdc_state, uint8_t* compute_out, void* out, uint8_t* gates, int32_t n_gates,
-               int num_sms, cudaStream_t s) {
+               int32_t refresh_every, const int32_t* step, const int32_t* tdc_state, uint8_t* compute_out, void* out,
+               uint8_t* gates, int32_t n_gates, int num_sms, cudaStream_t s) {
   int64_t want = cdiv(n / 8 + 1, kThreads * 4);
   int64_t cap = int64_t(num_sms) * 8;
   const unsigned grid = unsigned(want < cap ? (want < 1 ? 1 : want) : cap);
   tdc_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(xin), static_cast<const uint16_t*>(delta), n, r2,
-                                       tau2, max_skip, tdc_state, compute_out, static_cast<uint16_t*>(out), gates,
-                                       n_gates);
+                                       tau2, max_skip, refresh_every, step, tdc_state, compute_out,
+                                       static_cast<uint16_t*>(out), gates, n_gates);
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 

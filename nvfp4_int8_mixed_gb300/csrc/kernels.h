@@ -23,6 +23,7 @@ int launch_block_gamma_noalloc(const void* xin, const void* xout, int64_t n, voi
 int launch_dmpq(const float* gamma, const float* alpha, const float* beta, const int32_t* layer_block,
                 int32_t n_layers, float tau, const int32_t* step, uint8_t* use_nvfp4, uint8_t* gates, cudaStream_t s);
 int launch_tdc(const void* xin, const void* delta, int64_t n, const float* r2, float tau2, int32_t max_skip,
+               int32_t refresh_every, const int32_t* step,
                const int32_t* tdc_state, uint8_t* compute_out, void* out, uint8_t* gates, int32_t n_gates,
                int num_sms, cudaStream_t s);
 int launch_layernorm(const void* x, int64_t M, int64_t H, int64_t ldx, float eps, void* y, int64_t ldy,

@@ -33,15 +33,17 @@ class DiTStack:
     weights: list (per block) of dicts qkv [3H,H], out [H,H], up [F,H], down [H,F]
     (float32 numpy or torch); alpha, beta: per-layer predictor lines (4 per
     block, layer order qkv, out, up, down); tau: DMPQ threshold; tau_tdc,
-    max_skip: TDC rule (max_skip = 0 disables skipping).
+    max_skip: TDC rule (max_skip = 0 disables skipping); refresh_every: PDR
+    periodic refresh (every k-th step is computed; 0 = off).
     """
 
     def __init__(self, weights, alpha, beta, M: int, H: int, F: int, tau: float, tau_tdc: float = 0.05,
-                 max_skip: int = 1, device=None):
+                 max_skip: int = 1, device=None, refresh_every: int = 0):
         self.dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
         dev = self.dev
         self.nb, self.M, self.H, self.F = len(weights), M, H, F
         self.tau, self.tau_tdc, self.max_skip = float(tau), float(tau_tdc), int(max_skip)
+        self.refresh_every = int(refresh_every)
         nl = 4 * self.nb
         to_t = lambda a: torch.as_tensor(np.asarray(a, np.float32)).to(dev)
         self.alpha, self.beta = to_t(alpha), to_t(beta)
@@ -100,7 +102,7 @@ class DiTStack:
             gates = self.gates[4 * l:4 * l + 4]
             c = self.cflag[l:l + 1]
             tdc_decide_and_apply(h, self.delta[l], self.r2[l:l + 1], self.tau_tdc, self.max_skip, self.state[l],
-                                 c, out, gates=gates)
+                                 c, out, gates=gates, refresh_every=self.refresh_every, step=self.step_dev)
             g = lambda i, f: gates[i, f:f + 1]
             layernorm(h, LN_EPS, out=self.h1, amax_out=self.amax, row_amax_out=self.row_amax, pred=c)
             self._ql(self.h1, self.wq[l]["qkv"], g(0, 0), g(0, 1), self.qkv, amax_in=self.amax,

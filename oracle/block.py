@@ -70,7 +70,7 @@ def block_forward(x_bits, wq_block, flags):
 
 
 def run_stack(x_steps, wq_blocks, alpha, beta, tau, tau_tdc, max_skip=1, use_tdc=True,
-              forced_flags=None, forced_skips=None):
+              forced_flags=None, forced_skips=None, refresh_every=0):
     """Run every step.  Returns dict(outputs, flags[t], skips[t], gammas[t], r2[t]).
 
     forced_flags (optional) [steps][layers] replaces DMPQ's decisions and
@@ -95,7 +95,7 @@ def run_stack(x_steps, wq_blocks, alpha, beta, tau, tau_tdc, max_skip=1, use_tdc
             if forced_skips is not None:
                 skip = bool(forced_skips[t][l])
             else:
-                skip = use_tdc and tdc.decide(c, tau_tdc, max_skip)
+                skip = use_tdc and tdc.decide(c, tau_tdc, max_skip, refresh_every, t)
             if skip:
                 out = tdc.apply(h, c.delta)
                 tdc.after_skip(c)

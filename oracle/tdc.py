@@ -19,9 +19,18 @@ Readings (no rule is printed):
   * a computed block stores its new update, measures r2 against the old one
     (if any), fresh_count + 1, consec = 0.
 
+PDR ("Table 3" names it as a component; the pages give no definition).
+Variants of the reading above, each a parameter of the same rule:
+  * "purified" Delta: Delta is replaced only by a computed step, so a reused
+    update never feeds the next one (the default above);
+  * max_skip > 1: up to max_skip consecutive reuses;
+  * periodic refresh: with refresh_every = k > 0, a step t with t % k == 0 is
+    always computed, whatever r2 says.
+
 Parity: pinned (tau_tdc = 0 never skips; max_skip = 0 never skips; a forced
-skip gives out - in equal to Delta up to one bf16 rounding; a hand-written
-r2 sequence gives a hand-derived skip pattern).
+skip gives out - in equal to Delta up to one bf16 rounding; hand-written r2
+sequences give hand-derived skip patterns, also with max_skip = 2 and a
+periodic refresh).
 """
 from __future__ import annotations
 
@@ -42,7 +51,9 @@ class BlockCache:
     delta: np.ndarray | None = None       # bf16 bits
 
 
-def decide(cache: BlockCache, tau_tdc: float, max_skip: int) -> bool:
+def decide(cache: BlockCache, tau_tdc: float, max_skip: int, refresh_every: int = 0, step: int = 0) -> bool:
+    if refresh_every > 0 and step % refresh_every == 0:
+        return False                       # periodic refresh: this step is computed
     t2 = F32(F32(tau_tdc) * F32(tau_tdc))
     return cache.fresh_count >= 2 and F32(cache.r2) < t2 and cache.consec < max_skip
 

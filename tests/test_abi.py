@@ -73,7 +73,10 @@ def test_argument_errors_before_launch(lib):
                                    None, None) == sb.EINVAL
     assert lib.sixbit_block_gamma(fake, fake, 0, None, fake, None, None, None, fake, None) == sb.EINVAL
     assert lib.sixbit_dmpq_assign(fake, fake, fake, fake, 0, ctypes.c_float(0.1), fake, fake, None, None) == sb.EINVAL
-    assert lib.sixbit_tdc_decide_and_apply(fake, fake, 16, fake, ctypes.c_float(0.05), 1, None, fake, fake, None, 0,
-                                           None) == sb.EINVAL
+    assert lib.sixbit_tdc_decide_and_apply(fake, fake, 16, fake, ctypes.c_float(0.05), 1, 0, None, None, fake, fake,
+                                           None, 0, None) == sb.EINVAL
+    # a periodic refresh needs the step counter
+    assert lib.sixbit_tdc_decide_and_apply(fake, fake, 16, fake, ctypes.c_float(0.05), 1, 3, None, fake, fake, fake,
+                                           None, 0, None) == sb.EINVAL
     assert lib.sixbit_layernorm_bf16(fake, 4, 20, 20, ctypes.c_float(1e-5), fake, 20, None, None, None,
                                      None) == sb.ESHAPE

@@ -86,10 +86,13 @@ def test_dmpq_bit_exact():
     assert host(f)[7] == 0
 
 
-@pytest.mark.parametrize("fresh,consec,r2,tau,max_skip", [
-    (2, 0, 0.001, 0.05, 1), (1, 0, 0.0, 0.05, 1), (2, 1, 0.001, 0.05, 1), (2, 0, 0.0025, 0.05, 1),
-    (5, 1, 0.001, 0.05, 2), (2, 0, 0.001, 0.0, 1), (2, 0, np.inf, 0.05, 1)])
-def test_tdc_decide_and_apply(fresh, consec, r2, tau, max_skip):
+@pytest.mark.parametrize("fresh,consec,r2,tau,max_skip,refresh,step", [
+    (2, 0, 0.001, 0.05, 1, 0, 0), (1, 0, 0.0, 0.05, 1, 0, 0), (2, 1, 0.001, 0.05, 1, 0, 0),
+    (2, 0, 0.0025, 0.05, 1, 0, 0), (5, 1, 0.001, 0.05, 2, 0, 0), (2, 0, 0.001, 0.0, 1, 0, 0),
+    (2, 0, np.inf, 0.05, 1, 0, 0),
+    # periodic refresh (PDR variant): step % k == 0 forces a computed step
+    (2, 0, 0.001, 0.05, 1, 3, 6), (2, 0, 0.001, 0.05, 1, 3, 7), (5, 1, 0.001, 0.05, 2, 4, 9), (5, 1, 0.001, 0.05, 2, 4, 12)])
+def test_tdc_decide_and_apply(fresh, consec, r2, tau, max_skip, refresh, step):
     sb = _sb()
     M, H = 37, 104
     p = synthetic.gamma_pair(4, M, H)
@@ -98,10 +101,11 @@ def test_tdc_decide_and_apply(fresh, consec, r2, tau, max_skip):
     cflag = torch.full((1,), 7, dtype=torch.uint8, device="cuda")
     out = torch.zeros((M, H), dtype=torch.bfloat16, device="cuda")
     gates = torch.ones(8, dtype=torch.uint8, device="cuda")
+    step_t = torch.tensor([step], dtype=torch.int32, device="cuda")
     sb.tdc_decide_and_apply(xin, dl, torch.tensor([np.float32(r2)], device="cuda"), tau, max_skip, state, cflag, out,
-                            gates=gates)
+                            gates=gates, refresh_every=refresh, step=step_t)
     cache = o_tdc.BlockCache(fresh_count=fresh, consec=consec, r2=np.float32(r2))
-    skip = o_tdc.decide(cache, tau, max_skip)
+    skip = o_tdc.decide(cache, tau, max_skip, refresh, step)
     assert host(cflag)[0] == (0 if skip else 1)
     assert host(state).tolist() == [fresh, consec]           # counters advance in the Gamma pass
     if skip:

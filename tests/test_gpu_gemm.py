@@ -135,6 +135,17 @@ def test_pred_zero_skips_gemm():
 def test_2b_shapes_sampled_rows(name, K, N, gelu, use_res):
     """Config-2 shapes at full size in the bench's launch configuration; the
     oracle checks a sample of rows (all N columns)."""
+    _full_shape_sampled_rows(K, N, gelu, use_res)
+
+
+@pytest.mark.parametrize("name,K,N,gelu,use_res", synthetic.GEMM_SHAPES["5B"])
+def test_5b_shapes_sampled_rows(name, K, N, gelu, use_res):
+    """Config-3 shapes (5B-class set, M=17776, K 3072/12288, N up to 12288) at
+    full size; the oracle checks a sample of rows (all N columns)."""
+    _full_shape_sampled_rows(K, N, gelu, use_res)
+
+
+def _full_shape_sampled_rows(K, N, gelu, use_res):
     sb = _sb()
     M = synthetic.M_2B
     lay = synthetic.gemm_layer(1, M, K, N, use_res)

@@ -108,8 +108,17 @@ def test_int8_caller_row_amax_saturates():
 def test_quantizers_full_2b_shape_sampled_rows():
     """Config-2 activation (M=17776, K=1920 and 7680): every row through the
     kernels, a sample of rows through the oracle with the tensor amax."""
+    _quantizers_full_shape(1920, 7680)
+
+
+def test_quantizers_full_5b_shape_sampled_rows():
+    """Config-3 activation (M=17776, K=3072 and 12288), as above."""
+    _quantizers_full_shape(3072, 12288)
+
+
+def _quantizers_full_shape(*Ks):
     sb = _sb()
-    for K in (1920, 7680):
+    for K in Ks:
         lay = synthetic.gemm_layer(1, synthetic.M_2B, K, 128, False)
         a = lay["a"]
         x = dev_bf16(a)

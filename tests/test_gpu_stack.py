@@ -17,12 +17,13 @@ from tests.helpers import dev_bf16, host, host_bf16_bits
 pytestmark = pytest.mark.gpu
 
 
-def _run(tau_tdc, max_skip, nb=3, M=300, H=256, F=512, steps=6, seed=7):
+def _run(tau_tdc, max_skip, nb=3, M=300, H=256, F=512, steps=6, seed=7, refresh=0):
     from nvfp4_int8_mixed_gb300.stack import DiTStack, calibrate_tau
     st = synthetic.stack_setup(seed, nb, H, F)
     xs = synthetic.stack_inputs(st["noise_seed"], M, H, steps)
     xs_dev = [dev_bf16(x) for x in xs]
-    stack = DiTStack(st["blocks"], st["alpha"], st["beta"], M, H, F, tau=0.0, tau_tdc=tau_tdc, max_skip=max_skip)
+    stack = DiTStack(st["blocks"], st["alpha"], st["beta"], M, H, F, tau=0.0, tau_tdc=tau_tdc, max_skip=max_skip,
+                     refresh_every=refresh)
     tau = calibrate_tau(stack, xs_dev)
     stack.tau = tau
     outs, log = stack.run(xs_dev, record=True)
@@ -31,9 +32,10 @@ def _run(tau_tdc, max_skip, nb=3, M=300, H=256, F=512, steps=6, seed=7):
     return st, xs, tau, [host_bf16_bits(o) for o in outs], rec
 
 
-@pytest.mark.parametrize("tau_tdc,max_skip", [(0.0, 1), (10.0, 1), (0.05, 1)])
-def test_stack_decisions_and_outputs(tau_tdc, max_skip):
-    st, xs, tau, outs, rec = _run(tau_tdc, max_skip)
+@pytest.mark.parametrize("tau_tdc,max_skip,refresh", [(0.0, 1, 0), (10.0, 1, 0), (0.05, 1, 0),
+                                                      (10.0, 3, 3)])    # PDR: 3 reuses, refresh every 3rd step
+def test_stack_decisions_and_outputs(tau_tdc, max_skip, refresh):
+    st, xs, tau, outs, rec = _run(tau_tdc, max_skip, refresh=refresh, steps=8 if refresh else 6)
     nb = len(st["blocks"])
     lb = np.repeat(np.arange(nb), 4)
     steps = len(xs)
@@ -50,7 +52,7 @@ def test_stack_decisions_and_outputs(tau_tdc, max_skip):
             else:
                 c = o_tdc.BlockCache(fresh_count=int(rec["state"][t - 1][l, 0]), consec=int(rec["state"][t - 1][l, 1]),
                                      r2=np.float32(rec["r2"][t - 1][l]))
-                want = o_tdc.decide(c, tau_tdc, max_skip)
+                want = o_tdc.decide(c, tau_tdc, max_skip, refresh, t)
             assert bool(rec["skips"][t][l]) == want, (t, l)
     # outputs under the same decisions
     wq = [{k: o_block.quantize_weights(v) for k, v in b.items()} for b in st["blocks"]]
@@ -69,6 +71,8 @@ def test_stack_decisions_and_outputs(tau_tdc, max_skip):
         assert not skips.any()
     if tau_tdc == 10.0:
         assert skips.any()
+    if refresh:
+        assert not skips[::refresh].any() and skips[2].all() and skips[4].all() and skips[5].all()
 
 
 def test_stack_graph_replay_is_deterministic():

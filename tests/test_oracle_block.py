@@ -49,6 +49,14 @@ def test_stack_skip_reuses_delta():
     assert skips[2].all() and not skips[3].any() and skips[4].all()   # max_skip = 1 alternates
 
 
+def test_stack_periodic_refresh_computes_every_kth_step():
+    st, wq, xs = _tiny_stack(steps=8)
+    r = block.run_stack(xs, wq, st["alpha"], st["beta"], 0.05, 10.0, 3, refresh_every=3)
+    skips = np.array(r["skips"])
+    assert not skips[[0, 3, 6]].any()              # refresh steps are computed
+    assert skips[2].all() and skips[4].all() and skips[5].all() and skips[7].all()
+
+
 def test_block_residual_wiring_with_zero_weights():
     # all weights zero: every linear outputs 0 (+ residual), GELU(0) = 0, so out == in exactly
     rng = np.random.default_rng(3)

@@ -101,6 +101,27 @@ def test_tdc_state_machine_hand_sequence():
     assert "".join(seq) == "CCSCSCCS"
 
 
+def test_tdc_pdr_variants_hand_sequences():
+    # every computed step yields r2 = 1e-4 < tau^2: skips are limited only by
+    # fresh_count, max_skip and the periodic refresh
+    def run(max_skip, refresh_every, steps=12):
+        c = tdc.BlockCache()
+        seq = []
+        for t in range(steps):
+            if tdc.decide(c, 0.05, max_skip, refresh_every, t):
+                tdc.after_skip(c)
+                seq.append("S")
+            else:
+                tdc.after_compute(c, np.zeros(1, np.uint16), 1e-4 if c.delta is not None else None)
+                seq.append("C")
+        return "".join(seq)
+    assert run(1, 0) == "CCSCSCSCSCSC"          # max_skip 1 alternates after two fresh updates
+    assert run(2, 0) == "CCSSCSSCSSCS"          # two reuses between computed steps
+    # refresh every 4 steps: t = 0, 4, 8 computed whatever the rule says
+    assert run(2, 4) == "CCSSCSSCCSSC"
+    assert run(1, 3) == "CCSCSCCSCCSC"
+
+
 def test_tdc_never_skips_with_zero_threshold_or_zero_max_skip():
     c = tdc.BlockCache(fresh_count=5, consec=0, r2=np.float32(0.0), delta=None)
     assert not tdc.decide(c, 0.0, 1)                      # r2 < 0 is impossible

@@ -229,7 +229,7 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- DiT stack
 STACKS = {
-    "2b": dict(n_blocks=30, M=synthetic.M_2B, H=1920, F=7680, steps=50, seed=3),
+    "2b": dict(n_blocks=30, M=synthetic.M_2B, H=1920, F=7680, steps=50, seed=3, calib_steps=10),
     "5b": dict(n_blocks=42, M=2 * synthetic.M_2B, H=3072, F=12288, steps=50, seed=4),   # CFG batch 2
 }
 
@@ -242,10 +242,12 @@ def run_stack_bench(name: str, dev):
     generator; (alpha, beta) ~ U(0.5,1.5) x U(0,0.01) per layer; tau is
     calibrated for ~60% NVFP4 from an all-INT8 run; TDC threshold 0.05,
     max_skip 1.  Also the PDR variant "pdr": max_skip 2 with a forced
-    computed step every 4th step.  Timed: every step's graph replay plus its
-    input copy."""
+    computed step every 4th step, and "measured_lines": (alpha, beta) refitted
+    from E_rel measured on the first calib_steps steps (DMPQ calibration side)
+    with tau set from them.  Timed: every step's graph replay plus its input
+    copy."""
     import torch
-    from nvfp4_int8_mixed_gb300.stack import DiTStack, calibrate_tau
+    from nvfp4_int8_mixed_gb300.stack import DiTStack, calibrate_lines, calibrate_tau
     c = STACKS[name]
     nb, M, H, F, T = c["n_blocks"], c["M"], c["H"], c["F"], c["steps"]
     gen = torch.Generator(device=dev).manual_seed(c["seed"])
@@ -263,11 +265,26 @@ def run_stack_bench(name: str, dev):
         xs.append(x.to(torch.bfloat16))
     del x
     stack = DiTStack(weights, alpha, beta, M, H, F, tau=0.0, tau_tdc=0.05, max_skip=1, device=dev)
-    del weights
     torch.cuda.synchronize()
     tau = calibrate_tau(stack, xs)
     res = {"config": f"{nb} blocks, M={M}, H={H}, F={F}, {T} steps", "tau": tau}
-    for mode, max_skip, refresh in (("dmpq_tdc", 1, 0), ("dmpq_only", 0, 0), ("pdr_skip2_refresh4", 2, 4)):
+    runs = [("dmpq_tdc", 1, 0, None), ("dmpq_only", 0, 0, None), ("pdr_skip2_refresh4", 2, 4, None)]
+    if c.get("calib_steps"):
+        cal = calibrate_lines(stack, xs, weights, steps=c["calib_steps"])
+        lines = (cal["alpha"].astype(np.float32), cal["beta"].astype(np.float32))
+        fin = lambda a: float(np.nanmean(a))
+        res["calibration"] = {"steps": c["calib_steps"], "e_rel_nvfp4_mean": fin(cal["e_rel_nvfp4"]),
+                              "e_rel_int8_mean": fin(cal["e_rel_int8"]), "fit_r2_mean": fin(cal["r2"]),
+                              "alpha_mean": fin(cal["alpha"]), "beta_mean": fin(cal["beta"]),
+                              "delta_cos_mean": fin(cal["delta_cos"]), "delta_rel_mean": fin(cal["delta_rel"])}
+        runs.append(("measured_lines", 1, 0, lines))
+    del weights
+    for mode, max_skip, refresh, lines in runs:
+        if lines is not None:
+            stack.alpha.copy_(torch.from_numpy(lines[0]))
+            stack.beta.copy_(torch.from_numpy(lines[1]))
+            tau = calibrate_tau(stack, xs)
+            res["calibration"]["tau"] = tau
         stack.tau, stack.max_skip, stack.refresh_every = tau, max_skip, refresh
         stack.graph = None
         stack.reset()

@@ -174,6 +174,18 @@ int sixbit_block_gamma_noalloc(const void* in, const void* out, int64_t n, void*
                                float* gamma_out, float* r2_out, int32_t* tdc_state,
                                const uint8_t* computed, sixbit_stream_t stream);
 
+/* DMPQ calibration diagnostic (Figure 1: per-layer relative L2 quantization
+ * error; Figure 4: updates compared by cosine similarity and relative L2).
+ * One pass over two tensors of n elements (a_dtype, b_dtype: SIXBIT_BF16 or
+ * SIXBIT_F32; n % 8 == 0; 16-byte aligned):
+ *   out[0..3] = float64 {sum (a-b)^2, sum b^2, sum a*b, sum a^2}
+ * so ||a-b||/||b|| = sqrt(out[0]/out[1]) and cos = out[2]/sqrt(out[3]*out[1]).
+ * Sums: fp32 per thread, float64 across CTAs in a fixed order
+ * (deterministic).  ws: sixbit_workspace_size(n, 1) bytes of scratch; out:
+ * 4 device doubles. */
+int sixbit_pair_stats(const void* a, int a_dtype, const void* b, int b_dtype, int64_t n,
+                      double* out, void* ws, sixbit_stream_t stream);
+
 /* a8 -- DMPQ assignment (Figure 3: per-layer line E_rel = alpha*Gamma_{t-1}
  * + beta; "Abstract": NVFP4 for stable layers).  For each layer l:
  *   p = f32(f32(alpha[l]*gamma[layer_block[l]]) + beta[l]);

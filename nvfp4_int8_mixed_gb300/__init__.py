@@ -42,6 +42,7 @@ _SIGS = {
     "sixbit_block_gamma": ([_P, _P, _I64, _P, _P, _P, _P, _P, _P, _P], _INT),
     "sixbit_block_gamma_noalloc": ([_P, _P, _I64, _P, _P, _P, _P, _P, _P], _INT),
     "sixbit_dmpq_assign": ([_P, _P, _P, _P, _I32, _F, _P, _P, _P, _P], _INT),
+    "sixbit_pair_stats": ([_P, _I32, _P, _I32, _I64, _P, _P, _P], _INT),
     "sixbit_tdc_decide_and_apply": ([_P, _P, _I64, _P, _F, _I32, _I32, _P, _P, _P, _P, _P, _I32, _P], _INT),
     "sixbit_layernorm_bf16": ([_P, _I64, _I64, _I64, _F, _P, _I64, _P, _P, _P, _P], _INT),
     "sixbit_get_error": ([_P], _INT),
@@ -220,6 +221,23 @@ def block_gamma(xin, xout, delta=None, gamma_out=None, r2_out=None, tdc_state=No
            lib().sixbit_block_gamma(_ptr(xin), _ptr(xout), n, _ptr(delta), _ptr(g), _ptr(r2), _ptr(tdc_state),
                                     _ptr(computed), _ptr(_ws_for(n)), _stream()))
     return g, r2
+
+
+def pair_stats(a, b, out=None):
+    """Calibration diagnostic: float64 device tensor [4] = {sum (a-b)^2,
+    sum b^2, sum a*b, sum a^2} over two same-size bf16/fp32 tensors."""
+    _need_cuda(a, b)
+    if a.numel() != b.numel():
+        raise ValueError("pair_stats: size mismatch")
+    dt = {torch.bfloat16: BF16, torch.float32: F32}
+    if a.dtype not in dt or b.dtype not in dt:
+        raise ValueError("pair_stats: bf16 or fp32 tensors")
+    a, b = a.contiguous(), b.contiguous()
+    n = a.numel()
+    o = out if out is not None else torch.empty(4, dtype=torch.float64, device=a.device)
+    _check("sixbit_pair_stats", lib().sixbit_pair_stats(_ptr(a), dt[a.dtype], _ptr(b), dt[b.dtype], n, _ptr(o),
+                                                        _ptr(_ws_for(n)), _stream()))
+    return o
 
 
 def dmpq_assign(gamma, alpha, beta, layer_block, tau: float, step, use_nvfp4=None, gates=None):

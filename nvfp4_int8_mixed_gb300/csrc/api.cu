@@ -183,6 +183,18 @@ int sixbit_block_gamma_noalloc(const void* in, const void* out, int64_t n, void*
   return launch_block_gamma_noalloc(in, out, n, delta, gamma_out, r2_out, tdc_state, computed, sms, cs(stream));
 }
 
+int sixbit_pair_stats(const void* a, int a_dtype, const void* b, int b_dtype, int64_t n, double* out, void* ws,
+                      sixbit_stream_t stream) {
+  if (!a || !b || !out || !ws || n <= 0) return kEInval;
+  if ((a_dtype != SIXBIT_BF16 && a_dtype != SIXBIT_F32) || (b_dtype != SIXBIT_BF16 && b_dtype != SIXBIT_F32))
+    return kEInval;
+  if (n % 8 != 0) return kEShape;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(ws) || (reinterpret_cast<uintptr_t>(out) & 7u)) return kEAlign;
+  int sms;
+  if (device_setup(&sms, nullptr) != kOk) return kELaunch;
+  return launch_pair_stats(a, a_dtype == SIXBIT_F32, b, b_dtype == SIXBIT_F32, n, out, ws, sms, cs(stream));
+}
+
 int sixbit_dmpq_assign(const float* gamma, const float* alpha, const float* beta, const int32_t* layer_block,
                        int32_t n_layers, float tau, const int32_t* step, uint8_t* use_nvfp4, uint8_t* gates,
                        sixbit_stream_t stream) {

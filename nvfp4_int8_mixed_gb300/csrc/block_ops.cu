@@ -161,6 +161,77 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_kernel(
   }
 }
 
+// Calibration diagnostic (DMPQ side, Figures 1 and 4): one pass over two
+// tensors, {sum (a-b)^2, sum b^2, sum a*b, sum a^2}.  Same shape as the Gamma
+// pass: persistent CTAs over 8192-element tiles, fp32 per thread, float64
+// per CTA, the last CTA sums the partials in CTA order (deterministic).
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, int64_t i, float (&v)[8]);
+template <>
+__device__ __forceinline__ void load8<uint16_t>(const uint16_t* p, int64_t i, float (&v)[8]) {
+  const uint4 w = ldg_nc_v4(p + i);
+  const uint32_t* pw = &w.x;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) { v[2 * e] = bf16lo(pw[e]); v[2 * e + 1] = bf16hi(pw[e]); }
+}
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, int64_t i, float (&v)[8]) {
+  const uint4 w0 = ldg_nc_v4(p + i), w1 = ldg_nc_v4(p + i + 4);
+  v[0] = __uint_as_float(w0.x); v[1] = __uint_as_float(w0.y); v[2] = __uint_as_float(w0.z); v[3] = __uint_as_float(w0.w);
+  v[4] = __uint_as_float(w1.x); v[5] = __uint_as_float(w1.y); v[6] = __uint_as_float(w1.z); v[7] = __uint_as_float(w1.w);
+}
+
+template <typename TA, typename TB>
+__global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) pair_stats_kernel(const TA* __restrict__ a,
+                                                                               const TB* __restrict__ b, int64_t n,
+                                                                               double* out, GammaWs* ws,
+                                                                               double* partials) {
+  __shared__ float sm[kThreads / 32][4];
+  __shared__ bool is_last;
+  const int64_t ntiles = cdiv(n, kTile);
+  float sdd = 0.f, sbb = 0.f, sab = 0.f, saa = 0.f;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+#pragma unroll
+    for (int i = 0; i < kVecPerThread; ++i) {
+      const int64_t idx = t * kTile + (int64_t(i) * kThreads + threadIdx.x) * 8;
+      if (idx >= n) continue;                   // n % 8 == 0: whole vectors only
+      float va[8], vb[8];
+      load8(a, idx, va);
+      load8(b, idx, vb);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float d = va[e] - vb[e];
+        sdd = __fmaf_rn(d, d, sdd);
+        sbb = __fmaf_rn(vb[e], vb[e], sbb);
+        sab = __fmaf_rn(va[e], vb[e], sab);
+        saa = __fmaf_rn(va[e], va[e], saa);
+      }
+    }
+  }
+  float v[4] = {sdd, sbb, sab, saa};
+  block_sum4(v, sm);
+  if (threadIdx.x == 0) {
+    double* p = partials + 4 * int64_t(blockIdx.x);
+    p[0] = v[0]; p[1] = v[1]; p[2] = v[2]; p[3] = v[3];
+    __threadfence();
+    is_last = atomicAdd(&ws->counter, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  if (threadIdx.x == 0) {
+    double acc[4] = {0, 0, 0, 0};
+    for (unsigned c = 0; c < gridDim.x; ++c) {
+      const volatile double* p = partials + 4 * int64_t(c);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] += p[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) out[i] = acc[i];
+    ws->counter = 0u;
+  }
+}
+
 // a8: p = f32(f32(alpha*Gamma) + beta); NVFP4 iff step > 0 and p < tau.
 __global__ void dmpq_kernel(const float* __restrict__ gamma, const float* __restrict__ alpha,
                             const float* __restrict__ beta, const int32_t* __restrict__ layer_block,
@@ -331,6 +402,26 @@ int launch_block_gamma(const void* xin, const void* xout, int64_t n, void* delta
   gamma_kernel<<<unsigned(gamma_grid(n, num_sms)), kThreads, 0, s>>>(static_cast<const uint16_t*>(xin), static_cast<const uint16_t*>(xout),
                                                     n, static_cast<uint16_t*>(delta), gamma_out, r2_out, tdc_state,
                                                     computed, w, partials);
+  return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
+}
+
+int launch_pair_stats(const void* a, int a_f32, const void* b, int b_f32, int64_t n, double* out, void* ws,
+                      int num_sms, cudaStream_t s) {
+  GammaWs* w = static_cast<GammaWs*>(ws);
+  double* partials = reinterpret_cast<double*>(static_cast<char*>(ws) + 256);
+  const unsigned grid = unsigned(gamma_grid(n, num_sms));
+  if (!a_f32 && !b_f32)
+    pair_stats_kernel<uint16_t, uint16_t><<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(a),
+                                                                    static_cast<const uint16_t*>(b), n, out, w, partials);
+  else if (!a_f32)
+    pair_stats_kernel<uint16_t, float><<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(a),
+                                                                 static_cast<const float*>(b), n, out, w, partials);
+  else if (!b_f32)
+    pair_stats_kernel<float, uint16_t><<<grid, kThreads, 0, s>>>(static_cast<const float*>(a),
+                                                                 static_cast<const uint16_t*>(b), n, out, w, partials);
+  else
+    pair_stats_kernel<float, float><<<grid, kThreads, 0, s>>>(static_cast<const float*>(a), static_cast<const float*>(b),
+                                                              n, out, w, partials);
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 

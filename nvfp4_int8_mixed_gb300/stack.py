@@ -91,9 +91,12 @@ class DiTStack:
         quantize_act_int8(x, row_amax=row_amax_in, want_q=False, pred=gate_i8, out=(None, planes, self.rs))
         qlinear_w4a8(planes, self.rs, *wq, residual=residual, gelu=gelu, out=out, pred=gate_i8)
 
-    def enqueue_step(self):
-        """Enqueue one denoising step on the current stream (graph-capturable)."""
+    def enqueue_step(self, hook=None):
+        """Enqueue one denoising step on the current stream (graph-capturable).
+        hook (eager calibration runs only): called as hook(block, layer_index,
+        x) with each linear layer's bf16 input before the layer runs."""
         H = self.H
+        call = (lambda l, i, x: hook(l, i, x)) if hook is not None else (lambda l, i, x: None)
         dmpq_assign(self.gamma, self.alpha, self.beta, self.layer_block, self.tau, self.step_dev,
                     use_nvfp4=self.use_nvfp4, gates=self.gates)
         h = self.x_in
@@ -105,13 +108,17 @@ class DiTStack:
                                  c, out, gates=gates, refresh_every=self.refresh_every, step=self.step_dev)
             g = lambda i, f: gates[i, f:f + 1]
             layernorm(h, LN_EPS, out=self.h1, amax_out=self.amax, row_amax_out=self.row_amax, pred=c)
+            call(l, 0, self.h1)
             self._ql(self.h1, self.wq[l]["qkv"], g(0, 0), g(0, 1), self.qkv, amax_in=self.amax,
                      row_amax_in=self.row_amax)
             v = self.qkv[:, 2 * H:3 * H]
+            call(l, 1, v)
             self._ql(v, self.wq[l]["out"], g(1, 0), g(1, 1), self.x1, residual=h)
             layernorm(self.x1, LN_EPS, out=self.h2, amax_out=self.amax, row_amax_out=self.row_amax, pred=c)
+            call(l, 2, self.h2)
             self._ql(self.h2, self.wq[l]["up"], g(2, 0), g(2, 1), self.u, amax_in=self.amax,
                      row_amax_in=self.row_amax, gelu=True)
+            call(l, 3, self.u)
             self._ql(self.u, self.wq[l]["down"], g(3, 0), g(3, 1), out, residual=self.x1)
             block_gamma(h, out, delta=self.delta[l], gamma_out=self.gamma[l:l + 1], r2_out=self.r2[l:l + 1],
                         tdc_state=self.state[l], computed=c)
@@ -189,3 +196,103 @@ def calibrate_tau(stack: DiTStack, xs, frac: float = 0.6) -> float:
     stack.graph = None
     stack.reset()
     return float(np.float32(np.quantile(p.astype(np.float64), frac)))
+
+
+def calibrate_lines(stack: DiTStack, xs, weights, steps=None):
+    """The calibration side of DMPQ (thelatestinai.com page, Figures 1, 3, 4)
+    on the synthetic stack.
+
+    Runs the stack eagerly with every layer in INT8 and TDC off (the same
+    trajectory calibrate_tau uses).  For every step t and linear layer it
+    measures E_rel = ||Y_q - Y|| / ||Y|| for both activation formats, with
+    Y = x W^T in fp32 from the layer's actual bf16 input and the unquantized
+    weights (a plain library GEMM: this is an offline diagnostic) and Y_q the
+    W4A4 / W4A8 product of the same input.  Also per block: Gamma_t and the
+    similarity of consecutive updates (cosine, relative L2).  Each layer's
+    line E_rel_NVFP4(t) ~ alpha * Gamma_{b(l)}(t-1) + beta is then fitted by
+    least squares over t >= 1.
+
+    weights: the per-block dicts the stack was built from (fp32).  Returns a
+    dict of numpy arrays: e_rel_nvfp4, e_rel_int8 [T, layers], gamma [T,
+    blocks], delta_cos, delta_rel [T, blocks] (NaN at t = 0), alpha, beta,
+    r2 [layers].
+    """
+    from . import pair_stats, qlinear_w4a4, qlinear_w4a8
+    T = len(xs) if steps is None else min(steps, len(xs))
+    nb = stack.nb
+    names = ("qkv", "out", "up", "down")
+    dev = stack.dev
+    w32 = [{k: torch.as_tensor(b[k]).to(dev, torch.float32) for k in names} for b in weights]
+    e4 = np.full((T, 4 * nb), np.nan)
+    e8 = np.full((T, 4 * nb), np.nan)
+    gam = np.zeros((T, nb))
+    dcos = np.full((T, nb), np.nan)
+    drel = np.full((T, nb), np.nan)
+    stats = torch.empty((T, 4 * nb, 2, 4), dtype=torch.float64, device=dev)
+
+    def hook(t):
+        def measure(l, i, x):
+            w = w32[l][names[i]]
+            y_ref = x.float() @ w.t()
+            codes, sf, ga = quantize_act_nvfp4(x)
+            y4 = qlinear_w4a4(codes, sf, ga, *stack.wq[l][names[i]], out_dtype=torch.float32)
+            _, planes, s = quantize_act_int8(x, want_q=False)
+            y8 = qlinear_w4a8(planes, s, *stack.wq[l][names[i]], out_dtype=torch.float32)
+            pair_stats(y4, y_ref, out=stats[t, 4 * l + i, 0])
+            pair_stats(y8, y_ref, out=stats[t, 4 * l + i, 1])
+        return measure
+
+    tau0, skip0, graph0 = stack.tau, stack.max_skip, stack.graph
+    stack.tau, stack.max_skip, stack.graph = float("-inf"), 0, None
+    stack.reset()
+    prev = [None] * nb
+    dstats = torch.full((T, nb, 4), float("nan"), dtype=torch.float64, device=dev)
+    for t in range(T):
+        stack.x_in.copy_(xs[t])
+        stack.step_dev.fill_(t)
+        old = [d.clone() for d in stack.delta] if t >= 1 else None
+        stack.enqueue_step(hook=hook(t))
+        if old is not None:                        # Delta_{t-1} existed: compare Delta_t with it
+            for l in range(nb):
+                pair_stats(stack.delta[l], old[l], out=dstats[t, l])
+        gam[t] = stack.gamma.cpu().numpy()
+    torch.cuda.synchronize()
+    st = stats.cpu().numpy()
+    with np.errstate(divide="ignore", invalid="ignore"):
+        e4[:] = np.sqrt(st[:, :, 0, 0] / st[:, :, 0, 1])
+        e8[:] = np.sqrt(st[:, :, 1, 0] / st[:, :, 1, 1])
+        ds = dstats.cpu().numpy()
+        drel[:] = np.sqrt(ds[:, :, 0] / ds[:, :, 1])
+        dcos[:] = ds[:, :, 2] / np.sqrt(ds[:, :, 3] * ds[:, :, 1])
+    lb = stack.layer_block.cpu().numpy()
+    alpha = np.zeros(4 * nb)
+    beta = np.zeros(4 * nb)
+    r2 = np.zeros(4 * nb)
+    for k in range(4 * nb):
+        x = gam[:T - 1, lb[k]]                     # Gamma_{t-1}
+        y = e4[1:T, k]                             # E_rel at t
+        alpha[k], beta[k] = _fit_line(x, y)
+        r2[k] = _r_squared(x, y, alpha[k], beta[k])
+    stack.tau, stack.max_skip, stack.graph = tau0, skip0, graph0
+    stack.reset()
+    return dict(e_rel_nvfp4=e4, e_rel_int8=e8, gamma=gam, delta_cos=dcos, delta_rel=drel, alpha=alpha, beta=beta,
+                r2=r2)
+
+
+def _fit_line(x, y):
+    """Least-squares alpha, beta of y ~ alpha x + beta (float64); constant x -> (0, mean y)."""
+    x = np.asarray(x, np.float64)
+    y = np.asarray(y, np.float64)
+    mx, my = x.mean(), y.mean()
+    sxx = ((x - mx) ** 2).sum()
+    if sxx == 0.0:
+        return 0.0, float(my)
+    a = ((x - mx) * (y - my)).sum() / sxx
+    return float(a), float(my - a * mx)
+
+
+def _r_squared(x, y, a, b):
+    y = np.asarray(y, np.float64)
+    res = y - (a * np.asarray(x, np.float64) + b)
+    tot = ((y - y.mean()) ** 2).sum()
+    return 1.0 if tot == 0.0 else float(1.0 - (res @ res) / tot)

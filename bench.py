@@ -234,6 +234,48 @@ STACKS = {
 }
 
 
+def bf16_stack_context(weights, xs, H):
+    """The same block stack in plain bf16 torch ops (cuBLAS GEMMs), one CUDA
+    graph per step: the unquantized "original" the pages compare against.
+    Context only; none of the library's kernels run here."""
+    import torch
+    import torch.nn.functional as Fn
+    w = [{k: b[k].to(torch.bfloat16) for k in ("qkv", "out", "up", "down")} for b in weights]
+    x_in = torch.empty_like(xs[0])
+
+    def step():
+        x = x_in
+        for b in w:
+            h1 = Fn.layer_norm(x, (H,), eps=1e-5)
+            v = (h1 @ b["qkv"].t())[:, 2 * H:]
+            x1 = x + v @ b["out"].t()
+            u = Fn.gelu(Fn.layer_norm(x1, (H,), eps=1e-5) @ b["up"].t(), approximate="tanh")
+            x = x1 + u @ b["down"].t()
+        return x
+
+    x_in.copy_(xs[0])
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for t in range(3):
+        x_in.copy_(xs[t])
+        g.replay()
+    torch.cuda.synchronize()
+    e0.record()
+    for x in xs:
+        x_in.copy_(x)
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3
+    del g, w
+    torch.cuda.empty_cache()
+    return {"blocks_per_s": len(weights) * len(xs) / sec, "ms_per_step": sec / len(xs) * 1e3}
+
+
 def run_stack_bench(name: str, dev):
     """Blocks/s of the synthetic DiT stack with DMPQ+TDC and with DMPQ only.
 
@@ -278,6 +320,7 @@ def run_stack_bench(name: str, dev):
                               "alpha_mean": fin(cal["alpha"]), "beta_mean": fin(cal["beta"]),
                               "delta_cos_mean": fin(cal["delta_cos"]), "delta_rel_mean": fin(cal["delta_rel"])}
         runs.append(("measured_lines", 1, 0, lines))
+    res["bf16_torch_context"] = bf16_stack_context(weights, xs, H)
     del weights
     for mode, max_skip, refresh, lines in runs:
         if lines is not None:

@@ -18,6 +18,16 @@ W4A8) and stores bf16.  Biases are zero.  The stack feeds step t's input to
 block 0, chains the blocks, and records the last block's output (reading:
 the output is not fed back into the next step's input).
 
+Fused producers (`fused=True`, an extension, not from the pages): the
+three layer inputs whose producer can quantize them in one pass -- h1 and h2
+(the LayerNorms) and u (the up-projection's GELU epilogue) -- take NVFP4 by
+delayed scaling (nvfp4.quantize_delayed) from a per-block history of their
+exact tensor amaxes at the block's previous computed step; INT8 stays exact
+(a per-row amax is known to a row-owning producer).  The history is updated
+with this step's exact amaxes of h1, h2, u whenever the block is computed,
+whatever format each layer took, and left alone when TDC skips the block.
+The V slice (the out-projection's input) is quantized as before.
+
 Parity: LN pinned against torch's layer_norm (float64); the block's wiring
 pinned by zero weights (the block is then the identity) and by weights
 confined to the Q/K rows (the V slice is zero, so x1 = x); the stack's rules
@@ -32,6 +42,7 @@ from . import nvfp4, int8, gemm, gamma, dmpq, tdc
 from .codecs import bf16_to_f32, f64_to_bf16
 
 LN_EPS = 1e-5
+F32 = np.float32
 
 
 def layernorm(x_bits, eps: float = LN_EPS):
@@ -46,10 +57,11 @@ def quantize_weights(w_f32):
     return dict(codes=codes, sf=sf, g=g)
 
 
-def qlinear(h_bits, wq, use_nvfp4: bool, gelu=False, residual=None):
+def qlinear(h_bits, wq, use_nvfp4: bool, gelu=False, residual=None, amax_t=None):
+    """amax_t: the NVFP4 tensor amax to quantize with (None: the input's own)."""
     h = bf16_to_f32(h_bits)
     if use_nvfp4:
-        codes, sf, g, _ = nvfp4.quantize(h)
+        codes, sf, g, _ = nvfp4.quantize(h, amax_t)
         return gemm.w4a4(codes, sf, g, wq["codes"], wq["sf"], wq["g"], gelu=gelu,
                          residual=residual, out_dtype="bf16")
     q, s, _ = int8.quantize(h)
@@ -57,21 +69,34 @@ def qlinear(h_bits, wq, use_nvfp4: bool, gelu=False, residual=None):
                      residual=residual, out_dtype="bf16")
 
 
-def block_forward(x_bits, wq_block, flags):
-    """flags: 4 uint8 (qkv, out, up, down); 1 = NVFP4."""
+def block_forward(x_bits, wq_block, flags, amax_hist=None, headroom=2.0):
+    """flags: 4 uint8 (qkv, out, up, down); 1 = NVFP4.
+
+    amax_hist (fused producers): float32 [3] history of the tensor amaxes of
+    h1, h2, u; their NVFP4 layers quantize with headroom * history, and the
+    array is overwritten with this call's exact amaxes."""
     H = x_bits.shape[1]
+    fused = amax_hist is not None
+    used = [F32(F32(headroom) * F32(a)) for a in amax_hist] if fused else [None] * 3
     h1 = layernorm(x_bits)
-    qkv = qlinear(h1, wq_block["qkv"], bool(flags[0]))
+    qkv = qlinear(h1, wq_block["qkv"], bool(flags[0]), amax_t=used[0])
     v = np.ascontiguousarray(qkv[:, 2 * H:3 * H])
     x1 = qlinear(v, wq_block["out"], bool(flags[1]), residual=x_bits)
     h2 = layernorm(x1)
-    u = qlinear(h2, wq_block["up"], bool(flags[2]), gelu=True)
-    return qlinear(u, wq_block["down"], bool(flags[3]), residual=x1)
+    u = qlinear(h2, wq_block["up"], bool(flags[2]), gelu=True, amax_t=used[1])
+    out = qlinear(u, wq_block["down"], bool(flags[3]), residual=x1, amax_t=used[2])
+    if fused:
+        for i, t in enumerate((h1, h2, u)):
+            amax_hist[i] = nvfp4.tensor_amax(bf16_to_f32(t))
+    return out
 
 
 def run_stack(x_steps, wq_blocks, alpha, beta, tau, tau_tdc, max_skip=1, use_tdc=True,
-              forced_flags=None, forced_skips=None, refresh_every=0):
+              forced_flags=None, forced_skips=None, refresh_every=0, fused=False, headroom=2.0):
     """Run every step.  Returns dict(outputs, flags[t], skips[t], gammas[t], r2[t]).
+
+    fused: fused producers with delayed NVFP4 scaling (module header); every
+    block's amax history starts at zero.
 
     forced_flags (optional) [steps][layers] replaces DMPQ's decisions and
     forced_skips (optional) [steps][blocks] replaces TDC's (teacher forcing
@@ -80,6 +105,7 @@ def run_stack(x_steps, wq_blocks, alpha, beta, tau, tau_tdc, max_skip=1, use_tdc
     nb = len(wq_blocks)
     layer_block = np.repeat(np.arange(nb), 4)
     caches = [tdc.BlockCache() for _ in range(nb)]
+    hist = [np.zeros(3, dtype=F32) if fused else None for _ in range(nb)]
     g_prev = np.zeros(nb, dtype=np.float32)
     out_log = dict(outputs=[], flags=[], skips=[], gammas=[], r2=[])
     for t, x in enumerate(x_steps):
@@ -100,7 +126,7 @@ def run_stack(x_steps, wq_blocks, alpha, beta, tau, tau_tdc, max_skip=1, use_tdc
                 out = tdc.apply(h, c.delta)
                 tdc.after_skip(c)
             else:
-                out = block_forward(h, wq_blocks[l], flags[4 * l:4 * l + 4])
+                out = block_forward(h, wq_blocks[l], flags[4 * l:4 * l + 4], hist[l], headroom)
             G, dn, r2 = gamma.block_pass(h, out, c.delta, computed=not skip)
             if not skip:
                 tdc.after_compute(c, dn, r2)
@@ -112,5 +138,7 @@ def run_stack(x_steps, wq_blocks, alpha, beta, tau, tau_tdc, max_skip=1, use_tdc
         out_log["skips"].append(skips)
         out_log["gammas"].append(g_t)
         out_log["r2"].append(np.array([c.r2 for c in caches], dtype=np.float32))
+        if fused:
+            out_log.setdefault("amax_hist", []).append(np.stack(hist))
         g_prev = g_t
     return out_log

@@ -23,8 +23,20 @@ row m, scale column c sits at
     ((m // 128) * (Kc4 // 4) + c // 4) * 512 + (m % 32) * 16 + ((m % 128) // 32) * 4 + c % 4
 with Kc4 the padded column count.  Pads are zero.
 
+Delayed scaling (an extension for quantizing inside the producing kernel,
+not from the pages): a producer that emits NVFP4 in one pass cannot know the
+tensor amax of what it is producing.  It uses instead headroom * (the exact
+tensor amax of the same layer input at the previous call), and records this
+call's exact amax for the next one.  With a power-of-two headroom the
+product S_b * g is unchanged whenever the amax did not grow (S_b halves and g
+doubles exactly, E4M3 subnormals aside), so the headroom costs no precision;
+an amax that grew past headroom * previous saturates the largest blocks at
++-6 * 448 * g = +-amax_used.  `quantize_delayed` is steps 1-6 with amax_t =
+headroom * amax_prev.
+
 Parity: pinned (hand-built blocks with known scales, brute-force nearest
-code, swizzle bijection and fixed offsets).
+code, swizzle bijection and fixed offsets; delayed scaling by the zero
+history, the power-of-two identity and the saturation bound).
 """
 from __future__ import annotations
 
@@ -76,6 +88,16 @@ def quantize(x: np.ndarray, amax_t=None):
     codes = e2m1_encode(v)
     codes = np.where(nz[:, :, None], codes, np.uint8(0)).astype(np.uint8)
     return pack_e2m1(codes.reshape(R, K)), sf.astype(np.uint8), g, amax_t
+
+
+def quantize_delayed(x: np.ndarray, amax_prev, headroom=2.0):
+    """Delayed-scaling NVFP4: quantize with amax_t = f32(headroom * amax_prev).
+
+    Returns (codes, scale bytes, g, amax_used, amax_new) with amax_new the
+    exact tensor amax of x, the history value for the next call."""
+    amax_used = F32(F32(headroom) * F32(amax_prev))
+    codes, sf, g, _ = quantize(x, amax_used)
+    return codes, sf, g, amax_used, tensor_amax(x)
 
 
 def dequantize(packed: np.ndarray, sf: np.ndarray, g=1.0) -> np.ndarray:

@@ -286,8 +286,10 @@ def run_stack_bench(name: str, dev):
     max_skip 1.  Also the PDR variant "pdr": max_skip 2 with a forced
     computed step every 4th step, and "measured_lines": (alpha, beta) refitted
     from E_rel measured on the first calib_steps steps (DMPQ calibration side)
-    with tau set from them.  Timed: every step's graph replay plus its input
-    copy."""
+    with tau set from them, and "dmpq_tdc_fused_quant": DMPQ+TDC with the
+    quantizing producers (LayerNorms and the up-projection's epilogue emit
+    the next layer's NVFP4 / INT8 input; delayed NVFP4 scaling).  Timed:
+    every step's graph replay plus its input copy."""
     import torch
     from nvfp4_int8_mixed_gb300.stack import DiTStack, calibrate_lines, calibrate_tau
     c = STACKS[name]
@@ -306,11 +308,13 @@ def run_stack_bench(name: str, dev):
         x = x + synthetic.drift_sigma(t, T) * torch.randn((M, H), generator=gen, device=dev)
         xs.append(x.to(torch.bfloat16))
     del x
-    stack = DiTStack(weights, alpha, beta, M, H, F, tau=0.0, tau_tdc=0.05, max_skip=1, device=dev)
+    stack = DiTStack(weights, alpha, beta, M, H, F, tau=0.0, tau_tdc=0.05, max_skip=1, device=dev, fused=True)
+    stack.fused = False
     torch.cuda.synchronize()
     tau = calibrate_tau(stack, xs)
     res = {"config": f"{nb} blocks, M={M}, H={H}, F={F}, {T} steps", "tau": tau}
-    runs = [("dmpq_tdc", 1, 0, None), ("dmpq_only", 0, 0, None), ("pdr_skip2_refresh4", 2, 4, None)]
+    runs = [("dmpq_tdc", 1, 0, None), ("dmpq_only", 0, 0, None), ("pdr_skip2_refresh4", 2, 4, None),
+            ("dmpq_tdc_fused_quant", 1, 0, None)]
     if c.get("calib_steps"):
         cal = calibrate_lines(stack, xs, weights, steps=c["calib_steps"])
         lines = (cal["alpha"].astype(np.float32), cal["beta"].astype(np.float32))
@@ -329,6 +333,7 @@ def run_stack_bench(name: str, dev):
             tau = calibrate_tau(stack, xs)
             res["calibration"]["tau"] = tau
         stack.tau, stack.max_skip, stack.refresh_every = tau, max_skip, refresh
+        stack.fused = mode.endswith("fused_quant")
         stack.graph = None
         stack.reset()
         stack.capture()

@@ -50,6 +50,7 @@ enum {
 
 enum { SIXBIT_F32 = 0, SIXBIT_BF16 = 1 };          /* dtype / out_dtype */
 enum { SIXBIT_EPI_GELU = 1 };                       /* epilogue flag bits */
+enum { SIXBIT_QOUT_W4A4 = 0, SIXBIT_QOUT_W4A8 = 1 };  /* sixbit_qlinear_qout mode */
 
 /* Library version string (static storage). */
 const char* sixbit_version(void);
@@ -221,6 +222,60 @@ int sixbit_tdc_decide_and_apply(const void* in, const void* delta, int64_t n, co
 int sixbit_layernorm_bf16(const void* x, int64_t M, int64_t H, int64_t ldx, float eps,
                           void* y, int64_t ldy, float* amax_out, float* row_amax_out,
                           const uint8_t* pred, sixbit_stream_t stream);
+
+/* ---- Quantizing producers (an extension, not from the pages): the next
+ * linear layer's activation quantization fused into the kernel that
+ * produces the activation, which removes the bf16 write and re-read of it.
+ *
+ * Delayed scaling.  A one-pass producer cannot know the tensor amax of what
+ * it produces, so its NVFP4 output uses amax_t = headroom * (the exact
+ * tensor amax of its previous call's output), read from `amax_hist`, and
+ * records this call's exact amax there for the next call.  amax_hist:
+ * device uint32[4], 16-byte aligned, one per producing layer, zeroed by the
+ * caller before the first call and then owned by the library (previous
+ * amax, running amax, CTA ticket; the call's last CTA rolls it over, so no
+ * other kernel is needed).  Calls that share one amax_hist must be ordered
+ * on one stream.  With a zero history every NVFP4 code is 0 (amax_t = 0).
+ * With a power-of-two headroom and an unchanged amax the codes equal those
+ * of sixbit_quantize_act_nvfp4 with the true amax (S halves, g doubles);
+ * an amax that grew past headroom * previous saturates the largest blocks.
+ * INT8 outputs need no history: a row-owning producer knows the row amax.
+ * Results equal: the bf16 value the unfused producer would store, then the
+ * quantizer of a2 (NVFP4 with amax_in = headroom * previous amax) or a3. */
+
+/* LayerNorm (as sixbit_layernorm_bf16) that also quantizes its output.
+ * Outputs, each optional, at least one given:
+ *   y        bf16 [M, ldy];
+ *   NVFP4    codes [M, H/2], sf (sixbit_sf_bytes(M, H)), g_out[0], by delayed
+ *            scaling from amax_hist (required with codes); written when
+ *            nv_pred is NULL or *nv_pred != 0;
+ *   INT8     planes [3][M][H/2] and row_scale [M] as sixbit_quantize_act_int8
+ *            with the row's own amax; written when i8_pred is NULL or
+ *            *i8_pred != 0.
+ * amax_hist (nullable without codes) records |y|'s tensor amax.
+ * H % 8 == 0, H <= 4096, and H % 64 == 0 with codes or planes. */
+int sixbit_layernorm_quant(const void* x, int64_t M, int64_t H, int64_t ldx, float eps,
+                           void* y, int64_t ldy,
+                           uint8_t* codes, uint8_t* sf, float* g_out, uint32_t* amax_hist, float headroom,
+                           const uint8_t* nv_pred,
+                           uint8_t* planes, float* row_scale, const uint8_t* i8_pred,
+                           const uint8_t* pred, sixbit_stream_t stream);
+
+/* Linear layer with a quantizing epilogue: the product and epilogue of
+ * sixbit_qlinear_w4a4 (mode SIXBIT_QOUT_W4A4: a = codes, a_sf, g_a) or
+ * sixbit_qlinear_w4a8 (mode SIXBIT_QOUT_W4A8: a = digit planes, row_scale),
+ * bias and SIXBIT_EPI_GELU allowed, no residual, a bf16 result.  When q_pred
+ * is NULL or *q_pred != 0 the result leaves as NVFP4 for the next layer --
+ * q_codes [M, N/2], q_sf (sixbit_sf_bytes(M, N)), q_g[0], delayed scaling from
+ * amax_hist -- and y is not written; otherwise it leaves as bf16 y [M, ldy]
+ * (for an INT8 next layer).  amax_hist records |y|'s amax either way.
+ * N % 64 == 0 (the next layer's K). */
+int sixbit_qlinear_qout(int mode, const uint8_t* a, const uint8_t* a_sf, const float* g_a,
+                        const float* row_scale, int64_t M, int64_t K,
+                        const uint8_t* w_codes, const uint8_t* w_sf, const float* g_w, int64_t N,
+                        const void* bias, int epi, void* y, int64_t ldy,
+                        uint8_t* q_codes, uint8_t* q_sf, float* q_g, uint32_t* amax_hist, float headroom,
+                        const uint8_t* q_pred, const uint8_t* pred, sixbit_stream_t stream);
 
 /* Synchronizes `stream`, returns SIXBIT_EDEVICE if a device wait gave up
  * since the last call (and clears the word), else the stream's CUDA status

@@ -45,6 +45,10 @@ _SIGS = {
     "sixbit_pair_stats": ([_P, _I32, _P, _I32, _I64, _P, _P, _P], _INT),
     "sixbit_tdc_decide_and_apply": ([_P, _P, _I64, _P, _F, _I32, _I32, _P, _P, _P, _P, _P, _I32, _P], _INT),
     "sixbit_layernorm_bf16": ([_P, _I64, _I64, _I64, _F, _P, _I64, _P, _P, _P, _P], _INT),
+    "sixbit_layernorm_quant": ([_P, _I64, _I64, _I64, _F, _P, _I64, _P, _P, _P, _P, _F, _P, _P, _P, _P, _P, _P],
+                               _INT),
+    "sixbit_qlinear_qout": ([_INT, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _I64, _P, _INT, _P, _I64, _P, _P, _P, _P,
+                             _F, _P, _P, _P], _INT),
     "sixbit_get_error": ([_P], _INT),
 }
 
@@ -209,6 +213,32 @@ def qlinear_w4a8(planes, row_scale, w_codes, w_sf, g_w, bias=None, residual=None
     return y
 
 
+def amax_history(n: int = 1, device=None) -> torch.Tensor:
+    """Zeroed delayed-scaling histories for n quantizing producers: uint32 [n, 4]
+    (16-byte rows), handed to layernorm_quant / qlinear_qout one row per layer."""
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    return torch.zeros((n, 4), dtype=torch.int32, device=dev)
+
+
+def qlinear_qout(mode: str, a, w_codes, w_sf, g_w, q_codes, q_sf, q_g, amax_hist, a_sf=None, g_a=None,
+                 row_scale=None, bias=None, gelu=False, headroom=2.0, y=None, q_pred=None, pred=None):
+    """Linear layer whose epilogue quantizes its bf16 result to NVFP4 for the
+    next layer by delayed scaling (y written instead when *q_pred == 0).
+    mode "w4a4": a = codes [M, K/2] with a_sf, g_a; "w4a8": a = digit planes
+    [3, M, K/2] with row_scale.  Returns y (bf16 [M, N]; allocated if None)."""
+    w4a4 = mode == "w4a4"
+    _need_cuda(a, w_codes)
+    M, K = (a.shape[0], a.shape[1] * 2) if w4a4 else (a.shape[1], a.shape[2] * 2)
+    N = w_codes.shape[0]
+    y = _out(M, N, torch.bfloat16, a.device, y)
+    _check("sixbit_qlinear_qout",
+           lib().sixbit_qlinear_qout(0 if w4a4 else 1, _ptr(a), _ptr(a_sf), _ptr(g_a), _ptr(row_scale), M, K,
+                                     _ptr(w_codes), _ptr(w_sf), _ptr(g_w), N, _ptr(bias), EPI_GELU if gelu else 0,
+                                     _ptr(y), y.stride(0), _ptr(q_codes), _ptr(q_sf), _ptr(q_g), _ptr(amax_hist),
+                                     float(headroom), _ptr(q_pred), _ptr(pred), _stream()))
+    return y
+
+
 # --------------------------------------------------------------- block ops
 def block_gamma(xin, xout, delta=None, gamma_out=None, r2_out=None, tdc_state=None, computed=None):
     """a7: Gamma (and Delta in place, r2, TDC counters). Returns (gamma [1], r2 [1])."""
@@ -270,6 +300,24 @@ def layernorm(x, eps=1e-5, out=None, amax_out=None, row_amax_out=None, pred=None
     _check("sixbit_layernorm_bf16",
            lib().sixbit_layernorm_bf16(_ptr(x), M, H, x.stride(0), float(eps), _ptr(y), y.stride(0), _ptr(amax_out),
                                        _ptr(row_amax_out), _ptr(pred), _stream()))
+    return y
+
+
+def layernorm_quant(x, eps=1e-5, y=None, nvfp4=None, amax_hist=None, headroom=2.0, nv_pred=None, int8=None,
+                    i8_pred=None, pred=None):
+    """LayerNorm that quantizes its output for the next linear layer.
+    nvfp4 = (codes [M, H/2], sf, g) by delayed scaling from amax_hist;
+    int8 = (planes [3, M, H/2], row_scale [M]) exact per row; y bf16 [M, H]
+    (optional).  Each quantized output is written when its gate is None or
+    nonzero."""
+    M, H = x.shape
+    codes, sf, g = nvfp4 if nvfp4 is not None else (None, None, None)
+    planes, rs = int8 if int8 is not None else (None, None)
+    _check("sixbit_layernorm_quant",
+           lib().sixbit_layernorm_quant(_ptr(x), M, H, x.stride(0), float(eps), _ptr(y),
+                                        y.stride(0) if y is not None else 0, _ptr(codes), _ptr(sf), _ptr(g),
+                                        _ptr(amax_hist), float(headroom), _ptr(nv_pred), _ptr(planes), _ptr(rs),
+                                        _ptr(i8_pred), _ptr(pred), _stream()))
     return y
 
 

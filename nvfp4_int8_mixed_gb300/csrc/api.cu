@@ -163,6 +163,29 @@ int sixbit_qlinear_w4a8(const uint8_t* a_planes, const float* row_scale, int64_t
   return launch_gemm_fp4(c, sms, cs(stream));
 }
 
+int sixbit_qlinear_qout(int mode, const uint8_t* a, const uint8_t* a_sf, const float* g_a, const float* row_scale,
+                        int64_t M, int64_t K, const uint8_t* w_codes, const uint8_t* w_sf, const float* g_w, int64_t N,
+                        const void* bias, int epi, void* y, int64_t ldy, uint8_t* q_codes, uint8_t* q_sf, float* q_g,
+                        uint32_t* amax_hist, float headroom, const uint8_t* q_pred, const uint8_t* pred,
+                        sixbit_stream_t stream) {
+  if (mode != SIXBIT_QOUT_W4A4 && mode != SIXBIT_QOUT_W4A8) return kEInval;
+  int rc = check_gemm(a, w_codes, w_sf, g_w, M, K, N, bias, nullptr, 0, SIXBIT_BF16, y, ldy);
+  if (rc != kOk) return rc;
+  if (mode == SIXBIT_QOUT_W4A4 ? (!a_sf || !g_a) : !row_scale) return kEInval;
+  if (!q_codes || !q_sf || !q_g || !amax_hist || !(headroom > 0.f) || headroom > 3.0e38f) return kEInval;
+  if (N % 64 != 0) return kEShape;
+  if ((a_sf && !aligned16(a_sf)) || !aligned16(q_codes) || !aligned16(q_sf) || !aligned16(amax_hist)) return kEAlign;
+  int sms;
+  int* err;
+  if (device_setup(&sms, &err) != kOk) return kELaunch;
+  if (M == 0) return kOk;
+  GemmCall c{mode == SIXBIT_QOUT_W4A4 ? 0 : 1, a, mode == SIXBIT_QOUT_W4A4 ? a_sf : nullptr,
+             mode == SIXBIT_QOUT_W4A4 ? g_a : nullptr, mode == SIXBIT_QOUT_W4A4 ? nullptr : row_scale, w_codes, w_sf,
+             g_w, M, N, K, bias, nullptr, 0, (epi & SIXBIT_EPI_GELU) ? 1 : 0, 1, y, ldy, pred, err,
+             q_codes, q_sf, q_g, amax_hist, headroom, q_pred};
+  return launch_gemm_fp4(c, sms, cs(stream));
+}
+
 int sixbit_block_gamma(const void* in, const void* out, int64_t n, void* delta, float* gamma_out, float* r2_out,
                        int32_t* tdc_state, const uint8_t* computed, void* ws, sixbit_stream_t stream) {
   if (!in || !out || !gamma_out || !ws || n <= 0) return kEInval;
@@ -225,6 +248,32 @@ int sixbit_layernorm_bf16(const void* x, int64_t M, int64_t H, int64_t ldx, floa
   if (device_setup(&sms, nullptr) != kOk) return kELaunch;
   if (M == 0) return kOk;
   return launch_layernorm(x, M, H, ldx, eps, y, ldy, amax_out, row_amax_out, pred, sms, cs(stream));
+}
+
+int sixbit_layernorm_quant(const void* x, int64_t M, int64_t H, int64_t ldx, float eps, void* y, int64_t ldy,
+                           uint8_t* codes, uint8_t* sf, float* g_out, uint32_t* amax_hist, float headroom,
+                           const uint8_t* nv_pred, uint8_t* planes, float* row_scale, const uint8_t* i8_pred,
+                           const uint8_t* pred, sixbit_stream_t stream) {
+  if (!x || M < 0 || H <= 0 || ldx < H || (y && ldy < H)) return kEInval;
+  if (!y && !codes && !planes) return kEInval;
+  if (codes && (!sf || !g_out || !amax_hist)) return kEInval;
+  if (planes && !row_scale) return kEInval;
+  if (amax_hist && (!(headroom > 0.f) || headroom > 3.0e38f)) return kEInval;
+  if (H % 8 != 0 || H > kLnQuantMaxH || ldx % 8 != 0 || (y && ldy % 8 != 0)) return kEShape;
+  if ((codes || planes) && H % 64 != 0) return kEShape;
+  if (M > (int64_t(1) << 30)) return kEShape;
+  if (!aligned16(x) || (y && !aligned16(y)) || (codes && (!aligned16(codes) || !aligned16(sf))) ||
+      (planes && !aligned16(planes)) || (amax_hist && !aligned16(amax_hist)))
+    return kEAlign;
+  int sms;
+  if (device_setup(&sms, nullptr) != kOk) return kELaunch;
+  if (M == 0) return kOk;
+  LnQuantCall c = {};
+  c.x = static_cast<const uint16_t*>(x); c.M = M; c.H = H; c.ldx = ldx; c.eps = eps;
+  c.y = static_cast<uint16_t*>(y); c.ldy = ldy;
+  c.codes = codes; c.sf = sf; c.g_out = g_out; c.hist = amax_hist; c.headroom = headroom; c.nv_pred = nv_pred;
+  c.planes = planes; c.row_scale = row_scale; c.i8_pred = i8_pred; c.pred = pred;
+  return launch_ln_quant(c, sms, cs(stream));
 }
 
 int sixbit_get_error(sixbit_stream_t stream) {

@@ -97,6 +97,111 @@ __device__ __forceinline__ uint4 ldg_v4(const void* p) {
 
 __host__ __device__ __forceinline__ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// ------------------------------------------------------- NVFP4 arithmetic
+// g = amax_t / 2688 (6 * 448), 1 when amax_t = 0.
+__device__ __forceinline__ float nvfp4_global_scale(float amax_t) {
+  return amax_t == 0.f ? 1.f : __fdiv_rn(amax_t, 2688.f);
+}
+// Scale of one 16-element block: S = E4M3(amax_b * 448 / amax_t) (0 when
+// amax_t = 0), d = S * g.  Returns S's byte; r = 1/d, or 0 when d = 0 (the
+// block's codes are then all +0, which the caller must write as 0).
+__device__ __forceinline__ uint32_t nvfp4_block_scale(float amax_b, float amax_t, float g, float& r) {
+  const float s = (amax_t == 0.f) ? 0.f : __fdiv_rn(__fmul_rn(amax_b, 448.f), amax_t);
+  const uint32_t sb = e4m3_encode(s);
+  const float d = __fmul_rn(e4m3_decode(sb), g);
+  r = d != 0.f ? __frcp_rn(d) : 0.f;
+  return sb;
+}
+// Eight bf16 values (four packed words) times r -> eight E2M1 codes; 0 when r = 0.
+__device__ __forceinline__ uint32_t nvfp4_codes8(const uint32_t* pw, float r) {
+  if (r == 0.f) return 0u;
+  return e2m1x8(__fmul_rn(bf16lo(pw[0]), r), __fmul_rn(bf16hi(pw[0]), r), __fmul_rn(bf16lo(pw[1]), r),
+                __fmul_rn(bf16hi(pw[1]), r), __fmul_rn(bf16lo(pw[2]), r), __fmul_rn(bf16hi(pw[2]), r),
+                __fmul_rn(bf16lo(pw[3]), r), __fmul_rn(bf16hi(pw[3]), r));
+}
+// |x| max of eight bf16 values (four packed words), as a float.
+__device__ __forceinline__ float bf16x8_absmax(const uint32_t* pw) {
+  uint32_t a = __vmaxu2(pw[0] & 0x7FFF7FFFu, pw[1] & 0x7FFF7FFFu);
+  a = __vmaxu2(a, __vmaxu2(pw[2] & 0x7FFF7FFFu, pw[3] & 0x7FFF7FFFu));
+  return __uint_as_float(max(a & 0xFFFFu, a >> 16) << 16);
+}
+
+// -------------------------------------------------------- INT8 arithmetic
+// E2M1 code of an integer in [-4, 4].
+__device__ __forceinline__ uint32_t digit_code(int d) {
+  const uint32_t mag = (0x65420u >> (4 * (d < 0 ? -d : d))) & 0xFu;
+  return mag | (d < 0 ? 8u : 0u);
+}
+// Digit split of an INT8 code q in [-128, 127]: byte 0 = E2M1 code of a,
+// byte 1 = of b, byte 2 = of c, q = 64a + 8b + c, c = q mod 8 in [-3, 4],
+// b likewise for (q - c)/8, a the rest.
+__device__ __forceinline__ uint32_t digit_entry(int q) {
+  const int c = ((q + 3) & 7) - 3;
+  const int q1 = (q - c) >> 3;                 // exact: q - c is a multiple of 8
+  const int b = ((q1 + 3) & 7) - 3;
+  const int a = (q1 - b) >> 3;
+  return digit_code(a) | (digit_code(b) << 8) | (digit_code(c) << 16);
+}
+// Eight bf16 values (four packed words) -> q = rne(x * inv), clamped to
+// +-127 when CLAMP, returned as the bits of q + 1.5 * 2^23 (the low byte of
+// each word is q as a two's complement byte).
+template <bool CLAMP>
+__device__ __forceinline__ void int8_encode8(const uint32_t* pw, float inv, uint32_t* qb) {
+  constexpr float kMagic = 12582912.0f;        // 1.5 * 2^23
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float lo = __fmul_rn(bf16lo(pw[e]), inv), hi = __fmul_rn(bf16hi(pw[e]), inv);
+    if (CLAMP) {
+      lo = fminf(fmaxf(lo, -127.f), 127.f);
+      hi = fminf(fmaxf(hi, -127.f), 127.f);
+    }
+    qb[2 * e] = __float_as_uint(__fadd_rn(lo, kMagic));
+    qb[2 * e + 1] = __float_as_uint(__fadd_rn(hi, kMagic));
+  }
+}
+// The three digit-plane words of eight consecutive codes (element 2j in the
+// low nibble of byte j), from qb of int8_encode8 and a 256-entry digit_entry
+// table indexed by the code's byte.
+__device__ __forceinline__ void int8_planes8(const uint32_t* qb, const uint32_t* lut, uint32_t& p0, uint32_t& p1,
+                                             uint32_t& p2) {
+  uint32_t p[4];                               // byte k of p[j] = digit-k codes of elements 2j, 2j+1
+#pragma unroll
+  for (int j = 0; j < 4; ++j) p[j] = lut[qb[2 * j] & 0xFFu] | (lut[qb[2 * j + 1] & 0xFFu] << 4);
+  const uint32_t x01 = __byte_perm(p[0], p[1], 0x5140);   // a01 a23 b01 b23
+  const uint32_t x23 = __byte_perm(p[2], p[3], 0x5140);   // a45 a67 b45 b67
+  const uint32_t c01 = __byte_perm(p[0], p[1], 0x0062);   // c01 c23
+  const uint32_t c23 = __byte_perm(p[2], p[3], 0x0062);   // c45 c67
+  p0 = __byte_perm(x01, x23, 0x5410);
+  p1 = __byte_perm(x01, x23, 0x7632);
+  p2 = __byte_perm(c01, c23, 0x5410);
+}
+
+// ------------------------------------------- delayed-scaling amax history
+// A producer that quantizes its own output to NVFP4 in one pass cannot know
+// that output's tensor amax; it scales by headroom * the amax its previous
+// call recorded.  History word layout, uint32[4]: {previous call's amax
+// (float bits), this call's running amax, CTA arrival ticket, unused};
+// zero-initialised before the first call.  The last CTA of a call to arrive
+// moves the running amax into the previous-amax word and clears the other
+// two, so consecutive calls need no other kernel.
+__device__ __forceinline__ float hist_prev(const uint32_t* h) { return __uint_as_float(__ldcg(h)); }
+// One call per warp (or thread) holding a partial amax; fences its atomic.
+__device__ __forceinline__ void hist_accumulate(uint32_t* h, float amax) {
+  if (amax > 0.f) atomicMax(h + 1, __float_as_uint(amax));
+  __threadfence();
+}
+// One thread per CTA, after a CTA barrier that follows every
+// hist_accumulate of the CTA.
+__device__ __forceinline__ void hist_arrive(uint32_t* h) {
+  __threadfence();
+  if (atomicAdd(h + 2, 1u) == gridDim.x * gridDim.y * gridDim.z - 1) {
+    __threadfence();
+    const uint32_t a = atomicExch(h + 1, 0u);
+    atomicExch(h, a);
+    atomicExch(h + 2, 0u);
+  }
+}
+
 // Swizzled scale-factor byte offset: 128x4 atoms of 512 bytes.
 __host__ __device__ __forceinline__ int64_t sf_offset(int64_t m, int64_t c, int64_t kc4) {
   return ((m >> 7) * (kc4 >> 2) + (c >> 2)) * 512 + (m & 31) * 16 + ((m & 127) >> 5) * 4 + (c & 3);

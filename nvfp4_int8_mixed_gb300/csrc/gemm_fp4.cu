@@ -311,6 +311,13 @@ struct Params {
   int chunked;               // 1: K chunk maps (one op per operand per stage); 0: 2-D maps, one chunk per stage
   const uint8_t* pred;
   int* err;
+  // quantizing epilogue (q_hist != null), see GemmCall
+  uint8_t* q_codes;
+  uint8_t* q_sf;
+  float* q_g;
+  uint32_t* q_hist;
+  float q_headroom;
+  const uint8_t* q_pred;
 };
 
 template <int BN, int MODE, int STAGES, int KB, int NC, bool PAIR>
@@ -570,6 +577,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     const float gw = *p.g_w;
     const float gscale = MODE == 0 ? __fmul_rn(*p.g_a, gw) : gw;
+    // Quantizing epilogue: the bf16 result encoded as NVFP4 for the next
+    // layer, with amax_t = headroom * the previous call's |y| amax (delayed
+    // scaling); a lane holds 32 consecutive columns of one row, i.e. two
+    // whole 16-element blocks.  Either way the lane tracks |bf16 y|'s max
+    // over its rows < M for the history.
+    const bool qo = p.q_hist != nullptr;
+    const bool q_nv = qo && (p.q_pred == nullptr || *p.q_pred != 0);
+    const float q_amax_t = qo ? __fmul_rn(p.q_headroom, hist_prev(p.q_hist)) : 0.f;
+    const float q_g = nvfp4_global_scale(q_amax_t);
+    if (q_nv && blockIdx.x == 0 && ew == 0 && lane == 0) *p.q_g = q_g;
+    const int q_mpad = ((p.M + 127) / 128) * 128;   // rows of the padded scale layout
+    uint32_t q_run = 0;                          // |y| max as two bf16 halves
     for (int tile = blockIdx.x / kCtas; tile < ntiles && ok; tile += gridDim.x / kCtas) {
       const int mt = tile / p.NT, nt = tile - mt * p.NT;
       if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar, acc_phase, abort_flag))) {   // warp-uniform verdict
@@ -592,7 +611,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m0 = mt * C::kTileM + int(rank) * BM + q * 32;   // first row of this warp's block
       const int m = m0 + lane;
       const int nbase = nt * BN + half * 128;
-      if (p.out_bf16) {
+      if (q_nv) {
+        const float scale = MODE == 0 ? gscale : (m < p.M ? __fmul_rn(p.row_scale[m], gw) : 0.f);
+        const int64_t kc4 = p.N / 16;
+        uint32_t sfw = 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t* rc = c == 0 ? r0 : (c == 1 ? r1 : (c == 2 ? r2 : r3));
+          const int n0 = nbase + 32 * c;
+          if (n0 >= p.N) break;                  // N % 64 == 0: whole 64-column pairs
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(__uint_as_float(rc[i]), scale);
+          if (p.bias) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint4 b = *reinterpret_cast<const uint4*>(p.bias + n0 + 8 * i);
+              const uint32_t* pb = &b.x;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                v[8 * i + 2 * e] = __fadd_rn(v[8 * i + 2 * e], bf16lo(pb[e]));
+                v[8 * i + 2 * e + 1] = __fadd_rn(v[8 * i + 2 * e + 1], bf16hi(pb[e]));
+              }
+            }
+          }
+          if (p.gelu) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+          }
+          uint32_t pk[16];                       // the bf16 values the unfused path would store
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+          float ra, rb;
+          const uint32_t sa = nvfp4_block_scale(fmaxf(bf16x8_absmax(pk), bf16x8_absmax(pk + 4)), q_amax_t, q_g, ra);
+          const uint32_t sb = nvfp4_block_scale(fmaxf(bf16x8_absmax(pk + 8), bf16x8_absmax(pk + 12)), q_amax_t, q_g, rb);
+          if (m < p.M) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) q_run = __vmaxu2(q_run, pk[j] & 0x7FFF7FFFu);
+            uint4 w;
+            w.x = nvfp4_codes8(pk, ra);
+            w.y = nvfp4_codes8(pk + 4, ra);
+            w.z = nvfp4_codes8(pk + 8, rb);
+            w.w = nvfp4_codes8(pk + 12, rb);
+            *reinterpret_cast<uint4*>(p.q_codes + int64_t(m) * (p.N / 2) + n0 / 2) = w;
+          }
+          sfw |= (sa | (sb << 8)) << (16 * (c & 1));
+          if (c & 1) {                           // 4 blocks = one word of the swizzled layout
+            if (m < q_mpad)
+              *reinterpret_cast<uint32_t*>(p.q_sf + sf_offset(m, (n0 - 32) / 16, kc4)) = m < p.M ? sfw : 0u;
+            sfw = 0;
+          }
+        }
+      } else if (p.out_bf16) {
         const float scale = MODE == 0 ? gscale : (m < p.M ? __fmul_rn(p.row_scale[m], gw) : 0.f);
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
@@ -655,6 +725,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
               w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
               *slot = w;
+              if (qo && m < p.M) {
+                q_run = __vmaxu2(q_run, w.x & 0x7FFF7FFFu);
+                q_run = __vmaxu2(q_run, w.y & 0x7FFF7FFFu);
+                q_run = __vmaxu2(q_run, w.z & 0x7FFF7FFFu);
+                q_run = __vmaxu2(q_run, w.w & 0x7FFF7FFFu);
+              }
             }
           }
           fence_async_smem();                    // generic writes -> visible to the TMA store
@@ -717,9 +793,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (lane == 0) bulk_wait0();                 // this warp's output stores are complete
+    if (qo) {
+      const float a = warp_max(__uint_as_float(max(q_run & 0xFFFFu, q_run >> 16) << 16));
+      if (lane == 0) hist_accumulate(p.q_hist, a);
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0 && p.q_hist) hist_arrive(p.q_hist);
   if constexpr (PAIR) cluster_sync();          // the leader's MMAs into this CTA's TMEM are complete
   if (warp == 1) {
     tc_fence_after();
@@ -832,6 +913,8 @@ int run(const GemmCall& c, int num_sms, cudaStream_t s) {
   p.residual = static_cast<const uint16_t*>(c.residual);
   p.ldr = c.ldr; p.y = c.y; p.ldy = c.ldy; p.out_bf16 = c.out_bf16; p.gelu = c.gelu; p.pred = c.pred; p.err = c.err;
   p.chunked = chunked ? 1 : 0;
+  p.q_codes = c.q_codes; p.q_sf = c.q_sf; p.q_g = c.q_g; p.q_hist = c.q_hist; p.q_headroom = c.q_headroom;
+  p.q_pred = c.q_pred;
 
   auto kern = gemm_fp4_kernel<BN, MODE, STAGES, KB, NC, PAIR>;
   static bool attr_set = false;

@@ -31,6 +31,31 @@ int launch_tdc(const void* xin, const void* delta, int64_t n, const float* r2, f
 int launch_layernorm(const void* x, int64_t M, int64_t H, int64_t ldx, float eps, void* y, int64_t ldy,
                      float* amax_out, float* row_amax_out, const uint8_t* pred, int num_sms, cudaStream_t s);
 
+// LayerNorm that also quantizes its output (NVFP4 by delayed scaling, INT8
+// exact per row); every output pointer is optional.  H % 8 == 0 and
+// H <= kLnQuantMaxH; NVFP4 / INT8 outputs need H % 64 == 0.
+constexpr int64_t kLnQuantMaxH = 4096;
+struct LnQuantCall {
+  const uint16_t* x;
+  int64_t M, H, ldx;
+  float eps;
+  uint16_t* y;
+  int64_t ldy;
+  float* amax_out;
+  float* row_amax_out;
+  uint8_t* codes;
+  uint8_t* sf;
+  float* g_out;
+  uint32_t* hist;
+  float headroom;
+  const uint8_t* nv_pred;
+  uint8_t* planes;
+  float* row_scale;
+  const uint8_t* i8_pred;
+  const uint8_t* pred;
+};
+int launch_ln_quant(const LnQuantCall& c, int num_sms, cudaStream_t s);
+
 // Block-scaled FP4 GEMM on tcgen05.  mode 0: W4A4 (A = NVFP4 codes + scales),
 // mode 1: W4A8 (A = three E2M1 digit planes of the INT8 codes + row scales).
 struct GemmCall {
@@ -52,6 +77,16 @@ struct GemmCall {
   int64_t ldy;
   const uint8_t* pred;
   int* err;                  // device error word
+  // Quantizing epilogue (q_hist != null): the bf16 result is also encoded as
+  // NVFP4 for the next layer by delayed scaling.  When q_pred is null or
+  // *q_pred != 0 the codes [M, N/2], swizzled scales and g are written and y
+  // is not; otherwise y is written.  The history records |y|'s amax either way.
+  uint8_t* q_codes;
+  uint8_t* q_sf;
+  float* q_g;
+  uint32_t* q_hist;
+  float q_headroom;
+  const uint8_t* q_pred;
 };
 int launch_gemm_fp4(const GemmCall& c, int num_sms, cudaStream_t s);
 

@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(const T* __restri
                                                                float* g_out, const uint8_t* pred, int64_t Mpad) {
   if (pred && *pred == 0) return;
   const float amax_t = *amax_ptr;
-  const float g = (amax_t == 0.f) ? 1.f : __fdiv_rn(amax_t, 2688.f);
+  const float g = nvfp4_global_scale(amax_t);
   if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
   const int lane = threadIdx.x & 31;
   const int64_t kc4 = K / 16;                 // K % 64 == 0 -> a multiple of 4
@@ -190,13 +190,10 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(const T* __restri
       for (int u = 0; u < kU; ++u) {
         if (sp0 + u >= nspan) break;          // warp-uniform
         const int b = (sp0 + u) * 32 + lane;
-        const float am = blk[u].amax();
-        const float s = (amax_t == 0.f) ? 0.f : __fdiv_rn(__fmul_rn(am, 448.f), amax_t);
-        const uint32_t sb = e4m3_encode(s);
-        const float d = __fmul_rn(e4m3_decode(sb), g);
+        float r;
+        const uint32_t sb = nvfp4_block_scale(blk[u].amax(), amax_t, g, r);
         uint32_t w0 = 0, w1 = 0;
-        if (d != 0.f) {
-          const float r = __frcp_rn(d);
+        if (r != 0.f) {
           float y[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) y[e] = __fmul_rn(blk[u].at(e), r);
@@ -216,22 +213,6 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(const T* __restri
 }
 
 // ------------------------------------------------------------------ INT8 (a3)
-__device__ __forceinline__ uint32_t digit_code(int d) {    // integer in [-4, 4] -> E2M1 code
-  const uint32_t mag = (0x65420u >> (4 * (d < 0 ? -d : d))) & 0xFu;
-  return mag | (d < 0 ? 8u : 0u);
-}
-
-// Digit split of an INT8 code q in [-128, 127] (entry q & 0xFF):
-// byte 0 = E2M1 code of a, byte 1 = of b, byte 2 = of c, q = 64a + 8b + c,
-// c = q mod 8 in [-3, 4], b likewise for (q - c)/8, a the rest.
-__device__ __forceinline__ uint32_t digit_entry(int q) {
-  const int c = ((q + 3) & 7) - 3;
-  const int q1 = (q - c) >> 3;                 // exact: q - c is a multiple of 8
-  const int b = ((q1 + 3) & 7) - 3;
-  const int a = (q1 - b) >> 3;
-  return digit_code(a) | (digit_code(b) << 8) | (digit_code(c) << 16);
-}
-
 // WPR warps per row, NVL 16-byte vectors (8 bf16) per lane: the whole row
 // stays in registers between the amax reduction and the encode, so the input
 // is read from HBM once.  Vector v of the row sits in warp v / (32*NVL) of
@@ -258,7 +239,6 @@ __global__ void __launch_bounds__(128) int8_quant_kernel(const uint16_t* __restr
   const int rloc = warp / WPR, wpart = warp % WPR;
   const int64_t nvec = K / 8;
   const int64_t plane_stride = M * (K / 2);
-  constexpr float kMagic = 12582912.0f;        // 1.5 * 2^23
   for (int64_t m0 = int64_t(blockIdx.x) * RPC; m0 < M; m0 += int64_t(gridDim.x) * RPC) {
     const int64_t m = m0 + rloc;
     const bool row_ok = m < M;
@@ -296,18 +276,8 @@ __global__ void __launch_bounds__(128) int8_quant_kernel(const uint16_t* __restr
     for (int i = 0; i < NVL; ++i) {
       const int64_t vi = int64_t(wpart * NVL + i) * 32 + lane;
       if (vi >= nvec) continue;
-      const uint32_t* pw = &v[i].x;
       uint32_t qb[8];                          // bits of (v + magic): low byte = q
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float lo = __fmul_rn(bf16lo(pw[e]), inv), hi = __fmul_rn(bf16hi(pw[e]), inv);
-        if (kClamp) {
-          lo = fminf(fmaxf(lo, -127.f), 127.f);
-          hi = fminf(fmaxf(hi, -127.f), 127.f);
-        }
-        qb[2 * e] = __float_as_uint(__fadd_rn(lo, kMagic));
-        qb[2 * e + 1] = __float_as_uint(__fadd_rn(hi, kMagic));
-      }
+      int8_encode8<kClamp>(&v[i].x, inv, qb);
       if (q) {
         uint2 w;
         w.x = __byte_perm(__byte_perm(qb[0], qb[1], 0x0040), __byte_perm(qb[2], qb[3], 0x0040), 0x5410);
@@ -315,18 +285,12 @@ __global__ void __launch_bounds__(128) int8_quant_kernel(const uint16_t* __restr
         *reinterpret_cast<uint2*>(q + m * K + vi * 8) = w;
       }
       if (planes) {
-        // pair elements (2j, 2j+1): byte k of p[j] = digit-k codes, low nibble element 2j
-        uint32_t p[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) p[j] = lut[qb[2 * j] & 0xFFu] | (lut[qb[2 * j + 1] & 0xFFu] << 4);
-        const uint32_t x01 = __byte_perm(p[0], p[1], 0x5140);   // a01 a23 b01 b23
-        const uint32_t x23 = __byte_perm(p[2], p[3], 0x5140);   // a45 a67 b45 b67
-        const uint32_t c01 = __byte_perm(p[0], p[1], 0x0062);   // c01 c23
-        const uint32_t c23 = __byte_perm(p[2], p[3], 0x0062);   // c45 c67
+        uint32_t p0, p1, p2;
+        int8_planes8(qb, lut, p0, p1, p2);
         uint8_t* base = planes + m * (K / 2) + vi * 4;
-        *reinterpret_cast<uint32_t*>(base) = __byte_perm(x01, x23, 0x5410);
-        *reinterpret_cast<uint32_t*>(base + plane_stride) = __byte_perm(x01, x23, 0x7632);
-        *reinterpret_cast<uint32_t*>(base + 2 * plane_stride) = __byte_perm(c01, c23, 0x5410);
+        *reinterpret_cast<uint32_t*>(base) = p0;
+        *reinterpret_cast<uint32_t*>(base + plane_stride) = p1;
+        *reinterpret_cast<uint32_t*>(base + 2 * plane_stride) = p2;
       }
     }
   }

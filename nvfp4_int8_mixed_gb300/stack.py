@@ -8,6 +8,13 @@ flag says.  6Bit-Diffusion (thelatestinai.com page, Figure 2): DMPQ picks
 each layer's activation bits from the block's Gamma at the previous step;
 TDC skips a block whose update barely changed and reuses in + Delta.
 
+Fused producers (fused=True; an extension, not from the pages): the
+LayerNorms quantize their own outputs (INT8 exactly per row, NVFP4 by
+delayed scaling from a per-layer amax history) and the up-projection's GELU
+epilogue writes the down layer's NVFP4 input directly, so h1, h2 and (for an
+NVFP4 down layer) u never round-trip through HBM as bf16; the quantizer
+passes of those layers disappear.  The V slice keeps its own quantizer.
+
 Every decision stays on the device.  At the start of a step DMPQ writes one
 gate byte per (layer, format); the TDC kernel of a block clears the block's
 gates when it skips it; every kernel of the block reads its gate (`pred`)
@@ -20,8 +27,9 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (block_gamma, dmpq_assign, layernorm, qlinear_w4a4, qlinear_w4a8, quantize_act_int8,
-               quantize_act_nvfp4, quantize_weight_nvfp4, sf_bytes, tdc_decide_and_apply)
+from . import (amax_history, block_gamma, dmpq_assign, layernorm, layernorm_quant, qlinear_qout, qlinear_w4a4,
+               qlinear_w4a8, quantize_act_int8, quantize_act_nvfp4, quantize_weight_nvfp4, sf_bytes,
+               tdc_decide_and_apply)
 
 LN_EPS = 1e-5
 LAYERS = ("qkv", "out", "up", "down")
@@ -34,16 +42,19 @@ class DiTStack:
     (float32 numpy or torch); alpha, beta: per-layer predictor lines (4 per
     block, layer order qkv, out, up, down); tau: DMPQ threshold; tau_tdc,
     max_skip: TDC rule (max_skip = 0 disables skipping); refresh_every: PDR
-    periodic refresh (every k-th step is computed; 0 = off).
+    periodic refresh (every k-th step is computed; 0 = off); fused: quantizing
+    producers with delayed NVFP4 scaling (headroom: its power-of-two margin).
     """
 
     def __init__(self, weights, alpha, beta, M: int, H: int, F: int, tau: float, tau_tdc: float = 0.05,
-                 max_skip: int = 1, device=None, refresh_every: int = 0):
+                 max_skip: int = 1, device=None, refresh_every: int = 0, fused: bool = False,
+                 headroom: float = 2.0):
         self.dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
         dev = self.dev
         self.nb, self.M, self.H, self.F = len(weights), M, H, F
         self.tau, self.tau_tdc, self.max_skip = float(tau), float(tau_tdc), int(max_skip)
         self.refresh_every = int(refresh_every)
+        self.fused, self.headroom = bool(fused), float(headroom)
         nl = 4 * self.nb
         to_t = lambda a: torch.as_tensor(np.asarray(a, np.float32)).to(dev)
         self.alpha, self.beta = to_t(alpha), to_t(beta)
@@ -68,6 +79,13 @@ class DiTStack:
         self.rs = torch.empty(M, dtype=torch.float32, device=dev)
         self.amax = torch.empty(1, dtype=torch.float32, device=dev)
         self.row_amax = torch.empty(M, dtype=torch.float32, device=dev)
+        # fused producers: the down layer's NVFP4 input (written by the up
+        # epilogue) and one delayed-scaling history per producer (LN1, LN2, up)
+        self.hist = amax_history(3 * self.nb, dev)
+        if self.fused:
+            self.codes_u = torch.empty((M, F // 2), dtype=torch.uint8, device=dev)
+            self.sf_u = torch.empty(sf_bytes(M, F), dtype=torch.uint8, device=dev)
+            self.g_u = torch.empty(1, dtype=torch.float32, device=dev)
         # decisions and TDC cache
         self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)
         self.use_nvfp4 = torch.zeros(nl, dtype=torch.uint8, device=dev)
@@ -91,10 +109,49 @@ class DiTStack:
         quantize_act_int8(x, row_amax=row_amax_in, want_q=False, pred=gate_i8, out=(None, planes, self.rs))
         qlinear_w4a8(planes, self.rs, *wq, residual=residual, gelu=gelu, out=out, pred=gate_i8)
 
+    def _ln_q(self, x, i, l, gates, c, keep_bf16):
+        """Fused LayerNorm feeding layer i of block l: NVFP4 / INT8 as its gates say."""
+        H, M = self.H, self.M
+        y = self.h1 if i == 0 else self.h2
+        layernorm_quant(x, LN_EPS, y=y if keep_bf16 else None,
+                        nvfp4=(self.codes[:M * H // 2].view(M, H // 2), self.sf[:sf_bytes(M, H)], self.g),
+                        amax_hist=self.hist[3 * l + (0 if i == 0 else 1)], headroom=self.headroom,
+                        nv_pred=gates[i, 0:1],
+                        int8=(self.planes[:3 * M * H // 2].view(3, M, H // 2), self.rs), i8_pred=gates[i, 1:2], pred=c)
+        return y
+
+    def _ql_from_ln(self, wq, gates, i, out, gelu=False):
+        """Layer i's GEMMs on the operands a fused LayerNorm left in the shared buffers."""
+        H, M = self.H, self.M
+        codes, sf = self.codes[:M * H // 2].view(M, H // 2), self.sf[:sf_bytes(M, H)]
+        planes = self.planes[:3 * M * H // 2].view(3, M, H // 2)
+        qlinear_w4a4(codes, sf, self.g, *wq, gelu=gelu, out=out, pred=gates[i, 0:1])
+        qlinear_w4a8(planes, self.rs, *wq, gelu=gelu, out=out, pred=gates[i, 1:2])
+
+    def _up_down_fused(self, l, gates, out):
+        """Up-projection whose GELU epilogue emits the down layer's NVFP4 input
+        (or bf16 u for an INT8 down layer), then the down-projection."""
+        H, M, F = self.H, self.M, self.F
+        codes, sf = self.codes[:M * H // 2].view(M, H // 2), self.sf[:sf_bytes(M, H)]
+        planes = self.planes[:3 * M * H // 2].view(3, M, H // 2)
+        wu, wd = self.wq[l]["up"], self.wq[l]["down"]
+        qo = dict(q_codes=self.codes_u, q_sf=self.sf_u, q_g=self.g_u, amax_hist=self.hist[3 * l + 2],
+                  headroom=self.headroom, gelu=True, y=self.u, q_pred=gates[3, 0:1])
+        qlinear_qout("w4a4", codes, *wu, a_sf=sf, g_a=self.g, pred=gates[2, 0:1], **qo)
+        qlinear_qout("w4a8", planes, *wu, row_scale=self.rs, pred=gates[2, 1:2], **qo)
+        qlinear_w4a4(self.codes_u, self.sf_u, self.g_u, *wd, residual=self.x1, out=out, pred=gates[3, 0:1])
+        planes_u = self.planes[:3 * M * F // 2].view(3, M, F // 2)
+        quantize_act_int8(self.u, want_q=False, pred=gates[3, 1:2], out=(None, planes_u, self.rs))
+        qlinear_w4a8(planes_u, self.rs, *wd, residual=self.x1, out=out, pred=gates[3, 1:2])
+
     def enqueue_step(self, hook=None):
         """Enqueue one denoising step on the current stream (graph-capturable).
         hook (eager calibration runs only): called as hook(block, layer_index,
         x) with each linear layer's bf16 input before the layer runs."""
+        if self.fused:
+            if hook is not None:
+                raise ValueError("calibration hooks need the unfused stack (fused=False)")
+            return self._enqueue_fused()
         H = self.H
         call = (lambda l, i, x: hook(l, i, x)) if hook is not None else (lambda l, i, x: None)
         dmpq_assign(self.gamma, self.alpha, self.beta, self.layer_block, self.tau, self.step_dev,
@@ -125,6 +182,29 @@ class DiTStack:
             h = out
         self.out = h
 
+    def _enqueue_fused(self):
+        H = self.H
+        dmpq_assign(self.gamma, self.alpha, self.beta, self.layer_block, self.tau, self.step_dev,
+                    use_nvfp4=self.use_nvfp4, gates=self.gates)
+        h = self.x_in
+        for l in range(self.nb):
+            out = self.buf[l % 2]
+            gates = self.gates[4 * l:4 * l + 4]
+            c = self.cflag[l:l + 1]
+            tdc_decide_and_apply(h, self.delta[l], self.r2[l:l + 1], self.tau_tdc, self.max_skip, self.state[l],
+                                 c, out, gates=gates, refresh_every=self.refresh_every, step=self.step_dev)
+            g = lambda i, f: gates[i, f:f + 1]
+            self._ln_q(h, 0, l, gates, c, keep_bf16=False)
+            self._ql_from_ln(self.wq[l]["qkv"], gates, 0, self.qkv)
+            v = self.qkv[:, 2 * H:3 * H]
+            self._ql(v, self.wq[l]["out"], g(1, 0), g(1, 1), self.x1, residual=h)
+            self._ln_q(self.x1, 2, l, gates, c, keep_bf16=False)
+            self._up_down_fused(l, gates, out)
+            block_gamma(h, out, delta=self.delta[l], gamma_out=self.gamma[l:l + 1], r2_out=self.r2[l:l + 1],
+                        tdc_state=self.state[l], computed=c)
+            h = out
+        self.out = h
+
     def capture(self):
         """Warm up once (kernel attributes, scratch) and capture one step as a CUDA graph."""
         snap = self._snapshot()
@@ -136,14 +216,17 @@ class DiTStack:
             self.enqueue_step()
         torch.cuda.synchronize()
 
+    def _state_tensors(self):
+        return (self.gamma, self.r2, self.state, self.cflag, self.use_nvfp4, self.gates, self.hist)
+
     def _snapshot(self):
-        return [t.clone() for t in (self.gamma, self.r2, self.state, self.cflag, self.use_nvfp4, self.gates)] + \
-               [d.clone() for d in self.delta]
+        return [t.clone() for t in self._state_tensors()] + [d.clone() for d in self.delta]
 
     def _restore(self, snap):
-        for t, s in zip((self.gamma, self.r2, self.state, self.cflag, self.use_nvfp4, self.gates), snap[:6]):
+        n = len(self._state_tensors())
+        for t, s in zip(self._state_tensors(), snap[:n]):
             t.copy_(s)
-        for d, s in zip(self.delta, snap[6:]):
+        for d, s in zip(self.delta, snap[n:]):
             d.copy_(s)
 
     def reset(self):
@@ -153,6 +236,7 @@ class DiTStack:
         self.cflag.fill_(1)
         self.use_nvfp4.zero_()
         self.gates.zero_()
+        self.hist.zero_()
         for d in self.delta:
             d.zero_()
 

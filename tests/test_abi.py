@@ -80,3 +80,33 @@ def test_argument_errors_before_launch(lib):
                                            None, 0, None) == sb.EINVAL
     assert lib.sixbit_layernorm_bf16(fake, 4, 20, 20, ctypes.c_float(1e-5), fake, 20, None, None, None,
                                      None) == sb.ESHAPE
+
+
+def test_quantizing_producer_argument_errors(lib):
+    import nvfp4_int8_mixed_gb300 as sb
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    f = ctypes.c_float
+    eps = f(1e-5)
+
+    def ln(M=4, H=128, y=fake, codes=fake, sf=fake, g=fake, hist=fake, head=2.0, planes=None, rs=None):
+        return lib.sixbit_layernorm_quant(fake, M, H, H, eps, y, H, codes, sf, g, hist, f(head), None, planes, rs,
+                                          None, None, None)
+    assert ln(hist=None) == sb.EINVAL                 # NVFP4 output needs a history
+    assert ln(head=0.0) == sb.EINVAL
+    assert ln(head=float("nan")) == sb.EINVAL
+    assert ln(y=None, codes=None) == sb.EINVAL        # no output at all
+    assert ln(codes=None, planes=fake) == sb.EINVAL   # planes without row scales
+    assert ln(H=96) == sb.ESHAPE                      # quantized outputs need H % 64 == 0
+    assert ln(H=8192) == sb.ESHAPE                    # row must fit the registers
+    assert ln(hist=P((1 << 20) + 4)) == sb.EALIGN
+
+    def qo(mode=0, N=128, hist=fake, head=2.0, a_sf=fake, rs=None):
+        return lib.sixbit_qlinear_qout(mode, fake, a_sf, fake, rs, 128, 256, fake, fake, fake, N, None, 0, fake, N,
+                                       fake, fake, fake, hist, f(head), None, None, None)
+    assert qo(mode=7) == sb.EINVAL
+    assert qo(N=80) == sb.ESHAPE                      # the next layer's K: N % 64 == 0
+    assert qo(hist=None) == sb.EINVAL
+    assert qo(head=-1.0) == sb.EINVAL
+    assert qo(mode=1, a_sf=None) == sb.EINVAL         # W4A8 needs the row scales
+    assert qo(hist=P((1 << 20) + 8)) == sb.EALIGN

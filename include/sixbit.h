@@ -253,7 +253,7 @@ int sixbit_layernorm_bf16(const void* x, int64_t M, int64_t H, int64_t ldx, floa
  *            with the row's own amax; written when i8_pred is NULL or
  *            *i8_pred != 0.
  * amax_hist (nullable without codes) records |y|'s tensor amax.
- * H % 8 == 0, H <= 4096, and H % 64 == 0 with codes or planes. */
+ * H % 16 == 0, H <= 4096, and H % 64 == 0 with codes or planes. */
 int sixbit_layernorm_quant(const void* x, int64_t M, int64_t H, int64_t ldx, float eps,
                            void* y, int64_t ldy,
                            uint8_t* codes, uint8_t* sf, float* g_out, uint32_t* amax_hist, float headroom,

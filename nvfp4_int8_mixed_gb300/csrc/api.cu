@@ -259,7 +259,7 @@ int sixbit_layernorm_quant(const void* x, int64_t M, int64_t H, int64_t ldx, flo
   if (codes && (!sf || !g_out || !amax_hist)) return kEInval;
   if (planes && !row_scale) return kEInval;
   if (amax_hist && (!(headroom > 0.f) || headroom > 3.0e38f)) return kEInval;
-  if (H % 8 != 0 || H > kLnQuantMaxH || ldx % 8 != 0 || (y && ldy % 8 != 0)) return kEShape;
+  if (H % 16 != 0 || H > kLnQuantMaxH || ldx % 8 != 0 || (y && ldy % 8 != 0)) return kEShape;
   if ((codes || planes) && H % 64 != 0) return kEShape;
   if (M > (int64_t(1) << 30)) return kEShape;
   if (!aligned16(x) || (y && !aligned16(y)) || (codes && (!aligned16(codes) || !aligned16(sf))) ||

@@ -333,24 +333,27 @@ __global__ void __launch_bounds__(kThreads) layernorm_kernel(const uint16_t* __r
 }
 
 // LayerNorm that quantizes its own output for the next linear layer.  One
-// warp per row, the row held in registers: lane l holds the 16-byte vectors
-// l, l + 32, ... (NVL per lane), so x is read once.  float32 statistics
-// with a fixed operation order: mean = sum / H, var = sum (x - mean)^2 / H,
-// y = bf16((x - mean) * (1 / sqrt(var + eps))).  Outputs (each optional):
+// warp per row, the row held in registers so x is read once: lane l holds
+// the 16-element blocks l, l + 32, ... (NB per lane, 32 contiguous bytes
+// each), so a lane owns whole NVFP4 blocks and computes each block's scale
+// once.  float32 statistics in packed pairs (f32x2): mean = sum / H, var =
+// sum (x - mean)^2 / H, y = bf16((x - mean) * (1 / sqrt(var + eps))).
+// Outputs (each optional):
 //   y              bf16 [M, ldy];
 //   amax_out, row_amax_out  tensor / row |y| maxima;
 //   NVFP4 (when nv): codes [M, H/2], scales (swizzled, rows padded to 128,
 //                  pads zero) and g, by delayed scaling from `hist`
-//                  (amax_t = headroom * the previous call's amax); a lane
-//                  pair holds one 16-element block, lanes 8j..8j+7 one
-//                  4-block scale word;
+//                  (amax_t = headroom * the previous call's amax); lanes
+//                  4j..4j+3 hold one 4-block scale word;
 //   INT8 (when i8): digit planes [3][M][H/2] and row scales from the row's
 //                  own amax (the exact per-token quantizer).
 // hist (nullable) records this call's tensor amax for the next call.
-template <int NVL>
+// H % 16 == 0.
+template <int NB>
 __global__ void __launch_bounds__(kThreads) ln_quant_kernel(const LnQuantCall a) {
   if (a.pred && *a.pred == 0) return;
   __shared__ uint32_t lut[256];
+  __shared__ float red[kThreads / 32];
   const bool nv = a.codes != nullptr && (a.nv_pred == nullptr || *a.nv_pred != 0);
   const bool i8 = a.planes != nullptr && (a.i8_pred == nullptr || *a.i8_pred != 0);
   if (i8) {
@@ -363,61 +366,85 @@ __global__ void __launch_bounds__(kThreads) ln_quant_kernel(const LnQuantCall a)
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
-  const int64_t M = a.M, H = a.H, nvec = H / 8, kc4 = H / 16;
+  const int64_t M = a.M, H = a.H, nblk = H / 16, kc4 = H / 16;
   const int64_t Mpad = nv ? cdiv(M, 128) * 128 : M;
   const int64_t plane_stride = M * (H / 2);
   float tmax = 0.f;
   for (int64_t m = warp; m < Mpad; m += nwarps) {
     if (m >= M) {                              // pad rows of the scale layout
 #pragma unroll
-      for (int i = 0; i < NVL; ++i) {
-        const int64_t vi = int64_t(i) * 32 + lane;
-        if (vi < nvec && (lane & 7) == 0) *reinterpret_cast<uint32_t*>(a.sf + sf_offset(m, vi / 2, kc4)) = 0u;
+      for (int i = 0; i < NB; ++i) {
+        const int64_t b = int64_t(i) * 32 + lane;
+        if (b < nblk && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(a.sf + sf_offset(m, b, kc4)) = 0u;
       }
       continue;
     }
     const uint16_t* row = a.x + m * a.ldx;
-    uint4 v[NVL];
+    uint4 v[NB][2];
 #pragma unroll
-    for (int i = 0; i < NVL; ++i) {
-      const int64_t vi = int64_t(i) * 32 + lane;
-      v[i] = vi < nvec ? ldg_nc_v4(row + vi * 8) : make_uint4(0, 0, 0, 0);
-    }
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < NVL; ++i) {
-      const uint32_t* p = &v[i].x;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s = __fadd_rn(s, __fadd_rn(bf16lo(p[e]), bf16hi(p[e])));
-    }
-    const float mean = __fdiv_rn(warp_sum(s), float(H));
-    float q = 0.f;
-#pragma unroll
-    for (int i = 0; i < NVL; ++i) {
-      if (int64_t(i) * 32 + lane >= nvec) continue;
-      const uint32_t* p = &v[i].x;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float d0 = __fsub_rn(bf16lo(p[e]), mean), d1 = __fsub_rn(bf16hi(p[e]), mean);
-        q = __fadd_rn(q, __fmaf_rn(d0, d0, __fmul_rn(d1, d1)));
+    for (int i = 0; i < NB; ++i) {
+      const int64_t b = int64_t(i) * 32 + lane;
+      if (b < nblk) {
+        v[i][0] = ldg_nc_v4(row + b * 16);
+        v[i][1] = ldg_nc_v4(row + b * 16 + 8);
+      } else {
+        v[i][0] = v[i][1] = make_uint4(0, 0, 0, 0);
       }
     }
-    const float var = __fdiv_rn(warp_sum(q), float(H));
+    uint64_t s2 = 0;                           // (sum of even elements, sum of odd elements)
+#pragma unroll
+    for (int i = 0; i < NB; ++i)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t* p = &v[i][h].x;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s2 = f2_add(s2, f2_from_bf16x2(p[e]));
+      }
+    float sl, sh;
+    f2_unpack(s2, sl, sh);
+    const float mean = __fdiv_rn(warp_sum(__fadd_rn(sl, sh)), float(H));
+    const uint64_t mean2 = f2_pack(mean, mean);
+    uint64_t q2 = 0;
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+      if (int64_t(i) * 32 + lane >= nblk) continue;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t* p = &v[i][h].x;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint64_t d = f2_sub(f2_from_bf16x2(p[e]), mean2);
+          q2 = f2_fma(d, d, q2);
+        }
+      }
+    }
+    float ql, qh;
+    f2_unpack(q2, ql, qh);
+    const float var = __fdiv_rn(warp_sum(__fadd_rn(ql, qh)), float(H));
     const float rstd = __fdiv_rn(1.f, __fsqrt_rn(__fadd_rn(var, a.eps)));
+    const uint64_t rstd2 = f2_pack(rstd, rstd);
     float rmax = 0.f;
+    float bmax[NB];                            // |y| max of each of the lane's blocks
 #pragma unroll
-    for (int i = 0; i < NVL; ++i) {
-      const int64_t vi = int64_t(i) * 32 + lane;
-      uint32_t* p = &v[i].x;
+    for (int i = 0; i < NB; ++i) {
+      const int64_t b = int64_t(i) * 32 + lane;
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        p[e] = pack_bf16x2(__fmul_rn(__fsub_rn(bf16lo(p[e]), mean), rstd),
-                           __fmul_rn(__fsub_rn(bf16hi(p[e]), mean), rstd));
-      if (vi < nvec) {
-        rmax = fmaxf(rmax, bf16x8_absmax(p));
-        if (a.y) *reinterpret_cast<uint4*>(a.y + m * a.ldy + vi * 8) = v[i];
+      for (int h = 0; h < 2; ++h) {
+        uint32_t* p = &v[i][h].x;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) p[e] = f2_to_bf16x2(f2_mul(f2_sub(f2_from_bf16x2(p[e]), mean2), rstd2));
+      }
+      if (b < nblk) {
+        bmax[i] = fmaxf(bf16x8_absmax(&v[i][0].x), bf16x8_absmax(&v[i][1].x));
+        rmax = fmaxf(rmax, bmax[i]);
+        if (a.y) {
+          uint4* yp = reinterpret_cast<uint4*>(a.y + m * a.ldy + b * 16);
+          yp[0] = v[i][0];
+          yp[1] = v[i][1];
+        }
       } else {
-        v[i] = make_uint4(0, 0, 0, 0);
+        bmax[i] = 0.f;
+        v[i][0] = v[i][1] = make_uint4(0, 0, 0, 0);
       }
     }
     rmax = warp_max(rmax);
@@ -428,44 +455,47 @@ __global__ void __launch_bounds__(kThreads) ln_quant_kernel(const LnQuantCall a)
       const float inv = nz ? __fdiv_rn(127.f, rmax) : 0.f;
       if (lane == 0) a.row_scale[m] = nz ? __fdiv_rn(rmax, 127.f) : 0.f;
 #pragma unroll
-      for (int i = 0; i < NVL; ++i) {
-        const int64_t vi = int64_t(i) * 32 + lane;
-        if (vi >= nvec) continue;
-        uint32_t qb[8], p0, p1, p2;
-        int8_encode8<false>(&v[i].x, inv, qb);
-        int8_planes8(qb, lut, p0, p1, p2);
-        uint8_t* base = a.planes + m * (H / 2) + vi * 4;
-        *reinterpret_cast<uint32_t*>(base) = p0;
-        *reinterpret_cast<uint32_t*>(base + plane_stride) = p1;
-        *reinterpret_cast<uint32_t*>(base + 2 * plane_stride) = p2;
+      for (int i = 0; i < NB; ++i) {
+        const int64_t b = int64_t(i) * 32 + lane;
+        if (b >= nblk) continue;
+        uint32_t qb[8], p0[2], p1[2], p2[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          int8_encode8<false>(&v[i][h].x, inv, qb);
+          int8_planes8(qb, lut, p0[h], p1[h], p2[h]);
+        }
+        uint8_t* base = a.planes + m * (H / 2) + b * 8;
+        *reinterpret_cast<uint2*>(base) = make_uint2(p0[0], p0[1]);
+        *reinterpret_cast<uint2*>(base + plane_stride) = make_uint2(p1[0], p1[1]);
+        *reinterpret_cast<uint2*>(base + 2 * plane_stride) = make_uint2(p2[0], p2[1]);
       }
     }
     if (nv) {
 #pragma unroll
-      for (int i = 0; i < NVL; ++i) {
-        if (i * 32 >= nvec) break;               // warp-uniform
-        const int64_t vi = int64_t(i) * 32 + lane;
-        const float am8 = bf16x8_absmax(&v[i].x);
-        const float amb = fmaxf(am8, __shfl_xor_sync(0xffffffffu, am8, 1));   // the lane pair's 16-element block
+      for (int i = 0; i < NB; ++i) {
+        if (i * 32 >= nblk) break;               // warp-uniform
+        const int64_t b = int64_t(i) * 32 + lane;
         float r;
-        const uint32_t sb = nvfp4_block_scale(amb, amax_t, g, r);
-        const uint32_t w = nvfp4_codes8(&v[i].x, r);
-        uint32_t word = sb | (__shfl_down_sync(0xffffffffu, sb, 2) << 8);
-        word |= __shfl_down_sync(0xffffffffu, word, 4) << 16;
-        if (vi < nvec) {
-          *reinterpret_cast<uint32_t*>(a.codes + m * (H / 2) + vi * 4) = w;
-          if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(a.sf + sf_offset(m, vi / 2, kc4)) = word;
+        const uint32_t sb = nvfp4_block_scale(bmax[i], amax_t, g, r);
+        const uint32_t w0 = nvfp4_codes8(&v[i][0].x, r), w1 = nvfp4_codes8(&v[i][1].x, r);
+        uint32_t word = sb | (__shfl_down_sync(0xffffffffu, sb, 1) << 8);
+        word |= __shfl_down_sync(0xffffffffu, word, 2) << 16;
+        if (b < nblk) {
+          *reinterpret_cast<uint2*>(a.codes + m * (H / 2) + b * 8) = make_uint2(w0, w1);
+          if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(a.sf + sf_offset(m, b, kc4)) = word;
         }
       }
     }
   }
-  if (lane == 0) {
-    if (a.amax_out) atomic_max_nonneg(a.amax_out, tmax);
-    if (a.hist) hist_accumulate(a.hist, tmax);
-  }
-  if (a.hist) {
+  if (a.amax_out || a.hist) {                // one atomic (and one fence) per CTA
+    if (lane == 0) red[threadIdx.x >> 5] = tmax;
     __syncthreads();
-    if (threadIdx.x == 0) hist_arrive(a.hist);
+    if (threadIdx.x == 0) {
+      float cmax = 0.f;
+      for (int w = 0; w < kThreads / 32; ++w) cmax = fmaxf(cmax, red[w]);
+      if (a.amax_out) atomic_max_nonneg(a.amax_out, cmax);
+      if (a.hist) hist_arrive(a.hist, cmax);
+    }
   }
 }
 
@@ -582,25 +612,35 @@ int launch_tdc(const void* xin, const void* delta, int64_t n, const float* r2, f
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 
+// Persistent grid: as many CTAs as are resident at once, each walking rows,
+// so the per-CTA tail (amax atomic, fence, history ticket) is paid once.
+template <int NB>
+void launch_lnq(const LnQuantCall& c, int64_t rows, int num_sms, cudaStream_t s) {
+  static int per_sm = 0;
+  if (per_sm == 0 &&
+      (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ln_quant_kernel<NB>, kThreads, 0) != cudaSuccess ||
+       per_sm < 1))
+    per_sm = 1;
+  const int64_t want = cdiv(rows, kThreads / 32), cap = int64_t(num_sms) * per_sm;
+  ln_quant_kernel<NB><<<unsigned(want < cap ? (want < 1 ? 1 : want) : cap), kThreads, 0, s>>>(c);
+}
+
 int launch_ln_quant(const LnQuantCall& c, int num_sms, cudaStream_t s) {
-  if (c.H % 8 != 0 || c.H > kLnQuantMaxH) return kEShape;
+  if (c.H % 16 != 0 || c.H > kLnQuantMaxH) return kEShape;
   if (c.amax_out && cudaMemsetAsync(c.amax_out, 0, sizeof(float), s) != cudaSuccess) return kELaunch;
-  const int64_t per_lane = cdiv(c.H / 8, 32);          // 16-byte vectors a lane holds
+  const int64_t per_lane = cdiv(c.H / 16, 32);         // 16-element blocks a lane holds
   const int64_t rows = c.codes ? cdiv(c.M, 128) * 128 : c.M;
-  int64_t want = cdiv(rows, kThreads / 32);
-  int64_t cap = int64_t(num_sms) * 8;
-  const unsigned grid = unsigned(want < cap ? (want < 1 ? 1 : want) : cap);
-  if (per_lane <= 2) ln_quant_kernel<2><<<grid, kThreads, 0, s>>>(c);
-  else if (per_lane <= 4) ln_quant_kernel<4><<<grid, kThreads, 0, s>>>(c);
-  else if (per_lane <= 8) ln_quant_kernel<8><<<grid, kThreads, 0, s>>>(c);
-  else if (per_lane <= 12) ln_quant_kernel<12><<<grid, kThreads, 0, s>>>(c);
-  else ln_quant_kernel<16><<<grid, kThreads, 0, s>>>(c);
+  if (per_lane <= 1) launch_lnq<1>(c, rows, num_sms, s);
+  else if (per_lane <= 2) launch_lnq<2>(c, rows, num_sms, s);
+  else if (per_lane <= 4) launch_lnq<4>(c, rows, num_sms, s);
+  else if (per_lane <= 6) launch_lnq<6>(c, rows, num_sms, s);
+  else launch_lnq<8>(c, rows, num_sms, s);
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 
 int launch_layernorm(const void* x, int64_t M, int64_t H, int64_t ldx, float eps, void* y, int64_t ldy,
                      float* amax_out, float* row_amax_out, const uint8_t* pred, int num_sms, cudaStream_t s) {
-  if (H % 8 == 0 && H <= kLnQuantMaxH) {       // the register-resident kernel, without quantized outputs
+  if (H % 16 == 0 && H <= kLnQuantMaxH) {      // the register-resident kernel, without quantized outputs
     LnQuantCall c = {};
     c.x = static_cast<const uint16_t*>(x); c.M = M; c.H = H; c.ldx = ldx; c.eps = eps;
     c.y = static_cast<uint16_t*>(y); c.ldy = ldy; c.amax_out = amax_out; c.row_amax_out = row_amax_out;

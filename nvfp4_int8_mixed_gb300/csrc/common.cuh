@@ -97,6 +97,45 @@ __device__ __forceinline__ uint4 ldg_v4(const void* p) {
 
 __host__ __device__ __forceinline__ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// ---------------------------------------------- packed fp32 pair arithmetic
+// sm_100-class f32x2 instructions: two IEEE round-to-nearest fp32 operations
+// (no flush to zero) per instruction on a pair held in one 64-bit register.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t d, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(d));
+}
+__device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t w) { return f2_pack(bf16lo(w), bf16hi(w)); }
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// bf16x2 word of a pair (lo in bits 0..15), round to nearest even.
+__device__ __forceinline__ uint32_t f2_to_bf16x2(uint64_t d) {
+  float lo, hi;
+  f2_unpack(d, lo, hi);
+  return pack_bf16x2(lo, hi);
+}
+
 // ------------------------------------------------------- NVFP4 arithmetic
 // g = amax_t / 2688 (6 * 448), 1 when amax_t = 0.
 __device__ __forceinline__ float nvfp4_global_scale(float amax_t) {
@@ -115,9 +154,11 @@ __device__ __forceinline__ uint32_t nvfp4_block_scale(float amax_b, float amax_t
 // Eight bf16 values (four packed words) times r -> eight E2M1 codes; 0 when r = 0.
 __device__ __forceinline__ uint32_t nvfp4_codes8(const uint32_t* pw, float r) {
   if (r == 0.f) return 0u;
-  return e2m1x8(__fmul_rn(bf16lo(pw[0]), r), __fmul_rn(bf16hi(pw[0]), r), __fmul_rn(bf16lo(pw[1]), r),
-                __fmul_rn(bf16hi(pw[1]), r), __fmul_rn(bf16lo(pw[2]), r), __fmul_rn(bf16hi(pw[2]), r),
-                __fmul_rn(bf16lo(pw[3]), r), __fmul_rn(bf16hi(pw[3]), r));
+  const uint64_t r2 = f2_pack(r, r);
+  float y[8];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) f2_unpack(f2_mul(f2_from_bf16x2(pw[e]), r2), y[2 * e], y[2 * e + 1]);
+  return e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
 }
 // |x| max of eight bf16 values (four packed words), as a float.
 __device__ __forceinline__ float bf16x8_absmax(const uint32_t* pw) {
@@ -191,8 +232,9 @@ __device__ __forceinline__ void hist_accumulate(uint32_t* h, float amax) {
   __threadfence();
 }
 // One thread per CTA, after a CTA barrier that follows every
-// hist_accumulate of the CTA.
-__device__ __forceinline__ void hist_arrive(uint32_t* h) {
+// hist_accumulate of the CTA (or with the CTA's whole amax in cta_amax).
+__device__ __forceinline__ void hist_arrive(uint32_t* h, float cta_amax = 0.f) {
+  if (cta_amax > 0.f) atomicMax(h + 1, __float_as_uint(cta_amax));
   __threadfence();
   if (atomicAdd(h + 2, 1u) == gridDim.x * gridDim.y * gridDim.z - 1) {
     __threadfence();

@@ -32,7 +32,7 @@ int launch_layernorm(const void* x, int64_t M, int64_t H, int64_t ldx, float eps
                      float* amax_out, float* row_amax_out, const uint8_t* pred, int num_sms, cudaStream_t s);
 
 // LayerNorm that also quantizes its output (NVFP4 by delayed scaling, INT8
-// exact per row); every output pointer is optional.  H % 8 == 0 and
+// exact per row); every output pointer is optional.  H % 16 == 0 and
 // H <= kLnQuantMaxH; NVFP4 / INT8 outputs need H % 64 == 0.
 constexpr int64_t kLnQuantMaxH = 4096;
 struct LnQuantCall {

@@ -320,7 +320,7 @@ struct Params {
   const uint8_t* q_pred;
 };
 
-template <int BN, int MODE, int STAGES, int KB, int NC, bool PAIR>
+template <int BN, int MODE, int STAGES, int KB, int NC, bool PAIR, bool QO>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
@@ -582,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // scaling); a lane holds 32 consecutive columns of one row, i.e. two
     // whole 16-element blocks.  Either way the lane tracks |bf16 y|'s max
     // over its rows < M for the history.
-    const bool qo = p.q_hist != nullptr;
+    const bool qo = QO && p.q_hist != nullptr;   // compiled out of the plain GEMM
     const bool q_nv = qo && (p.q_pred == nullptr || *p.q_pred != 0);
     const float q_amax_t = qo ? __fmul_rn(p.q_headroom, hist_prev(p.q_hist)) : 0.f;
     const float q_g = nvfp4_global_scale(q_amax_t);
@@ -800,7 +800,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0 && p.q_hist) hist_arrive(p.q_hist);
+  if (QO && threadIdx.x == 0 && p.q_hist) hist_arrive(p.q_hist);
   if constexpr (PAIR) cluster_sync();          // the leader's MMAs into this CTA's TMEM are complete
   if (warp == 1) {
     tc_fence_after();
@@ -833,7 +833,7 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int MODE, int STAGES, int KB, int NC, bool PAIR>
+template <int BN, int MODE, int STAGES, int KB, int NC, bool PAIR, bool QO>
 int run(const GemmCall& c, int num_sms, cudaStream_t s) {
   using Cf = Cfg<BN, MODE, STAGES, KB, NC, PAIR>;
   constexpr CUtensorMapSwizzle kSw = KB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
@@ -916,7 +916,7 @@ int run(const GemmCall& c, int num_sms, cudaStream_t s) {
   p.q_codes = c.q_codes; p.q_sf = c.q_sf; p.q_g = c.q_g; p.q_hist = c.q_hist; p.q_headroom = c.q_headroom;
   p.q_pred = c.q_pred;
 
-  auto kern = gemm_fp4_kernel<BN, MODE, STAGES, KB, NC, PAIR>;
+  auto kern = gemm_fp4_kernel<BN, MODE, STAGES, KB, NC, PAIR, QO>;
   static bool attr_set = false;
   if (!attr_set) {
     // The register split (setmaxnreg) assumes exactly kLaunchRegs per thread
@@ -964,9 +964,17 @@ int launch_gemm_fp4(const GemmCall& c, int num_sms, cudaStream_t s) {
   const bool chunked = (c.K / 2) % 64 == 0;
   // W4A4: 128-byte K steps (a 128-byte box row per TMA row: 7-8% faster than
   // two 64-byte chunks); the K tail past K/2 bytes reads as zeros.
-  if (c.mode == 0) return run<256, 0, GEMM_PAIR ? 5 : 3, 128, 1, GEMM_PAIR>(c, num_sms, s);
-  return chunked ? run<256, 1, W4A8_STAGES, 64, W4A8_NC, GEMM_PAIR>(c, num_sms, s)
-                 : run<256, 1, W4A8_STAGES, 64, 1, GEMM_PAIR>(c, num_sms, s);
+  // The quantizing epilogue is a separate instantiation: its code, even
+  // when not taken, slowed the plain epilogue (the critical path of the
+  // K = 1920 layers) by 5-10%.
+  if (c.q_hist) {
+    if (c.mode == 0) return run<256, 0, GEMM_PAIR ? 5 : 3, 128, 1, GEMM_PAIR, true>(c, num_sms, s);
+    return chunked ? run<256, 1, W4A8_STAGES, 64, W4A8_NC, GEMM_PAIR, true>(c, num_sms, s)
+                   : run<256, 1, W4A8_STAGES, 64, 1, GEMM_PAIR, true>(c, num_sms, s);
+  }
+  if (c.mode == 0) return run<256, 0, GEMM_PAIR ? 5 : 3, 128, 1, GEMM_PAIR, false>(c, num_sms, s);
+  return chunked ? run<256, 1, W4A8_STAGES, 64, W4A8_NC, GEMM_PAIR, false>(c, num_sms, s)
+                 : run<256, 1, W4A8_STAGES, 64, 1, GEMM_PAIR, false>(c, num_sms, s);
 }
 
 }  // namespace sixbit

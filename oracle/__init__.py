@@ -28,4 +28,4 @@ the kernels use.  Sums, matrix products and norms are float64.
 
 Parity status per function is listed in each module's header.
 """
-from . import codecs, nvfp4, int8, gemm, gamma, dmpq, tdc, block, calib  # noqa: F401
+from . import codecs, nvfp4, int8, gemm, gamma, dmpq, tdc, block, calib, mxcache  # noqa: F401

@@ -92,11 +92,12 @@ def block_forward(x_bits, wq_block, flags, amax_hist=None, headroom=2.0):
 
 
 def run_stack(x_steps, wq_blocks, alpha, beta, tau, tau_tdc, max_skip=1, use_tdc=True,
-              forced_flags=None, forced_skips=None, refresh_every=0, fused=False, headroom=2.0):
+              forced_flags=None, forced_skips=None, refresh_every=0, fused=False, headroom=2.0, tdc_cache="bf16"):
     """Run every step.  Returns dict(outputs, flags[t], skips[t], gammas[t], r2[t]).
 
     fused: fused producers with delayed NVFP4 scaling (module header); every
-    block's amax history starts at zero.
+    block's amax history starts at zero.  tdc_cache: "bf16", or "mx" for the
+    compressed update cache of oracle.mxcache (an extension).
 
     forced_flags (optional) [steps][layers] replaces DMPQ's decisions and
     forced_skips (optional) [steps][blocks] replaces TDC's (teacher forcing
@@ -127,7 +128,7 @@ def run_stack(x_steps, wq_blocks, alpha, beta, tau, tau_tdc, max_skip=1, use_tdc
                 tdc.after_skip(c)
             else:
                 out = block_forward(h, wq_blocks[l], flags[4 * l:4 * l + 4], hist[l], headroom)
-            G, dn, r2 = gamma.block_pass(h, out, c.delta, computed=not skip)
+            G, dn, r2 = gamma.block_pass(h, out, c.delta, computed=not skip, cache=tdc_cache)
             if not skip:
                 tdc.after_compute(c, dn, r2)
             g_t[l] = G

@@ -48,7 +48,7 @@ class BlockCache:
     fresh_count: int = 0
     consec: int = 0
     r2: np.float32 = F32(np.inf)
-    delta: np.ndarray | None = None       # bf16 bits
+    delta: np.ndarray | None = None       # bf16 bits, or float32 cached values (compressed cache)
 
 
 def decide(cache: BlockCache, tau_tdc: float, max_skip: int, refresh_every: int = 0, step: int = 0) -> bool:
@@ -59,8 +59,11 @@ def decide(cache: BlockCache, tau_tdc: float, max_skip: int, refresh_every: int 
 
 
 def apply(xin, delta_fresh):
-    """Skipped block output: bf16(f32(in) + f32(Delta_fresh))."""
-    return f32_to_bf16((bf16_to_f32(xin) + bf16_to_f32(delta_fresh)).astype(F32))
+    """Skipped block output: bf16(f32(in) + f32(Delta_fresh)); Delta_fresh is bf16
+    bits or the float32 value of a compressed cache."""
+    d = np.asarray(delta_fresh)
+    df = bf16_to_f32(d) if d.dtype == np.uint16 else d.astype(F32)
+    return f32_to_bf16((bf16_to_f32(xin) + df).astype(F32))
 
 
 def after_skip(cache: BlockCache) -> None:

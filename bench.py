@@ -234,11 +234,13 @@ STACKS = {
 }
 
 
-def time_producers(sb, L, dev, reps=20):
-    """Quantizing producers at the 2B shapes, each launch timed alone with CUDA
-    events (median of `reps`, a 256 MB L2 flush before each): the LayerNorm
-    over the FFN input (M x 1920) with each output, and the FFN up-projection
-    (GELU) whose epilogue emits the down layer's NVFP4 input."""
+def time_producers(sb, L, dev, gpair, reps=20):
+    """Quantizing producers and the compressed-cache Gamma pass at the 2B
+    shapes, each launch timed alone with CUDA events (median of `reps`, a
+    256 MB L2 flush before each): the LayerNorm over the FFN input
+    (M x 1920) with each output, the FFN up-projection (GELU) whose epilogue
+    emits the down layer's NVFP4 input, and the Gamma / Delta / r2 pass with
+    the bf16 and the compressed update cache."""
     import torch
     x = L[0]["x"]
     M, H = x.shape
@@ -252,7 +254,19 @@ def time_producers(sb, L, dev, reps=20):
     hist = sb.amax_history(2, dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     elt = M * H
+    bin_, bout = gpair
+    dcache = torch.zeros((M, H), dtype=torch.bfloat16, device=dev)
+    mcache = sb.mxcache(elt, dev)
+    st = torch.tensor([1, 0], dtype=torch.int32, device=dev)
+    gr = torch.empty(2, dtype=torch.float32, device=dev)
+
+    def gamma_call(cache):
+        st.fill_(1)                              # one previous update: the pass reads it and writes r2
+        sb.block_gamma(bin_, bout, delta=cache, gamma_out=gr[0:1], r2_out=gr[1:2], tdc_state=st)
+
     cases = {
+        "gamma_delta_bf16_cache": (lambda: gamma_call(dcache), 8 * elt),
+        "gamma_delta_mx_cache": (lambda: gamma_call(mcache), 4 * elt + 2 * int(sb.lib().sixbit_mxcache_bytes(elt))),
         "layernorm_bf16": (lambda: sb.layernorm(x, out=y), 4 * elt),
         "layernorm_nvfp4": (lambda: sb.layernorm_quant(x, nvfp4=(codes, sf, g), amax_hist=hist[0]), 2.5625 * elt),
         "layernorm_int8": (lambda: sb.layernorm_quant(x, int8=(planes, rs)), 3.5 * elt + 4 * M),
@@ -338,12 +352,16 @@ def run_stack_bench(name: str, dev):
     max_skip 1.  Also the PDR variant "pdr": max_skip 2 with a forced
     computed step every 4th step, and "measured_lines": (alpha, beta) refitted
     from E_rel measured on the first calib_steps steps (DMPQ calibration side)
-    with tau set from them, and "dmpq_tdc_fused_quant": DMPQ+TDC with the
+    with tau set from them, "dmpq_tdc_fused_quant": DMPQ+TDC with the
     quantizing producers (LayerNorms and the up-projection's epilogue emit
-    the next layer's NVFP4 / INT8 input; delayed NVFP4 scaling).  Timed:
-    every step's graph replay plus its input copy."""
+    the next layer's NVFP4 / INT8 input; delayed NVFP4 scaling), and the
+    "_mxcache" modes: the update cache stored as E4M3 codes with a
+    power-of-two scale per 32 elements.  Timed: every step's graph replay
+    plus its input copy."""
     import torch
+    from nvfp4_int8_mixed_gb300 import lib as _lib
     from nvfp4_int8_mixed_gb300.stack import DiTStack, calibrate_lines, calibrate_tau
+    sb_mx_bytes = lambda n: _lib().sixbit_mxcache_bytes(n)
     c = STACKS[name]
     nb, M, H, F, T = c["n_blocks"], c["M"], c["H"], c["F"], c["steps"]
     gen = torch.Generator(device=dev).manual_seed(c["seed"])
@@ -366,7 +384,8 @@ def run_stack_bench(name: str, dev):
     tau = calibrate_tau(stack, xs)
     res = {"config": f"{nb} blocks, M={M}, H={H}, F={F}, {T} steps", "tau": tau}
     runs = [("dmpq_tdc", 1, 0, None), ("dmpq_only", 0, 0, None), ("pdr_skip2_refresh4", 2, 4, None),
-            ("dmpq_tdc_fused_quant", 1, 0, None)]
+            ("dmpq_tdc_fused_quant", 1, 0, None), ("dmpq_tdc_mxcache", 1, 0, None),
+            ("dmpq_tdc_fused_quant_mxcache", 1, 0, None)]
     if c.get("calib_steps"):
         cal = calibrate_lines(stack, xs, weights, steps=c["calib_steps"])
         lines = (cal["alpha"].astype(np.float32), cal["beta"].astype(np.float32))
@@ -379,13 +398,14 @@ def run_stack_bench(name: str, dev):
     res["bf16_torch_context"] = bf16_stack_context(weights, xs, H)
     del weights
     for mode, max_skip, refresh, lines in runs:
+        stack.fused = "fused_quant" in mode
+        stack.set_tdc_cache("mx" if mode.endswith("mxcache") else "bf16")
         if lines is not None:
             stack.alpha.copy_(torch.from_numpy(lines[0]))
             stack.beta.copy_(torch.from_numpy(lines[1]))
             tau = calibrate_tau(stack, xs)
             res["calibration"]["tau"] = tau
         stack.tau, stack.max_skip, stack.refresh_every = tau, max_skip, refresh
-        stack.fused = mode.endswith("fused_quant")
         stack.graph = None
         stack.reset()
         stack.capture()
@@ -412,9 +432,9 @@ def run_stack_bench(name: str, dev):
     w_nvfp4 = sum(int(t.numel() * t.element_size()) for b in stack.wq for wl in b.values() for t in wl)
     act = sum(int(t.numel() * t.element_size()) for t in (stack.x_in, *stack.buf, stack.h1, stack.qkv, stack.x1,
                                                          stack.h2, stack.u, stack.codes, stack.sf, stack.planes))
-    cache = sum(int(d.numel() * d.element_size()) for d in stack.delta)
+    cache = nb * M * H * 2
     res["footprint_bytes"] = {"weights_nvfp4": w_nvfp4, "weights_bf16": 2 * w_params, "activations": act,
-                              "tdc_cache": cache,
+                              "tdc_cache": cache, "tdc_cache_mx": nb * int(sb_mx_bytes(M * H)),
                               "weights_ratio_bf16_over_nvfp4": 2 * w_params / w_nvfp4}
     del stack, xs
     torch.cuda.empty_cache()
@@ -691,7 +711,7 @@ def run_ours(args):
     tf = {n: {"ms": mean_t[n] * 1e3, "TFLOP/s": flops_layer[[l["name"] for l in L].index(n.split("[")[1][:-1])]
                     / mean_t[n] / 1e12} for n in gemm_names}
 
-    producers = time_producers(sb, L, dev) if rank == 0 and args.workload == "2b" else None
+    producers = time_producers(sb, L, dev, (bin_, bout)) if rank == 0 and args.workload == "2b" else None
 
     stack_res = None
     if rank == 0 and args.stack != "none":

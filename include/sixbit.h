@@ -216,6 +216,39 @@ int sixbit_tdc_decide_and_apply(const void* in, const void* delta, int64_t n, co
                                 uint8_t* compute_out, void* out, uint8_t* gates, int32_t n_gates,
                                 sixbit_stream_t stream);
 
+/* ---- Compressed update cache (an extension, not from the pages: Figure 2
+ * reuses a block's update, the pages do not say how it is stored).  One bf16
+ * update per block is 2 B/element (2-9 GB for the pages' models); this
+ * cache stores it as E4M3 codes with one power-of-two scale per 32
+ * consecutive elements, 1.03 B/element:
+ *   k_b = the smallest integer with max|D| over block b <= 448 * 2^k_b,
+ *         clamped to [-127, 127] (-127 for a zero block);
+ *   code_i = E4M3(D_i * 2^-k_b) (round to nearest even, saturating);
+ *   cached value = E4M3(code_i) * 2^k_b.
+ * Layout: n code bytes, then n/32 scale bytes (k_b + 127).  Element type and
+ * block size are those of OCP MXFP8 (E4M3); its shared-exponent rule can
+ * clip a block's largest element, this one does not.  n % 32 == 0. */
+
+/* Bytes of a compressed cache for n elements (0 if n <= 0 or n % 32 != 0). */
+size_t sixbit_mxcache_bytes(int64_t n);
+
+/* a7 with the compressed cache: as sixbit_block_gamma, with `cache`
+ * (sixbit_mxcache_bytes(n), 16-byte aligned, nullable) in place of delta.
+ * r2 compares the exact D_new = bf16(f32(out)-f32(in)) with the cached value
+ * of the previous update; a computed block stores D_new encoded.
+ * ws: sixbit_workspace_size(n, 1) bytes. */
+int sixbit_block_gamma_mxcache(const void* in, const void* out, int64_t n, void* cache,
+                               float* gamma_out, float* r2_out, int32_t* tdc_state,
+                               const uint8_t* computed, void* ws, sixbit_stream_t stream);
+
+/* a9 with the compressed cache: the decision of sixbit_tdc_decide_and_apply;
+ * a skipped block's output is bf16(f32(in) + cached value). */
+int sixbit_tdc_decide_and_apply_mxcache(const void* in, const void* cache, int64_t n, const float* r2,
+                                        float tau_tdc, int32_t max_skip, int32_t refresh_every,
+                                        const int32_t* step, const int32_t* tdc_state,
+                                        uint8_t* compute_out, void* out, uint8_t* gates, int32_t n_gates,
+                                        sixbit_stream_t stream);
+
 /* Block harness: LayerNorm without affine over rows of H, eps given,
  * fp32 statistics, bf16 out.  Optional side outputs for the next quantizer:
  * amax_out (tensor max |y|, zeroed by the call) and row_amax_out [M]. */

@@ -45,6 +45,10 @@ _SIGS = {
     "sixbit_pair_stats": ([_P, _I32, _P, _I32, _I64, _P, _P, _P], _INT),
     "sixbit_tdc_decide_and_apply": ([_P, _P, _I64, _P, _F, _I32, _I32, _P, _P, _P, _P, _P, _I32, _P], _INT),
     "sixbit_layernorm_bf16": ([_P, _I64, _I64, _I64, _F, _P, _I64, _P, _P, _P, _P], _INT),
+    "sixbit_mxcache_bytes": ([_I64], ctypes.c_size_t),
+    "sixbit_block_gamma_mxcache": ([_P, _P, _I64, _P, _P, _P, _P, _P, _P, _P], _INT),
+    "sixbit_tdc_decide_and_apply_mxcache": ([_P, _P, _I64, _P, _F, _I32, _I32, _P, _P, _P, _P, _P, _I32, _P],
+                                            _INT),
     "sixbit_layernorm_quant": ([_P, _I64, _I64, _I64, _F, _P, _I64, _P, _P, _P, _P, _F, _P, _P, _P, _P, _P, _P],
                                _INT),
     "sixbit_qlinear_qout": ([_INT, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _I64, _P, _INT, _P, _I64, _P, _P, _P, _P,
@@ -240,16 +244,26 @@ def qlinear_qout(mode: str, a, w_codes, w_sf, g_w, q_codes, q_sf, q_g, amax_hist
 
 
 # --------------------------------------------------------------- block ops
+def mxcache(n: int, device=None) -> torch.Tensor:
+    """A zeroed compressed update cache for n elements (uint8, codes then scales)."""
+    nb = int(lib().sixbit_mxcache_bytes(n))
+    if nb == 0:
+        raise ValueError("the compressed cache needs n > 0 and n % 32 == 0")
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    return torch.zeros(nb, dtype=torch.uint8, device=dev)
+
+
 def block_gamma(xin, xout, delta=None, gamma_out=None, r2_out=None, tdc_state=None, computed=None):
-    """a7: Gamma (and Delta in place, r2, TDC counters). Returns (gamma [1], r2 [1])."""
+    """a7: Gamma (and Delta in place, r2, TDC counters). Returns (gamma [1], r2 [1]).
+    delta: the bf16 update, or a uint8 compressed cache (mxcache)."""
     _need_cuda(xin, xout)
     n = xin.numel()
     dev = xin.device
     g = gamma_out if gamma_out is not None else torch.empty(1, dtype=torch.float32, device=dev)
     r2 = r2_out if r2_out is not None else torch.full((1,), float("nan"), dtype=torch.float32, device=dev)
-    _check("sixbit_block_gamma",
-           lib().sixbit_block_gamma(_ptr(xin), _ptr(xout), n, _ptr(delta), _ptr(g), _ptr(r2), _ptr(tdc_state),
-                                    _ptr(computed), _ptr(_ws_for(n)), _stream()))
+    name = "sixbit_block_gamma_mxcache" if delta is not None and delta.dtype == torch.uint8 else "sixbit_block_gamma"
+    _check(name, getattr(lib(), name)(_ptr(xin), _ptr(xout), n, _ptr(delta), _ptr(g), _ptr(r2), _ptr(tdc_state),
+                                      _ptr(computed), _ptr(_ws_for(n)), _stream()))
     return g, r2
 
 
@@ -284,13 +298,13 @@ def tdc_decide_and_apply(xin, delta, r2, tau_tdc: float, max_skip: int, tdc_stat
                          refresh_every: int = 0, step=None):
     """a9: compute_out[0] = 1 if the block must run; on a skip out = in + Delta.
     refresh_every > 0 (with step, a device int32) forces a computed step every
-    refresh_every steps."""
+    refresh_every steps.  delta: the bf16 update, or a uint8 compressed cache."""
     n = xin.numel()
-    _check("sixbit_tdc_decide_and_apply",
-           lib().sixbit_tdc_decide_and_apply(_ptr(xin), _ptr(delta), n, _ptr(r2), float(tau_tdc), int(max_skip),
-                                             int(refresh_every), _ptr(step), _ptr(tdc_state), _ptr(compute_out),
-                                             _ptr(out), _ptr(gates), gates.numel() if gates is not None else 0,
-                                             _stream()))
+    name = "sixbit_tdc_decide_and_apply_mxcache" if delta.dtype == torch.uint8 else "sixbit_tdc_decide_and_apply"
+    _check(name, getattr(lib(), name)(_ptr(xin), _ptr(delta), n, _ptr(r2), float(tau_tdc), int(max_skip),
+                                      int(refresh_every), _ptr(step), _ptr(tdc_state), _ptr(compute_out),
+                                      _ptr(out), _ptr(gates), gates.numel() if gates is not None else 0,
+                                      _stream()))
     return compute_out
 
 

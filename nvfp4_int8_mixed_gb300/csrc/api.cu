@@ -239,6 +239,37 @@ int sixbit_tdc_decide_and_apply(const void* in, const void* delta, int64_t n, co
                     gates ? n_gates : 0, sms, cs(stream));
 }
 
+size_t sixbit_mxcache_bytes(int64_t n) {
+  if (n <= 0 || n % 32 != 0) return 0;
+  return size_t(n + n / 32);
+}
+
+int sixbit_block_gamma_mxcache(const void* in, const void* out, int64_t n, void* cache, float* gamma_out,
+                               float* r2_out, int32_t* tdc_state, const uint8_t* computed, void* ws,
+                               sixbit_stream_t stream) {
+  if (!in || !out || !gamma_out || !ws || n <= 0) return kEInval;
+  if (n % 32 != 0 || n > (int64_t(1) << 40)) return kEShape;
+  if (!aligned16(in) || !aligned16(out) || (cache && !aligned16(cache)) || !aligned16(ws)) return kEAlign;
+  int sms;
+  if (device_setup(&sms, nullptr) != kOk) return kELaunch;
+  return launch_block_gamma_mx(in, out, n, cache, gamma_out, r2_out, tdc_state, computed, ws, sms, cs(stream));
+}
+
+int sixbit_tdc_decide_and_apply_mxcache(const void* in, const void* cache, int64_t n, const float* r2, float tau_tdc,
+                                        int32_t max_skip, int32_t refresh_every, const int32_t* step,
+                                        const int32_t* tdc_state, uint8_t* compute_out, void* out, uint8_t* gates,
+                                        int32_t n_gates, sixbit_stream_t stream) {
+  if (!in || !cache || !r2 || !tdc_state || !compute_out || !out || n <= 0 || (gates && n_gates < 0)) return kEInval;
+  if (refresh_every < 0 || (refresh_every > 0 && !step)) return kEInval;
+  if (n % 32 != 0) return kEShape;
+  if (!aligned16(in) || !aligned16(cache) || !aligned16(out)) return kEAlign;
+  int sms;
+  if (device_setup(&sms, nullptr) != kOk) return kELaunch;
+  const float tau2 = tau_tdc * tau_tdc;   // float32 product, round to nearest
+  return launch_tdc_mx(in, cache, n, r2, tau2, max_skip, refresh_every, step, tdc_state, compute_out, out, gates,
+                       gates ? n_gates : 0, sms, cs(stream));
+}
+
 int sixbit_layernorm_bf16(const void* x, int64_t M, int64_t H, int64_t ldx, float eps, void* y, int64_t ldy,
                           float* amax_out, float* row_amax_out, const uint8_t* pred, sixbit_stream_t stream) {
   if (!x || !y || M < 0 || H <= 0 || ldx < H || ldy < H) return kEInval;

@@ -44,6 +44,56 @@ __device__ __forceinline__ void block_sum4(float v[4], float (*sm)[4]) {
   }
 }
 
+// End of a Gamma pass: CTA partials to scratch as float64; the last CTA to
+// finish sums them in CTA order, writes Gamma / r2, advances the TDC
+// counters and resets the scratch counter.
+__device__ __forceinline__ void gamma_finish(float s1, float s0, float sd, float so, bool do_r2, bool computed,
+                                             float* gamma_out, float* r2_out, int32_t* tdc_state, GammaWs* ws,
+                                             double* partials) {
+  __shared__ float sm[kThreads / 32][4];
+  __shared__ bool is_last;
+  float v[4] = {s1, s0, sd, so};
+  block_sum4(v, sm);
+  if (threadIdx.x == 0) {
+    double* p = partials + 4 * int64_t(blockIdx.x);
+    p[0] = v[0]; p[1] = v[1]; p[2] = v[2]; p[3] = v[3];
+    __threadfence();
+    const unsigned int ticket = atomicAdd(&ws->counter, 1u);
+    is_last = (ticket == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  // Last CTA: float64 sum of the partials, thread t over tiles t, t+256, ...
+  // then a fixed tree.
+  __shared__ double dsm[kThreads][4];
+  double acc[4] = {0, 0, 0, 0};
+  for (int64_t t = threadIdx.x; t < gridDim.x; t += kThreads) {
+    const volatile double* p = partials + 4 * t;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] += p[i];
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dsm[threadIdx.x][i] = acc[i];
+  __syncthreads();
+  for (int h = kThreads / 2; h > 0; h >>= 1) {
+    if (threadIdx.x < h)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dsm[threadIdx.x][i] += dsm[threadIdx.x + h][i];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double S1 = dsm[0][0], S0 = dsm[0][1], Sd = dsm[0][2], So = dsm[0][3];
+    if (gamma_out) *gamma_out = (S0 == 0.0) ? 0.f : float(S1 / S0);
+    if (do_r2) *r2_out = (So == 0.0) ? __int_as_float(0x7f800000) : float(Sd / So);
+    if (tdc_state) {
+      if (computed) { tdc_state[0] += 1; tdc_state[1] = 0; }
+      else tdc_state[1] += 1;
+    }
+    ws->counter = 0u;
+  }
+}
+
 // a7: one pass over (in, out, previous Delta).  Per element:
 //   d = f32(out) - f32(in); S1 += |d|; S0 += |in|;
 //   if computed: D_new = bf16(d) (stored over D_old); if r2 wanted:
@@ -57,8 +107,6 @@ __device__ __forceinline__ void block_sum4(float v[4], float (*sm)[4]) {
 __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_kernel(
     const uint16_t* __restrict__ xin, const uint16_t* __restrict__ xout, int64_t n, uint16_t* delta, float* gamma_out,
     float* r2_out, int32_t* tdc_state, const uint8_t* computed_ptr, GammaWs* ws, double* partials) {
-  __shared__ float sm[kThreads / 32][4];
-  __shared__ bool is_last;
   const bool computed = computed_ptr ? (*computed_ptr != 0) : true;
   const bool do_delta = computed && delta != nullptr;
   const bool do_r2 = do_delta && r2_out != nullptr && (tdc_state ? tdc_state[0] >= 1 : true);
@@ -119,46 +167,96 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_kernel(
       }
     }
   }
-  float v[4] = {s1, s0, sd, so};
-  block_sum4(v, sm);
-  if (threadIdx.x == 0) {
-    double* p = partials + 4 * int64_t(blockIdx.x);
-    p[0] = v[0]; p[1] = v[1]; p[2] = v[2]; p[3] = v[3];
-    __threadfence();
-    const unsigned int ticket = atomicAdd(&ws->counter, 1u);
-    is_last = (ticket == gridDim.x - 1);
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  // Last CTA: float64 sum of the partials, thread t over tiles t, t+256, ...
-  // then a fixed tree.
-  __shared__ double dsm[kThreads][4];
-  double acc[4] = {0, 0, 0, 0};
-  for (int64_t t = threadIdx.x; t < gridDim.x; t += kThreads) {
-    const volatile double* p = partials + 4 * t;
+  gamma_finish(s1, s0, sd, so, do_r2, computed, gamma_out, r2_out, tdc_state, ws, partials);
+}
+
+// a7 with the compressed update cache (an extension; layout in common.cuh):
+// the same pass, but the previous update is read as E4M3 codes times its
+// block scale, r2 compares the exact bf16 D_new with that cached value, and
+// D_new is stored encoded.  Four consecutive threads hold one 32-element
+// block (8 elements each): its maximum is two shuffles, and the first of the
+// four reads the old scale byte and writes the new one (so its read comes
+// before its own write).  n % 32 == 0.
+__global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_mx_kernel(
+    const uint16_t* __restrict__ xin, const uint16_t* __restrict__ xout, int64_t n, uint8_t* cache, float* gamma_out,
+    float* r2_out, int32_t* tdc_state, const uint8_t* computed_ptr, GammaWs* ws, double* partials) {
+  const bool computed = computed_ptr ? (*computed_ptr != 0) : true;
+  const bool do_delta = computed && cache != nullptr;
+  const bool do_r2 = do_delta && r2_out != nullptr && (tdc_state ? tdc_state[0] >= 1 : true);
+  uint8_t* scales = cache ? cache + n : nullptr;
+  const int lane = threadIdx.x & 31;
+  const bool first = (lane & 3) == 0;
+  const int64_t ntiles = cdiv(n, kTile);
+  float s1 = 0.f, s0 = 0.f, sd = 0.f, so = 0.f;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t base = t * kTile;
+    uint4 vi[kVecPerThread], vo[kVecPerThread];
+    uint2 vc[kVecPerThread];
+    uint32_t vs[kVecPerThread];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] += p[i];
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) dsm[threadIdx.x][i] = acc[i];
-  __syncthreads();
-  for (int h = kThreads / 2; h > 0; h >>= 1) {
-    if (threadIdx.x < h)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) dsm[threadIdx.x][i] += dsm[threadIdx.x + h][i];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    const double S1 = dsm[0][0], S0 = dsm[0][1], Sd = dsm[0][2], So = dsm[0][3];
-    if (gamma_out) *gamma_out = (S0 == 0.0) ? 0.f : float(S1 / S0);
-    if (do_r2) *r2_out = (So == 0.0) ? __int_as_float(0x7f800000) : float(Sd / So);
-    if (tdc_state) {
-      if (computed) { tdc_state[0] += 1; tdc_state[1] = 0; }
-      else tdc_state[1] += 1;
+    for (int i = 0; i < kVecPerThread; ++i) {
+      const int64_t idx = base + (int64_t(i) * kThreads + threadIdx.x) * 8;
+      vi[i] = vo[i] = make_uint4(0, 0, 0, 0);
+      vc[i] = make_uint2(0, 0);
+      vs[i] = 0;
+      if (idx < n) {                          // n % 32 == 0: whole 8-element groups
+        vi[i] = ldg_nc_v4(xin + idx);
+        vo[i] = ldg_nc_v4(xout + idx);
+        if (do_r2) {
+          vc[i] = *reinterpret_cast<const uint2*>(cache + idx);
+          if (first) vs[i] = scales[idx / 32];
+        }
+      }
     }
-    ws->counter = 0u;
+#pragma unroll
+    for (int i = 0; i < kVecPerThread; ++i) {
+      const int64_t idx = base + (int64_t(i) * kThreads + threadIdx.x) * 8;
+      const bool valid = idx < n;               // uniform over each group of four threads
+      const uint32_t* a = &vi[i].x;
+      const uint32_t* b = &vo[i].x;
+      uint32_t pw[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float i0 = bf16lo(a[e]), i1 = bf16hi(a[e]);
+        const float d0 = __fsub_rn(bf16lo(b[e]), i0), d1 = __fsub_rn(bf16hi(b[e]), i1);
+        s1 += fabsf(d0) + fabsf(d1);
+        s0 += fabsf(i0) + fabsf(i1);
+        pw[e] = pack_bf16x2(d0, d1);           // D_new: one rounding of the fp32 difference
+      }
+      if (do_r2) {
+        const uint32_t sc = __shfl_sync(0xffffffffu, vs[i], lane & ~3);
+        float c[8];
+        mx_decode8(vc[i], exp2i(int(sc) - 127), c);
+        if (valid) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float e0 = __fsub_rn(bf16lo(pw[e]), c[2 * e]), e1 = __fsub_rn(bf16hi(pw[e]), c[2 * e + 1]);
+            sd = __fmaf_rn(e1, e1, __fmaf_rn(e0, e0, sd));
+            so = __fmaf_rn(c[2 * e + 1], c[2 * e + 1], __fmaf_rn(c[2 * e], c[2 * e], so));
+          }
+        }
+      }
+      if (do_delta) {
+        float am = bf16x8_absmax(pw);
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+        const int k = mx_scale_exp(am);
+        const float inv = exp2i(-k);
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          y[2 * e] = __fmul_rn(bf16lo(pw[e]), inv);
+          y[2 * e + 1] = __fmul_rn(bf16hi(pw[e]), inv);
+        }
+        if (valid) {
+          *reinterpret_cast<uint2*>(cache + idx) =
+              make_uint2(e4m3x4(y[0], y[1], y[2], y[3]), e4m3x4(y[4], y[5], y[6], y[7]));
+          if (first) scales[idx / 32] = uint8_t(k + 127);
+        }
+      }
+    }
   }
+  gamma_finish(s1, s0, sd, so, do_r2, computed, gamma_out, r2_out, tdc_state, ws, partials);
 }
 
 // Calibration diagnostic (DMPQ side, Figures 1 and 4): one pass over two
@@ -330,6 +428,39 @@ __global__ void __launch_bounds__(kThreads) layernorm_kernel(const uint16_t* __r
     tmax = fmaxf(tmax, rmax);
   }
   if (amax_out && lane == 0) atomic_max_nonneg(amax_out, tmax);
+}
+
+// a9 with the compressed update cache: the decision as tdc_kernel; a
+// skipped block's output is bf16(in + E4M3(code) * 2^k).  n % 32 == 0.
+__global__ void __launch_bounds__(kThreads) tdc_mx_kernel(const uint16_t* __restrict__ xin,
+                                                          const uint8_t* __restrict__ cache, int64_t n, const float* r2,
+                                                          float tau2, int32_t max_skip, int32_t refresh_every,
+                                                          const int32_t* step, const int32_t* tdc_state,
+                                                          uint8_t* compute_out, uint16_t* __restrict__ out,
+                                                          uint8_t* gates, int32_t n_gates) {
+  const bool refresh = refresh_every > 0 && (*step % refresh_every) == 0;
+  const bool skip = !refresh && tdc_state[0] >= 2 && *r2 < tau2 && tdc_state[1] < max_skip;
+  if (blockIdx.x == 0) {
+    if (threadIdx.x == 0) *compute_out = skip ? 0 : 1;
+    if (skip && gates)
+      for (int i = threadIdx.x; i < n_gates; i += blockDim.x) gates[i] = 0;
+  }
+  if (!skip) return;
+  const uint8_t* scales = cache + n;
+  const int64_t nvec = n / 8;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec; v += stride) {
+    const uint4 a = ldg_nc_v4(xin + v * 8);
+    float c[8];
+    mx_decode8(*reinterpret_cast<const uint2*>(cache + v * 8), exp2i(int(scales[v / 4]) - 127), c);
+    const uint32_t* pa = &a.x;
+    uint4 w;
+    uint32_t* pw = &w.x;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      pw[e] = pack_bf16x2(__fadd_rn(bf16lo(pa[e]), c[2 * e]), __fadd_rn(bf16hi(pa[e]), c[2 * e + 1]));
+    *reinterpret_cast<uint4*>(out + v * 8) = w;
+  }
 }
 
 // LayerNorm that quantizes its own output for the next linear layer.  One
@@ -572,6 +703,16 @@ int launch_block_gamma(const void* xin, const void* xout, int64_t n, void* delta
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 
+int launch_block_gamma_mx(const void* xin, const void* xout, int64_t n, void* cache, float* gamma_out, float* r2_out,
+                          int32_t* tdc_state, const uint8_t* computed, void* ws, int num_sms, cudaStream_t s) {
+  GammaWs* w = static_cast<GammaWs*>(ws);
+  double* partials = reinterpret_cast<double*>(static_cast<char*>(ws) + 256);
+  gamma_mx_kernel<<<unsigned(gamma_grid(n, num_sms)), kThreads, 0, s>>>(
+      static_cast<const uint16_t*>(xin), static_cast<const uint16_t*>(xout), n, static_cast<uint8_t*>(cache),
+      gamma_out, r2_out, tdc_state, computed, w, partials);
+  return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
+}
+
 int launch_pair_stats(const void* a, int a_f32, const void* b, int b_f32, int64_t n, double* out, void* ws,
                       int num_sms, cudaStream_t s) {
   GammaWs* w = static_cast<GammaWs*>(ws);
@@ -609,6 +750,18 @@ int launch_tdc(const void* xin, const void* delta, int64_t n, const float* r2, f
   tdc_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(xin), static_cast<const uint16_t*>(delta), n, r2,
                                        tau2, max_skip, refresh_every, step, tdc_state, compute_out,
                                        static_cast<uint16_t*>(out), gates, n_gates);
+  return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
+}
+
+int launch_tdc_mx(const void* xin, const void* cache, int64_t n, const float* r2, float tau2, int32_t max_skip,
+                  int32_t refresh_every, const int32_t* step, const int32_t* tdc_state, uint8_t* compute_out,
+                  void* out, uint8_t* gates, int32_t n_gates, int num_sms, cudaStream_t s) {
+  int64_t want = cdiv(n / 8 + 1, kThreads * 4);
+  int64_t cap = int64_t(num_sms) * 8;
+  const unsigned grid = unsigned(want < cap ? (want < 1 ? 1 : want) : cap);
+  tdc_mx_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(xin), static_cast<const uint8_t*>(cache), n, r2,
+                                          tau2, max_skip, refresh_every, step, tdc_state, compute_out,
+                                          static_cast<uint16_t*>(out), gates, n_gates);
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 

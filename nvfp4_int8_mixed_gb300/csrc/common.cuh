@@ -244,6 +244,49 @@ __device__ __forceinline__ void hist_arrive(uint32_t* h, float cta_amax = 0.f) {
   }
 }
 
+// ------------------------------------------- compressed update cache (MX)
+// A block update cached as E4M3 codes with one power-of-two scale per 32
+// consecutive elements: scale byte k + 127, k the smallest integer with the
+// block's max |v| <= 448 * 2^k, clamped to [-127, 127] (-127 for a zero
+// block); code = E4M3(v * 2^-k); value = E4M3(code) * 2^k.  Layout: n code
+// bytes, then n/32 scale bytes.
+__device__ __forceinline__ int mx_scale_exp(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  const int e = int((b >> 23) & 0xFFu);
+  if (!(amax > 0.f) || e == 0) return -127;    // zero (or fp32-subnormal) maximum
+  const int k = (e - 127) - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);   // mantissa 1.75 = 0x600000
+  return k < -127 ? -127 : (k > 127 ? 127 : k);
+}
+// 2^k exactly, k in [-127, 127] (2^-127 is an fp32 subnormal).
+__device__ __forceinline__ float exp2i(int k) {
+  return k >= -126 ? __uint_as_float(uint32_t(k + 127) << 23) : __uint_as_float(0x00400000u);
+}
+// Four floats -> four E4M3 codes (f0 in the low byte), round to nearest even, saturating.
+__device__ __forceinline__ uint32_t e4m3x4(float f0, float f1, float f2, float f3) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(f1), "f"(f0));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(f3), "f"(f2));
+  return uint32_t(lo) | (uint32_t(hi) << 16);
+}
+// Two E4M3 codes (low byte first) -> two floats (exact).
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t two, float& lo, float& hi) {
+  uint32_t h2;
+  const uint16_t in = uint16_t(two & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  asm("{ .reg .f16 a, b;\n mov.b32 {a, b}, %2;\n cvt.f32.f16 %0, a;\n cvt.f32.f16 %1, b; }"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2));
+}
+// Eight cached values: codes (two words, element 0 in the low byte) times 2^k.
+__device__ __forceinline__ void mx_decode8(uint2 codes, float scale, float* v) {
+  e4m3x2_to_f32(codes.x, v[0], v[1]);
+  e4m3x2_to_f32(codes.x >> 16, v[2], v[3]);
+  e4m3x2_to_f32(codes.y, v[4], v[5]);
+  e4m3x2_to_f32(codes.y >> 16, v[6], v[7]);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], scale);
+}
+
 // Swizzled scale-factor byte offset: 128x4 atoms of 512 bytes.
 __host__ __device__ __forceinline__ int64_t sf_offset(int64_t m, int64_t c, int64_t kc4) {
   return ((m >> 7) * (kc4 >> 2) + (c >> 2)) * 512 + (m & 31) * 16 + ((m & 127) >> 5) * 4 + (c & 3);

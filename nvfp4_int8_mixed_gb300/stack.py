@@ -27,7 +27,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (amax_history, block_gamma, dmpq_assign, layernorm, layernorm_quant, qlinear_qout, qlinear_w4a4,
+from . import (amax_history, block_gamma, dmpq_assign, layernorm, layernorm_quant, mxcache, qlinear_qout, qlinear_w4a4,
                qlinear_w4a8, quantize_act_int8, quantize_act_nvfp4, quantize_weight_nvfp4, sf_bytes,
                tdc_decide_and_apply)
 
@@ -43,12 +43,14 @@ class DiTStack:
     block, layer order qkv, out, up, down); tau: DMPQ threshold; tau_tdc,
     max_skip: TDC rule (max_skip = 0 disables skipping); refresh_every: PDR
     periodic refresh (every k-th step is computed; 0 = off); fused: quantizing
-    producers with delayed NVFP4 scaling (headroom: its power-of-two margin).
+    producers with delayed NVFP4 scaling (headroom: its power-of-two margin);
+    tdc_cache: "bf16" (one bf16 update per block) or "mx" (the compressed
+    cache: E4M3 codes with a power-of-two scale per 32 elements).
     """
 
     def __init__(self, weights, alpha, beta, M: int, H: int, F: int, tau: float, tau_tdc: float = 0.05,
                  max_skip: int = 1, device=None, refresh_every: int = 0, fused: bool = False,
-                 headroom: float = 2.0):
+                 headroom: float = 2.0, tdc_cache: str = "bf16"):
         self.dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
         dev = self.dev
         self.nb, self.M, self.H, self.F = len(weights), M, H, F
@@ -91,12 +93,28 @@ class DiTStack:
         self.use_nvfp4 = torch.zeros(nl, dtype=torch.uint8, device=dev)
         self.gates = torch.zeros((nl, 2), dtype=torch.uint8, device=dev)
         self.gamma = torch.zeros(self.nb, dtype=torch.float32, device=dev)
-        self.delta = [torch.zeros((M, H), **bf) for _ in range(self.nb)]
+        if tdc_cache not in ("bf16", "mx"):
+            raise ValueError("tdc_cache is 'bf16' or 'mx'")
+        self.tdc_cache = tdc_cache
+        self.delta = [torch.zeros((M, H), **bf) if tdc_cache == "bf16" else mxcache(M * H, dev)
+                      for _ in range(self.nb)]
         self.r2 = torch.full((self.nb,), float("inf"), dtype=torch.float32, device=dev)
         self.state = torch.zeros((self.nb, 2), dtype=torch.int32, device=dev)
         self.cflag = torch.ones(self.nb, dtype=torch.uint8, device=dev)
         self.graph = None
         self.out = self.buf[(self.nb - 1) % 2]
+
+    def set_tdc_cache(self, fmt: str):
+        """Switch the update cache format ("bf16" / "mx"); clears the caches and
+        drops the captured graph."""
+        if fmt not in ("bf16", "mx"):
+            raise ValueError("tdc_cache is 'bf16' or 'mx'")
+        if fmt != self.tdc_cache:
+            M, H = self.M, self.H
+            self.delta = [torch.zeros((M, H), dtype=torch.bfloat16, device=self.dev) if fmt == "bf16"
+                          else mxcache(M * H, self.dev) for _ in range(self.nb)]
+            self.tdc_cache = fmt
+        self.graph = None
 
     # ------------------------------------------------------------ one step
     def _ql(self, x, wq, gate_nv, gate_i8, out, amax_in=None, row_amax_in=None, residual=None, gelu=False):
@@ -302,6 +320,8 @@ def calibrate_lines(stack: DiTStack, xs, weights, steps=None):
     r2 [layers].
     """
     from . import pair_stats, qlinear_w4a4, qlinear_w4a8
+    if stack.tdc_cache != "bf16":
+        raise ValueError("calibration compares bf16 updates: build the stack with tdc_cache='bf16'")
     T = len(xs) if steps is None else min(steps, len(xs))
     nb = stack.nb
     names = ("qkv", "out", "up", "down")

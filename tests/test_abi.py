@@ -82,6 +82,20 @@ def test_argument_errors_before_launch(lib):
                                      None) == sb.ESHAPE
 
 
+def test_mxcache_argument_errors(lib):
+    import nvfp4_int8_mixed_gb300 as sb
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    assert lib.sixbit_mxcache_bytes(64) == 66 and lib.sixbit_mxcache_bytes(33) == 0 and lib.sixbit_mxcache_bytes(0) == 0
+    assert lib.sixbit_block_gamma_mxcache(fake, fake, 48, fake, fake, None, None, None, fake, None) == sb.ESHAPE
+    assert lib.sixbit_block_gamma_mxcache(fake, fake, 64, P((1 << 20) + 8), fake, None, None, None, fake,
+                                          None) == sb.EALIGN
+    assert lib.sixbit_tdc_decide_and_apply_mxcache(fake, None, 64, fake, ctypes.c_float(0.05), 1, 0, None, fake,
+                                                   fake, fake, None, 0, None) == sb.EINVAL
+    assert lib.sixbit_tdc_decide_and_apply_mxcache(fake, fake, 40, fake, ctypes.c_float(0.05), 1, 0, None, fake,
+                                                   fake, fake, None, 0, None) == sb.ESHAPE
+
+
 def test_quantizing_producer_argument_errors(lib):
     import nvfp4_int8_mixed_gb300 as sb
     P = ctypes.c_void_p

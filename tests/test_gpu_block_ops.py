@@ -129,3 +129,62 @@ def test_layernorm(M, H):
     assert np.all(np.abs(got[rows] - ref) <= 2.0 ** -7 * np.abs(ref) + 1e-6)
     assert host(amax)[0] == np.max(np.abs(got))
     assert np.array_equal(host(ramax), np.max(np.abs(got), axis=1).astype(np.float32))
+
+
+# ------------------------------------------- compressed update cache (MX)
+def _mx_prev(p):
+    from oracle import mxcache
+    codes, sc = mxcache.encode(codecs.bf16_to_f32(p["delta_prev"]))
+    return mxcache.to_bytes(codes, sc), mxcache.decode(codes, sc)
+
+
+@pytest.mark.parametrize("M,H", [(256, 256), (1, 32), (3, 8192 + 96), (synthetic.M_2B, 1920)])
+def test_gamma_mxcache_parity(M, H):
+    from oracle import mxcache
+    sb = _sb()
+    p = synthetic.gamma_pair(M * 5 + H, M, H)
+    prev_bytes, prev_val = _mx_prev(p)
+    cache = dev(prev_bytes)
+    assert cache.numel() == sb.lib().sixbit_mxcache_bytes(M * H)
+    xin, xout = dev_bf16(p["xin"]), dev_bf16(p["xout"])
+    state = torch.tensor([1, 0], dtype=torch.int32, device="cuda")
+    g, r2 = sb.block_gamma(xin, xout, delta=cache, tdc_state=state)
+    rdn = o_gamma.delta(p["xin"], p["xout"])
+    rr2 = o_gamma.rel_l2_sq(rdn, prev_val.reshape(M, H))
+    rg = o_gamma.gamma(p["xin"], p["xout"])
+    assert abs(host(g)[0] - rg) <= RTOL * abs(rg)
+    assert abs(host(r2)[0] - rr2) <= RTOL * abs(rr2) + 1e-12
+    codes, sc = mxcache.encode(codecs.bf16_to_f32(rdn))
+    assert np.array_equal(host(cache), mxcache.to_bytes(codes, sc))       # the new update, encoded
+    assert host(state).tolist() == [2, 0]
+    # a first update (no previous one): no r2, the cache is written
+    c2 = torch.zeros_like(cache)
+    r2b = torch.full((1,), 0.5, device="cuda")
+    st0 = torch.tensor([0, 0], dtype=torch.int32, device="cuda")
+    sb.block_gamma(xin, xout, delta=c2, r2_out=r2b, tdc_state=st0)
+    assert np.array_equal(host(c2), host(cache)) and host(r2b)[0] == 0.5
+    # a skipped block leaves the cache alone
+    c3 = dev(prev_bytes)
+    sb.block_gamma(xin, xout, delta=c3, tdc_state=state, computed=torch.zeros(1, dtype=torch.uint8, device="cuda"))
+    assert np.array_equal(host(c3), prev_bytes)
+
+
+@pytest.mark.parametrize("n", [32, 8192 * 3 + 64, synthetic.M_2B * 1920])
+def test_tdc_mxcache_skip_output(n):
+    from oracle import mxcache
+    sb = _sb()
+    g = synthetic.rng(n % 1000)
+    xin = codecs.f32_to_bf16(g.standard_normal(n).astype(np.float32))
+    d = codecs.f32_to_bf16((0.05 * g.standard_normal(n)).astype(np.float32))
+    d[:32] = 0                                                            # a zero block
+    codes, sc = mxcache.encode(codecs.bf16_to_f32(d))
+    cache = dev(mxcache.to_bytes(codes, sc))
+    out = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    state = torch.tensor([2, 0], dtype=torch.int32, device="cuda")
+    r2 = torch.tensor([1e-6], device="cuda")
+    cflag = torch.empty(1, dtype=torch.uint8, device="cuda")
+    gates = torch.ones(8, dtype=torch.uint8, device="cuda")
+    sb.tdc_decide_and_apply(dev_bf16(xin), cache, r2, 0.05, 1, state, cflag, out, gates=gates)
+    assert host(cflag)[0] == 0 and not host(gates).any()
+    ref = o_tdc.apply(xin, mxcache.decode(codes, sc))
+    assert np.array_equal(host_bf16_bits(out), ref)

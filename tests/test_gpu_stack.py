@@ -17,13 +17,13 @@ from tests.helpers import dev_bf16, host, host_bf16_bits
 pytestmark = pytest.mark.gpu
 
 
-def _run(tau_tdc, max_skip, nb=3, M=300, H=256, F=512, steps=6, seed=7, refresh=0, fused=False):
+def _run(tau_tdc, max_skip, nb=3, M=300, H=256, F=512, steps=6, seed=7, refresh=0, fused=False, cache="bf16"):
     from nvfp4_int8_mixed_gb300.stack import DiTStack, calibrate_tau
     st = synthetic.stack_setup(seed, nb, H, F)
     xs = synthetic.stack_inputs(st["noise_seed"], M, H, steps)
     xs_dev = [dev_bf16(x) for x in xs]
     stack = DiTStack(st["blocks"], st["alpha"], st["beta"], M, H, F, tau=0.0, tau_tdc=tau_tdc, max_skip=max_skip,
-                     refresh_every=refresh, fused=fused)
+                     refresh_every=refresh, fused=fused, tdc_cache=cache)
     tau = calibrate_tau(stack, xs_dev)
     stack.tau = tau
     outs, log = stack.run(xs_dev, record=True)
@@ -32,12 +32,14 @@ def _run(tau_tdc, max_skip, nb=3, M=300, H=256, F=512, steps=6, seed=7, refresh=
     return st, xs, tau, [host_bf16_bits(o) for o in outs], rec
 
 
-@pytest.mark.parametrize("tau_tdc,max_skip,refresh,fused", [
-    (0.0, 1, 0, False), (10.0, 1, 0, False), (0.05, 1, 0, False),
-    (10.0, 3, 3, False),                        # PDR: 3 reuses, refresh every 3rd step
-    (0.05, 1, 0, True), (10.0, 1, 0, True)])    # quantizing producers, delayed NVFP4 scaling
-def test_stack_decisions_and_outputs(tau_tdc, max_skip, refresh, fused):
-    st, xs, tau, outs, rec = _run(tau_tdc, max_skip, refresh=refresh, steps=8 if refresh else 6, fused=fused)
+@pytest.mark.parametrize("tau_tdc,max_skip,refresh,fused,cache", [
+    (0.0, 1, 0, False, "bf16"), (10.0, 1, 0, False, "bf16"), (0.05, 1, 0, False, "bf16"),
+    (10.0, 3, 3, False, "bf16"),                # PDR: 3 reuses, refresh every 3rd step
+    (0.05, 1, 0, True, "bf16"), (10.0, 1, 0, True, "bf16"),   # quantizing producers, delayed NVFP4 scaling
+    (0.05, 1, 0, False, "mx"), (10.0, 1, 0, True, "mx")])     # compressed update cache
+def test_stack_decisions_and_outputs(tau_tdc, max_skip, refresh, fused, cache):
+    st, xs, tau, outs, rec = _run(tau_tdc, max_skip, refresh=refresh, steps=8 if refresh else 6, fused=fused,
+                                  cache=cache)
     nb = len(st["blocks"])
     lb = np.repeat(np.arange(nb), 4)
     steps = len(xs)
@@ -59,7 +61,7 @@ def test_stack_decisions_and_outputs(tau_tdc, max_skip, refresh, fused):
     # outputs under the same decisions
     wq = [{k: o_block.quantize_weights(v) for k, v in b.items()} for b in st["blocks"]]
     ref = o_block.run_stack(xs, wq, st["alpha"], st["beta"], tau, tau_tdc, max_skip,
-                            forced_flags=rec["flags"], forced_skips=rec["skips"], fused=fused)
+                            forced_flags=rec["flags"], forced_skips=rec["skips"], fused=fused, tdc_cache=cache)
     for t in range(steps):
         g = codecs.bf16_to_f32(outs[t]).astype(np.float64)
         r = codecs.bf16_to_f32(ref["outputs"][t]).astype(np.float64)

@@ -288,13 +288,34 @@ __host__ __device__ constexpr uint32_t idesc_fp4(int m, int n) {
 }
 
 // tanh-form GELU, 0.5 x (1 + tanh(u)) with u = sqrt(2/pi) (x + 0.044715 x^3),
-// written as x / (1 + exp(-2u)) (the same function).  exp and the division
-// use the hardware approximations (ex2.approx, rcp.approx: ~1e-6 relative);
-// the IEEE reciprocal's special-case path made this epilogue slower than the
-// tile's MMAs.  Large negative u gives exp = inf and a result of -0.
-__device__ __forceinline__ float gelu_tanh(float x) {
-  const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
-  return __fdividef(x, 1.f + __expf(-2.f * u));
+// written as x / (1 + 2^t), t = -2 u log2(e) (the same function), for two
+// elements at a time.  2^t is the hardware approximation (ex2.approx, one
+// special-function op an element); the reciprocal is computed on the FMA
+// pipe: the seed 2*bits(1.0) - bits(d) (exact at powers of two, at most
+// 12.5 % high in between), then three Newton steps r += r (1 - d r), which
+// take the relative error to 1.6e-2, 2.4e-4 and 6e-8.  Two special-function
+// ops an element (exp and reciprocal) bounded the FFN-up epilogue.  t is
+// clamped at 126 so d stays finite (a large negative x gives ~x * 2^-126).
+__device__ __forceinline__ void gelu_tanh2(float& x0, float& x1) {
+  const uint64_t x = f2_pack(x0, x1);
+  const uint64_t xx = f2_mul(x, x);
+  const uint64_t p = f2_fma(xx, f2_pack(0.044715f, 0.044715f), f2_pack(1.f, 1.f));   // 1 + 0.044715 x^2
+  // t = -2 sqrt(2/pi) log2(e) x (1 + 0.044715 x^2)
+  const uint64_t t2 = f2_mul(f2_mul(x, p), f2_pack(-2.302208198f, -2.302208198f));
+  float t0, t1;
+  f2_unpack(t2, t0, t1);
+  float e0, e1;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(e0) : "f"(fminf(t0, 126.f)));
+  asm("ex2.approx.f32 %0, %1;" : "=f"(e1) : "f"(fminf(t1, 126.f)));
+  const uint64_t one = f2_pack(1.f, 1.f);
+  const uint64_t d = f2_add(f2_pack(e0, e1), one);
+  float d0, d1;
+  f2_unpack(d, d0, d1);
+  uint64_t r = f2_pack(__int_as_float(0x7F000000 - __float_as_int(d0)), __int_as_float(0x7F000000 - __float_as_int(d1)));
+  const uint64_t nd = f2_sub(0, d);                                                // -d
+#pragma unroll
+  for (int it = 0; it < 3; ++it) r = f2_fma(r, f2_fma(nd, r, one), r);
+  f2_unpack(f2_mul(x, r), x0, x1);
 }
 
 struct Params {
@@ -637,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (p.gelu) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+            for (int i = 0; i < 32; i += 2) gelu_tanh2(v[i], v[i + 1]);
           }
           uint32_t pk[16];                       // the bf16 values the unfused path would store
 #pragma unroll
@@ -704,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (p.gelu) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+              for (int i = 0; i < 32; i += 2) gelu_tanh2(v[i], v[i + 1]);
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -767,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (p.gelu) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+            for (int i = 0; i < 32; i += 2) gelu_tanh2(v[i], v[i + 1]);
           }
           if (p.residual) {
             const uint16_t* rp = p.residual + int64_t(m) * p.ldr + n0;

@@ -202,6 +202,14 @@ def time_oracle(layers, M, rows, cols, steps=1, warmup=0, seed=0):
 
 
 # ---------------------------------------------------------------- reference arm
+def workload_config(workload: str, M: int, layers, ws: int) -> dict:
+    """The `config` of the JSON line, the same for both arms."""
+    return {"workload": f"{workload.upper()}-class video-DiT GEMM set, M={M} tokens, "
+                        "4 linears x (NVFP4+W4A4, INT8+W4A8) + Gamma/DMPQ/TDC",
+            "shapes": [[name, M, K, N] for name, K, N, _, _ in layers], "l2": "inputs larger than L2",
+            "parallelism": f"replicas x{ws}"}
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -221,7 +229,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{args.workload.upper()}-class video-DiT GEMM set, M={M}, oracle sample"},
+            "config": workload_config(args.workload, M, layers, ws),
             "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -300,6 +308,29 @@ def time_producers(sb, L, dev, gpair, reps=20):
     return out
 
 
+def time_oracle_block(weight_block, x_bits, M: int, row_counts=(128, 512), seed=0):
+    """CPU baseline of the stack metric: the oracle's block_forward on one
+    block at two row counts (random rows of the block input), timed on the
+    host cores; the time is fitted as fixed + per-row cost and extrapolated
+    to M rows.  Layer formats: qkv, up NVFP4; out, down INT8."""
+    from oracle import block as o_block
+    wq = {k: o_block.quantize_weights(np.asarray(v, np.float32)) for k, v in weight_block.items()}
+    rng = np.random.default_rng(seed)
+    flags = np.array([1, 0, 1, 0], np.uint8)
+    ts = []
+    for r in row_counts:
+        rows = np.sort(rng.choice(x_bits.shape[0], r, replace=False))
+        t0 = time.perf_counter()
+        o_block.block_forward(x_bits[rows], wq, flags)
+        ts.append(time.perf_counter() - t0)
+    b = (ts[1] - ts[0]) / (row_counts[1] - row_counts[0])
+    a = max(ts[0] - b * row_counts[0], 0.0)
+    t_full = a + b * M
+    return {"blocks_per_s": 1.0 / t_full, "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"oracle block_forward of one block at {row_counts[0]} and {row_counts[1]} random rows "
+                      f"({ts[0]:.1f} s, {ts[1]:.1f} s); blocks/s extrapolated linearly in rows to M={M}"}
+
+
 def bf16_stack_context(weights, xs, H):
     """The same block stack in plain bf16 torch ops (cuBLAS GEMMs), one CUDA
     graph per step: the unquantized "original" the pages compare against.
@@ -342,7 +373,7 @@ def bf16_stack_context(weights, xs, H):
     return {"blocks_per_s": len(weights) * len(xs) / sec, "ms_per_step": sec / len(xs) * 1e3}
 
 
-def run_stack_bench(name: str, dev):
+def run_stack_bench(name: str, dev, cpu_oracle: bool = False):
     """Blocks/s of the synthetic DiT stack with DMPQ+TDC and with DMPQ only.
 
     Weights N(0, 0.02) and the input drift x_t = x_{t-1} + sigma_t N(0,1)
@@ -396,6 +427,9 @@ def run_stack_bench(name: str, dev):
                               "delta_cos_mean": fin(cal["delta_cos"]), "delta_rel_mean": fin(cal["delta_rel"])}
         runs.append(("measured_lines", 1, 0, lines))
     res["bf16_torch_context"] = bf16_stack_context(weights, xs, H)
+    if cpu_oracle:
+        xb = xs[0].view(torch.int16).cpu().numpy().view(np.uint16)
+        res["cpu_oracle"] = time_oracle_block({k: v.cpu().numpy() for k, v in weights[0].items()}, xb, M)
     del weights
     for mode, max_skip, refresh, lines in runs:
         stack.fused = "fused_quant" in mode
@@ -715,7 +749,7 @@ def run_ours(args):
 
     stack_res = None
     if rank == 0 and args.stack != "none":
-        stack_res = run_stack_bench(args.stack, dev)
+        stack_res = run_stack_bench(args.stack, dev, cpu_oracle=not args.no_cpu_baseline)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -730,13 +764,10 @@ def run_ours(args):
                 "warmup": max(args.warmup, 3), "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "fp4 (e2m1 x e2m1, fp32 accumulate)",
                 "data": "synthetic",
-                "config": {"workload": f"{args.workload.upper()}-class video-DiT GEMM set, M={M} tokens, "
-                                       "4 linears x (NVFP4+W4A4, INT8+W4A8) + Gamma/DMPQ/TDC",
-                           "shapes": [[l["name"], M, l["K"], l["N"]] for l in L], "l2": "inputs larger than L2",
-                           "timing": "the K steps captured as one CUDA graph, replayed once between CUDA events; "
-                                     + ("per-launch events inside the graph" if in_graph_events
-                                        else "per-launch events from eager steps after the timed region"),
-                           "parallelism": f"replicas x{ws}"},
+                "config": dict(workload_config(args.workload, M, layers, ws),
+                               timing="the K steps captured as one CUDA graph, replayed once between CUDA events; "
+                                      + ("per-launch events inside the graph" if in_graph_events
+                                         else "per-launch events from eager steps after the timed region")),
                 "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
                         "d2h_bytes_per_step": int(d2h)},
                 "gpu_launches": launches_per_step * args.steps,

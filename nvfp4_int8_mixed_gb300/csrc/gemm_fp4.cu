@@ -84,8 +84,16 @@ struct Cfg {
   static constexpr int offB = kPlanes * kA;
   static constexpr int offSFA = offB + kB;
   static constexpr int offSFB = offSFA + kSFA;
-  static constexpr int kStage = offSFB + kSFB;
-  static_assert(kStage % 1024 == 0, "stages stay 1024-byte aligned");
+  // W4A4 on a single CTA keeps the scale atoms in a ring of their own
+  // (kSfSlots slots of shared memory and TMEM, with their own barriers), so
+  // the scale path can run ahead of the code tiles instead of landing with
+  // them; the stages then hold the codes only.
+  static constexpr bool kSfRing = MODE == 0 && !PAIR;
+  static constexpr int kSfSlots = kSfRing ? 4 : STAGES;    // TMEM scale slots
+  static constexpr int kStage = kSfRing ? offSFA : offSFB + kSFB;
+  static constexpr int kSfSlotBytes = kSFA + kSFB;         // one ring slot: SFA atoms, then SFB atoms
+  static constexpr int kRing = kSfRing ? kSfSlots * kSfSlotBytes : 0;
+  static_assert(kStage % 1024 == 0 && kSfSlotBytes % 1024 == 0, "stages stay 1024-byte aligned");
   static constexpr uint32_t kTxA = kPlanes * kA;           // bytes landed per stage, by producer
   static constexpr uint32_t kTxB = kB;
   static constexpr uint32_t kTxS = kSFA + kSFB;
@@ -95,11 +103,11 @@ struct Cfg {
   static constexpr int kSfaCols = MODE == 0 ? 4 * kAtoms : 0;
   static constexpr int kSfStride = kSfaCols + 4 * kAtoms * kRT;
   static constexpr int kSfBase = BN;
-  static constexpr int kConstCol = kSfBase + STAGES * kSfStride;
+  static constexpr int kConstCol = kSfBase + kSfSlots * kSfStride;
   static_assert(kConstCol + 12 <= int(kTmemCols), "TMEM budget");
   static constexpr int kStaging = 8 * 4096;               // per epilogue warp: 32 rows x 128 bytes of output
   static constexpr int kExtra = 1024;                      // barriers, TMEM address, abort flag
-  static constexpr size_t kSmem = size_t(STAGES) * kStage + kStaging + kExtra + 1024;
+  static constexpr size_t kSmem = size_t(STAGES) * kStage + kRing + kStaging + kExtra + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -351,11 +359,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (p.pred && *p.pred == 0) return;          // both CTAs of a pair read the same gate
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* staging = smem + size_t(STAGES) * C::kStage;          // 8 x 4 KB, 1024-byte aligned
+  uint8_t* ring = smem + size_t(STAGES) * C::kStage;             // scale-atom ring (W4A4, one CTA)
+  uint8_t* staging = ring + C::kRing;                            // 8 x 4 KB, 1024-byte aligned
   uint8_t* extra = staging + C::kStaging;
-  // barriers: full[S] empty[S] sfready[S] tfull tempty drain resid[8]
+  // barriers: full[S] empty[S] sfready[R] tfull tempty drain resid[8] sffull[R] sfempty[R], R = kSfSlots
+  constexpr int R = C::kSfSlots;
   uint64_t* bars = reinterpret_cast<uint64_t*>(extra);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 3 + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 3 * R + 11);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -364,10 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto full_bar = [&](int s) { return bar0 + 8u * uint32_t(s); };
   auto empty_bar = [&](int s) { return bar0 + 8u * uint32_t(STAGES + s); };
   auto sfready_bar = [&](int s) { return bar0 + 8u * uint32_t(2 * STAGES + s); };
-  const uint32_t tfull_bar = bar0 + 8u * uint32_t(3 * STAGES);
-  const uint32_t tempty_bar = bar0 + 8u * uint32_t(3 * STAGES + 1);
-  const uint32_t drain_bar = bar0 + 8u * uint32_t(3 * STAGES + 2);
-  auto resid_bar = [&](int w) { return bar0 + 8u * uint32_t(3 * STAGES + 3 + w); };
+  const uint32_t tfull_bar = bar0 + 8u * uint32_t(2 * STAGES + R);
+  const uint32_t tempty_bar = bar0 + 8u * uint32_t(2 * STAGES + R + 1);
+  const uint32_t drain_bar = bar0 + 8u * uint32_t(2 * STAGES + R + 2);
+  auto resid_bar = [&](int w) { return bar0 + 8u * uint32_t(2 * STAGES + R + 3 + w); };
+  auto sffull_bar = [&](int s) { return bar0 + 8u * uint32_t(2 * STAGES + R + 11 + s); };   // ring only
+  auto sfempty_bar = [&](int s) { return bar0 + 8u * uint32_t(2 * STAGES + 2 * R + 11 + s); };
   // Arrival on a barrier of the issuing CTA (rank 0): local, or across the pair.
   auto arrive_leader = [&](uint32_t bar) {
     if constexpr (PAIR) mbar_arrive_remote(map_rank(bar, 0));
@@ -377,9 +389,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 3);               // the A, W and scale producers
+      mbar_init(full_bar(s), C::kSfRing ? 2 : 3);   // the A and W producers (and the scale producer)
       mbar_init(empty_bar(s), 1);
+    }
+    for (int s = 0; s < R; ++s) {
       mbar_init(sfready_bar(s), 4 * kCtas);    // one arrival per scale warp of the pair
+      if (C::kSfRing) {
+        mbar_init(sffull_bar(s), 1);           // the scale producer
+        mbar_init(sfempty_bar(s), 1);          // the MMA commit of the k-step that read the slot
+      }
     }
     mbar_init(tfull_bar, 1);
     mbar_init(tempty_bar, 8 * kCtas);          // one arrival per epilogue warp of the pair
@@ -425,19 +443,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Descriptors of stage 0; stage s adds s * kStage bytes (>> 4) to the start address field.
     const uint64_t adesc_s0 = desc_kmajor<KB>(smem_u32(smem));
     const uint64_t bdesc_s0 = desc_kmajor<KB>(smem_u32(smem + C::offB));
-    int stage = 0;
-    uint32_t phase = 0, acc_phase = 0;
+    int stage = 0, slot = 0;
+    uint32_t phase = 0, sphase = 0, acc_phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x / kCtas; tile < ntiles && ok; tile += gridDim.x / kCtas) {
       // the epilogue warps (of both CTAs) have pulled the previous tile out of TMEM
       if (!mbar_wait<PAIR>(tempty_bar, acc_phase ^ 1u, abort_flag)) { fail(); ok = false; break; }
       tc_fence_after();
       for (int kt = 0; kt < p.KT; ++kt) {
-        // the stage landed and the scale warps (of both CTAs) have written its scales
-        if (!mbar_wait<PAIR>(sfready_bar(stage), phase, abort_flag)) { fail(); ok = false; break; }
+        // the codes landed and the scale warps (of both CTAs) have written the k-step's scales
+        if (C::kSfRing && !mbar_wait(full_bar(stage), phase, abort_flag)) { fail(); ok = false; break; }
+        if (!mbar_wait<PAIR>(sfready_bar(slot), C::kSfRing ? sphase : phase, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint64_t soff = uint64_t((stage * C::kStage) >> 4);
-        const uint32_t sfa_t = tmem + uint32_t(C::kSfBase + stage * C::kSfStride);
+        const uint32_t sfa_t = tmem + uint32_t(C::kSfBase + slot * C::kSfStride);
         const uint32_t sfb_t = sfa_t + uint32_t(C::kSfaCols);
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
@@ -459,6 +482,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_commit_all<PAIR>(empty_bar(stage));       // frees the stage in both CTAs
+        if constexpr (C::kSfRing) {
+          tc_commit_all<PAIR>(sfempty_bar(slot));    // frees the ring slot (smem and TMEM)
+          if (++slot == R) { slot = 0; sphase ^= 1u; }
+        } else {
+          slot = stage + 1 == STAGES ? 0 : stage + 1;
+        }
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
@@ -481,6 +510,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 75 ns plus ~150 ns per stage, which one producer for all four ops
       // of a stage could not keep ahead of the stage's MMAs.
       const int role = warp == 0 ? 0 : (warp == 2 ? 1 : 2);
+      if (C::kSfRing && role == 2) {
+        // the scale-atom ring: paced by its own free barrier, not the code stages'
+        int slot = 0;
+        uint32_t sphase = 0, issued = 0, last_par = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x / kCtas; tile < ntiles && ok; tile += gridDim.x / kCtas) {
+          const int mt = tile / p.NT, nt = tile - mt * p.NT;
+          const int arow = mt * C::kTileM;
+          for (int kt = 0; kt < p.KT; ++kt) {
+            if (!mbar_wait(sfempty_bar(slot), sphase ^ 1u, abort_flag)) { fail(); ok = false; break; }
+            uint8_t* rb = ring + size_t(slot) * C::kSfSlotBytes;
+            const uint32_t fb = sffull_bar(slot);
+            mbar_expect_tx(fb, C::kTxS);
+            tma_load_3d(smem_u32(rb), &tmSFA, 0, kt * C::kAtoms, arow / BM, fb);
+            tma_load_3d(smem_u32(rb + C::kSFA), &tmSFB, 0, kt * C::kAtoms, nt * C::kRT, fb);
+            issued |= 1u << slot;
+            last_par = (last_par & ~(1u << slot)) | (sphase << slot);
+            if (++slot == R) { slot = 0; sphase ^= 1u; }
+          }
+        }
+        if (!ok) {   // let the copies already issued land before the CTA exits
+          for (int s = 0; s < R; ++s)
+            if (issued & (1u << s)) mbar_wait(sffull_bar(s), (last_par >> s) & 1u, nullptr);
+        }
+      } else {
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
@@ -521,14 +575,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < STAGES; ++s)
           if (issued & (1u << s)) mbar_wait(full_bar(s), (last_par >> s) & 1u, nullptr);
       }
+      }
     } else if (warp == 1 && lane == 0 && rank == 0) {
       mma_issuer();
     }
   } else if (warp < 8) {
     regs_dec<kLowRegs>();
     // ------------------------------------------------------------ scale warps
-    // Stage s's TMEM scale columns are free again once stage s is refilled:
-    // the producers waited for the MMAs that read them (empty barrier).
+    // A slot's TMEM scale columns are free again once its next scales have
+    // landed: their producer waited for the MMAs that read the slot (the
+    // ring's free barrier, or the stage's empty barrier without the ring).
     const int q = warp & 3;
     const uint32_t lane_base = uint32_t(q * 32) << 16;
     if (MODE == 1) {
@@ -538,26 +594,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st4(cb + 4, 0x50505050u);
       tmem_st4(cb + 8, 0x38383838u);
     }
-    int stage = 0;
+    int slot = 0;                                // ring slot (the code stage when there is no ring)
     uint32_t phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x / kCtas; tile < ntiles && ok; tile += gridDim.x / kCtas) {
       for (int kt = 0; kt < p.KT; ++kt) {
         // every lane waits (each acquires the landed bytes); the verdict is
         // made warp-uniform so the .sync.aligned stores below never diverge
-        const bool landed = mbar_wait(full_bar(stage), phase, abort_flag);
+        const bool landed = mbar_wait(C::kSfRing ? sffull_bar(slot) : full_bar(slot), phase, abort_flag);
         if (!__all_sync(0xffffffffu, landed)) {
           if (lane == 0) fail();
           ok = false;
           break;
         }
-        const uint8_t* sb = smem + size_t(stage) * C::kStage;
-        const uint32_t sfa_t = tmem + lane_base + uint32_t(C::kSfBase + stage * C::kSfStride);
+        const uint8_t* sfa_s = C::kSfRing ? ring + size_t(slot) * C::kSfSlotBytes
+                                          : smem + size_t(slot) * C::kStage + C::offSFA;
+        const uint8_t* sfb_s = C::kSfRing ? sfa_s + C::kSFA : smem + size_t(slot) * C::kStage + C::offSFB;
+        const uint32_t sfa_t = tmem + lane_base + uint32_t(C::kSfBase + slot * C::kSfStride);
         const uint32_t sfb_t = sfa_t + uint32_t(C::kSfaCols);
         if (MODE == 0) {
           uint4 wa[C::kAtoms];
 #pragma unroll
-          for (int a = 0; a < C::kAtoms; ++a) wa[a] = *reinterpret_cast<const uint4*>(sb + C::offSFA + 512 * a + 16 * lane);
+          for (int a = 0; a < C::kAtoms; ++a) wa[a] = *reinterpret_cast<const uint4*>(sfa_s + 512 * a + 16 * lane);
           if constexpr (C::kAtoms == 4) {
             tmem_st16(sfa_t, wa[0], wa[1], wa[2], wa[3]);
           } else {
@@ -566,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int g = 0; g < C::kAtoms / 2; ++g) {   // K steps 2g, 2g+1; row tiles 0, 1 of each
-          const uint8_t* b0 = sb + C::offSFB + 16 * lane;
+          const uint8_t* b0 = sfb_s + 16 * lane;
           const uint4 w00 = *reinterpret_cast<const uint4*>(b0 + 512 * (2 * g));
           const uint4 w01 = *reinterpret_cast<const uint4*>(b0 + 512 * (C::kAtoms + 2 * g));
           const uint4 w10 = *reinterpret_cast<const uint4*>(b0 + 512 * (2 * g + 1));
@@ -576,8 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) arrive_leader(sfready_bar(stage));
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        if (lane == 0) arrive_leader(sfready_bar(slot));
+        if (++slot == R) { slot = 0; phase ^= 1u; }
       }
     }
     tmem_st_wait();                              // nothing of this warp is in flight at teardown

@@ -523,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* rb = ring + size_t(slot) * C::kSfSlotBytes;
             const uint32_t fb = sffull_bar(slot);
             mbar_expect_tx(fb, C::kTxS);
-            tma_load_3d(smem_u32(rb), &tmSFA, 0, kt * C::kAtoms, arow / BM, fb);
+            if (MODE == 0) tma_load_3d(smem_u32(rb), &tmSFA, 0, kt * C::kAtoms, arow / BM, fb);
             tma_load_3d(smem_u32(rb + C::kSFA), &tmSFB, 0, kt * C::kAtoms, nt * C::kRT, fb);
             issued |= 1u << slot;
             last_par = (last_par & ~(1u << slot)) | (sphase << slot);

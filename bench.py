@@ -63,6 +63,25 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, ws: int, device=None) -> float:
+    """The largest x over the ranks of the initialised process group (the
+    job's timed region ends when its slowest rank ends); x itself when ws == 1.
+    device: where the reduction tensor lives (the GPU for NCCL, None = CPU for gloo)."""
+    if ws <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, ws: int, elapsed_max: float) -> float:
+    """Whole-job throughput: every rank's units (weak scaling: the same work
+    per rank) over the slowest rank's time."""
+    return units_per_rank * ws / elapsed_max
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -612,12 +631,8 @@ def run_ours(args):
     barrier()
     clocks = sampler.stop()
     sb.get_error()
-    elapsed = t_start.elapsed_time(t_end) / 1e3
-    if ws > 1:
-        tt = torch.tensor([elapsed], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed = float(tt.item())
-    value = flops_step * args.steps * ws / elapsed / 1e12
+    elapsed = max_over_ranks(t_start.elapsed_time(t_end) / 1e3, ws, dev)
+    value = job_throughput(flops_step * args.steps, ws, elapsed) / 1e12
     n_ev = args.steps
     if not in_graph_events:
         # per-kernel durations from eager steps with CUDA events around every launch
@@ -707,12 +722,8 @@ def run_ours(args):
         e2e_step(s, last=(s == e2e_steps - 1))
     e1.record(stream)
     barrier()
-    e2e_elapsed = e0.elapsed_time(e1) / 1e3
-    if ws > 1:
-        tt = torch.tensor([e2e_elapsed], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_elapsed = float(tt.item())
-    e2e_value = flops_step * e2e_steps * ws / e2e_elapsed / 1e12
+    e2e_elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, ws, dev)
+    e2e_value = job_throughput(flops_step * e2e_steps, ws, e2e_elapsed) / 1e12
 
     # ---- roofline of the dominant kernel
     peaks, peak_kind = load_peaks()

@@ -302,7 +302,11 @@ int sixbit_layernorm_quant(const void* x, int64_t M, int64_t H, int64_t ldx, flo
  * q_codes [M, N/2], q_sf (sixbit_sf_bytes(M, N)), q_g[0], delayed scaling from
  * amax_hist -- and y is not written; otherwise it leaves as bf16 y [M, ldy]
  * (for an INT8 next layer).  amax_hist records |y|'s amax either way.
- * N % 64 == 0 (the next layer's K). */
+ * N % 64 == 0 (the next layer's K).
+ * q_codes, q_sf, q_g may all be NULL: then y is always written and the call
+ * is the plain linear layer with an exact amax side output -- after it,
+ * amax_hist[0] holds max |y| as a float (a next quantizer's amax_in, which
+ * then skips its own amax pass); N % 16 == 0 suffices. */
 int sixbit_qlinear_qout(int mode, const uint8_t* a, const uint8_t* a_sf, const float* g_a,
                         const float* row_scale, int64_t M, int64_t K,
                         const uint8_t* w_codes, const uint8_t* w_sf, const float* g_w, int64_t N,

@@ -217,6 +217,12 @@ def qlinear_w4a8(planes, row_scale, w_codes, w_sf, g_w, bias=None, residual=None
     return y
 
 
+def amax_hist_value(h: torch.Tensor) -> torch.Tensor:
+    """The float32 view of a history row's first word: the amax its producer's
+    last call recorded (an amax_in for the quantizers)."""
+    return h[0:1].view(torch.float32)
+
+
 def amax_history(n: int = 1, device=None) -> torch.Tensor:
     """Zeroed delayed-scaling histories for n quantizing producers: uint32 [n, 4]
     (16-byte rows), handed to layernorm_quant / qlinear_qout one row per layer."""
@@ -229,7 +235,10 @@ def qlinear_qout(mode: str, a, w_codes, w_sf, g_w, q_codes, q_sf, q_g, amax_hist
     """Linear layer whose epilogue quantizes its bf16 result to NVFP4 for the
     next layer by delayed scaling (y written instead when *q_pred == 0).
     mode "w4a4": a = codes [M, K/2] with a_sf, g_a; "w4a8": a = digit planes
-    [3, M, K/2] with row_scale.  Returns y (bf16 [M, N]; allocated if None)."""
+    [3, M, K/2] with row_scale.  q_codes, q_sf, q_g all None: y is written
+    and amax_hist[0] receives max |y| (float bits), an exact amax side output
+    for the next quantizer (amax_hist_value(h) views it as float32).
+    Returns y (bf16 [M, N]; allocated if None)."""
     w4a4 = mode == "w4a4"
     _need_cuda(a, w_codes)
     M, K = (a.shape[0], a.shape[1] * 2) if w4a4 else (a.shape[1], a.shape[2] * 2)

@@ -172,9 +172,12 @@ int sixbit_qlinear_qout(int mode, const uint8_t* a, const uint8_t* a_sf, const f
   int rc = check_gemm(a, w_codes, w_sf, g_w, M, K, N, bias, nullptr, 0, SIXBIT_BF16, y, ldy);
   if (rc != kOk) return rc;
   if (mode == SIXBIT_QOUT_W4A4 ? (!a_sf || !g_a) : !row_scale) return kEInval;
-  if (!q_codes || !q_sf || !q_g || !amax_hist || !(headroom > 0.f) || headroom > 3.0e38f) return kEInval;
-  if (N % 64 != 0) return kEShape;
-  if ((a_sf && !aligned16(a_sf)) || !aligned16(q_codes) || !aligned16(q_sf) || !aligned16(amax_hist)) return kEAlign;
+  const bool q_any = q_codes || q_sf || q_g;
+  if (q_any && !(q_codes && q_sf && q_g)) return kEInval;        // the NVFP4 outputs come together
+  if (!amax_hist || !(headroom > 0.f) || headroom > 3.0e38f) return kEInval;
+  if (q_any && N % 64 != 0) return kEShape;
+  if ((a_sf && !aligned16(a_sf)) || (q_any && (!aligned16(q_codes) || !aligned16(q_sf))) || !aligned16(amax_hist))
+    return kEAlign;
   int sms;
   int* err;
   if (device_setup(&sms, &err) != kOk) return kELaunch;

@@ -662,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // whole 16-element blocks.  Either way the lane tracks |bf16 y|'s max
     // over its rows < M for the history.
     const bool qo = QO && p.q_hist != nullptr;   // compiled out of the plain GEMM
-    const bool q_nv = qo && (p.q_pred == nullptr || *p.q_pred != 0);
+    const bool q_nv = qo && p.q_codes != nullptr && (p.q_pred == nullptr || *p.q_pred != 0);
     const float q_amax_t = qo ? __fmul_rn(p.q_headroom, hist_prev(p.q_hist)) : 0.f;
     const float q_g = nvfp4_global_scale(q_amax_t);
     if (q_nv && blockIdx.x == 0 && ew == 0 && lane == 0) *p.q_g = q_g;

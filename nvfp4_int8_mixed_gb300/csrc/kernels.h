@@ -84,9 +84,10 @@ struct GemmCall {
   const uint8_t* pred;
   int* err;                  // device error word
   // Quantizing epilogue (q_hist != null): the bf16 result is also encoded as
-  // NVFP4 for the next layer by delayed scaling.  When q_pred is null or
-  // *q_pred != 0 the codes [M, N/2], swizzled scales and g are written and y
-  // is not; otherwise y is written.  The history records |y|'s amax either way.
+  // NVFP4 for the next layer by delayed scaling.  When q_codes is set and
+  // q_pred is null or *q_pred != 0 the codes [M, N/2], swizzled scales and g
+  // are written and y is not; otherwise y is written.  The history records
+  // |y|'s amax either way (with q_codes null: an exact amax side output).
   uint8_t* q_codes;
   uint8_t* q_sf;
   float* q_g;

@@ -27,7 +27,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (amax_history, block_gamma, dmpq_assign, layernorm, layernorm_quant, mxcache, qlinear_qout, qlinear_w4a4,
+from . import (amax_hist_value, amax_history, block_gamma, dmpq_assign, layernorm, layernorm_quant, mxcache,
+               qlinear_qout, qlinear_w4a4,
                qlinear_w4a8, quantize_act_int8, quantize_act_nvfp4, quantize_weight_nvfp4, sf_bytes,
                tdc_decide_and_apply)
 
@@ -84,6 +85,9 @@ class DiTStack:
         # fused producers: the down layer's NVFP4 input (written by the up
         # epilogue) and one delayed-scaling history per producer (LN1, LN2, up)
         self.hist = amax_history(3 * self.nb, dev)
+        # unfused: the up-projection's exact |u| amax, a side output of its GEMM
+        # that lets the down layer's NVFP4 quantizer skip its amax pass
+        self.u_amax = amax_history(1, dev)[0]
         if self.fused:
             self.codes_u = torch.empty((M, F // 2), dtype=torch.uint8, device=dev)
             self.sf_u = torch.empty(sf_bytes(M, F), dtype=torch.uint8, device=dev)
@@ -117,15 +121,26 @@ class DiTStack:
         self.graph = None
 
     # ------------------------------------------------------------ one step
-    def _ql(self, x, wq, gate_nv, gate_i8, out, amax_in=None, row_amax_in=None, residual=None, gelu=False):
+    def _ql(self, x, wq, gate_nv, gate_i8, out, amax_in=None, row_amax_in=None, residual=None, gelu=False,
+            amax_side=None):
+        """Quantize x as the gates say and run the layer.  amax_side: a history
+        row that receives max |out| (the GEMM's exact amax side output)."""
         M, K = x.shape
         codes = self.codes[:M * K // 2].view(M, K // 2)
         sf = self.sf[:sf_bytes(M, K)]
         planes = self.planes[:3 * M * K // 2].view(3, M, K // 2)
         quantize_act_nvfp4(x, amax_in=amax_in, pred=gate_nv, out=(codes, sf, self.g))
-        qlinear_w4a4(codes, sf, self.g, *wq, residual=residual, gelu=gelu, out=out, pred=gate_nv)
+        if amax_side is None:
+            qlinear_w4a4(codes, sf, self.g, *wq, residual=residual, gelu=gelu, out=out, pred=gate_nv)
+        else:
+            qlinear_qout("w4a4", codes, *wq, None, None, None, amax_side, a_sf=sf, g_a=self.g, gelu=gelu, y=out,
+                         pred=gate_nv)
         quantize_act_int8(x, row_amax=row_amax_in, want_q=False, pred=gate_i8, out=(None, planes, self.rs))
-        qlinear_w4a8(planes, self.rs, *wq, residual=residual, gelu=gelu, out=out, pred=gate_i8)
+        if amax_side is None:
+            qlinear_w4a8(planes, self.rs, *wq, residual=residual, gelu=gelu, out=out, pred=gate_i8)
+        else:
+            qlinear_qout("w4a8", planes, *wq, None, None, None, amax_side, row_scale=self.rs, gelu=gelu, y=out,
+                         pred=gate_i8)
 
     def _ln_q(self, x, i, l, gates, c, keep_bf16):
         """Fused LayerNorm feeding layer i of block l: NVFP4 / INT8 as its gates say."""
@@ -192,9 +207,10 @@ class DiTStack:
             layernorm(self.x1, LN_EPS, out=self.h2, amax_out=self.amax, row_amax_out=self.row_amax, pred=c)
             call(l, 2, self.h2)
             self._ql(self.h2, self.wq[l]["up"], g(2, 0), g(2, 1), self.u, amax_in=self.amax,
-                     row_amax_in=self.row_amax, gelu=True)
+                     row_amax_in=self.row_amax, gelu=True, amax_side=self.u_amax)
             call(l, 3, self.u)
-            self._ql(self.u, self.wq[l]["down"], g(3, 0), g(3, 1), out, residual=self.x1)
+            self._ql(self.u, self.wq[l]["down"], g(3, 0), g(3, 1), out, residual=self.x1,
+                     amax_in=amax_hist_value(self.u_amax))
             block_gamma(h, out, delta=self.delta[l], gamma_out=self.gamma[l:l + 1], r2_out=self.r2[l:l + 1],
                         tdc_state=self.state[l], computed=c)
             h = out

@@ -123,4 +123,7 @@ def test_quantizing_producer_argument_errors(lib):
     assert qo(hist=None) == sb.EINVAL
     assert qo(head=-1.0) == sb.EINVAL
     assert qo(mode=1, a_sf=None) == sb.EINVAL         # W4A8 needs the row scales
+    # the NVFP4 outputs come together (all three, or none for the amax side output)
+    assert lib.sixbit_qlinear_qout(0, fake, fake, fake, None, 128, 256, fake, fake, fake, 128, None, 0, fake, 128,
+                                   fake, None, fake, fake, f(2.0), None, None, None) == sb.EINVAL
     assert qo(hist=P((1 << 20) + 8)) == sb.EALIGN

@@ -226,3 +226,28 @@ def test_qout_feeds_the_next_layer():
     rc, rsf, rg, _ = o_nvfp4.quantize(uf)
     ref = o_gemm.w4a4(rc, rsf, rg, rw["down"]["codes"], rw["down"]["sf"], rw["down"]["g"])
     assert_gemm_close(host(out), ref, "f32")
+
+
+@pytest.mark.parametrize("mode,M,N,K", [("w4a4", 300, 512, 256), ("w4a8", 129, 144, 320), ("w4a4", 17776, 7680, 1920)])
+def test_qlinear_amax_side_output(mode, M, N, K):
+    """No NVFP4 outputs: the plain layer (bit-identical y) plus the exact
+    max |y| in the history's first word, usable as a quantizer's amax_in."""
+    sb = _sb()
+    dev_a, dw, bias, ref_fn = _operands(M * 3 + N + K, mode, M, N, K)
+    hist = sb.amax_history(1)[0]
+    y = sb.qlinear_qout(mode, dev_a["a"], *dw, None, None, None, hist, a_sf=dev_a.get("a_sf"), g_a=dev_a.get("g_a"),
+                        row_scale=dev_a.get("row_scale"), gelu=True, bias=dev_bf16(bias))
+    if mode == "w4a4":
+        y_plain = sb.qlinear_w4a4(dev_a["a"], dev_a["a_sf"], dev_a["g_a"], *dw, bias=dev_bf16(bias), gelu=True)
+    else:
+        y_plain = sb.qlinear_w4a8(dev_a["a"], dev_a["row_scale"], *dw, bias=dev_bf16(bias), gelu=True)
+    assert torch.equal(y, y_plain)
+    yf = codecs.bf16_to_f32(host_bf16_bits(y))
+    assert _hist_words(hist) == (np.max(np.abs(yf)), 0, 0)
+    assert host(sb.amax_hist_value(hist))[0] == np.max(np.abs(yf))
+    if N % 64:
+        return                                            # NVFP4 needs K % 64 == 0 for the next layer
+    # the amax as a quantizer's input: the same codes as the quantizer's own amax pass
+    c1, s1, g1 = sb.quantize_act_nvfp4(y, amax_in=sb.amax_hist_value(hist))
+    c2, s2, g2 = sb.quantize_act_nvfp4(y)
+    assert torch.equal(c1, c2) and torch.equal(s1, s2) and torch.equal(g1, g2)

@@ -765,9 +765,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int h = 0; h < 2; ++h) {
             const uint32_t* rc = k == 0 ? (h == 0 ? r0 : r1) : (h == 0 ? r2 : r3);
             const int nc = n0 + 32 * h;
-            float v[32];
+            float v[32];                         // scale, bias (and residual) in f32x2 pairs
+            const uint64_t sc2 = f2_pack(scale, scale);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(__uint_as_float(rc[i]), scale);
+            for (int i = 0; i < 32; i += 2)
+              f2_unpack(f2_mul(f2_pack(__uint_as_float(rc[i]), __uint_as_float(rc[i + 1])), sc2), v[i], v[i + 1]);
             if (p.bias && nc < p.N) {
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
@@ -775,10 +777,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint4 b = *reinterpret_cast<const uint4*>(p.bias + nc + 8 * i);
                 const uint32_t* pb = &b.x;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  v[8 * i + 2 * e] = __fadd_rn(v[8 * i + 2 * e], bf16lo(pb[e]));
-                  v[8 * i + 2 * e + 1] = __fadd_rn(v[8 * i + 2 * e + 1], bf16hi(pb[e]));
-                }
+                for (int e = 0; e < 4; ++e)
+                  f2_unpack(f2_add(f2_pack(v[8 * i + 2 * e], v[8 * i + 2 * e + 1]), f2_from_bf16x2(pb[e])),
+                            v[8 * i + 2 * e], v[8 * i + 2 * e + 1]);
               }
             }
             if (p.gelu) {
@@ -793,10 +794,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint4 rr = *slot;
                 const uint32_t* pr = &rr.x;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  v[8 * i + 2 * e] = __fadd_rn(v[8 * i + 2 * e], bf16lo(pr[e]));
-                  v[8 * i + 2 * e + 1] = __fadd_rn(v[8 * i + 2 * e + 1], bf16hi(pr[e]));
-                }
+                for (int e = 0; e < 4; ++e)
+                  f2_unpack(f2_add(f2_pack(v[8 * i + 2 * e], v[8 * i + 2 * e + 1]), f2_from_bf16x2(pr[e])),
+                            v[8 * i + 2 * e], v[8 * i + 2 * e + 1]);
               }
               uint4 w;
               w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);

@@ -48,6 +48,9 @@ enum {
   SIXBIT_EDEVICE = -5   /* returned by sixbit_get_error(): a device wait gave up */
 };
 
+/* Calls over M rows (amax, the activation quantizers, the linear layers, the
+ * LayerNorms) return SIXBIT_OK at once when M == 0, before any check: no
+ * pointer is used, so an empty tensor's NULL data pointer is accepted. */
 enum { SIXBIT_F32 = 0, SIXBIT_BF16 = 1 };          /* dtype / out_dtype */
 enum { SIXBIT_EPI_GELU = 1 };                       /* epilogue flag bits */
 enum { SIXBIT_QOUT_W4A4 = 0, SIXBIT_QOUT_W4A8 = 1 };  /* sixbit_qlinear_qout mode */

@@ -64,6 +64,7 @@ size_t sixbit_workspace_size(int64_t M, int64_t K) {
 
 int sixbit_amax_bf16(const void* x, int64_t M, int64_t K, int64_t ldx, float* amax_out, float* row_amax_out,
                      sixbit_stream_t stream) {
+  if (M == 0) return kOk;                 // empty: nothing to do, pointers unused
   if (!x || (!amax_out && !row_amax_out) || M < 0 || K < 0 || ldx < K) return kEInval;
   if (K % 8 != 0 || ldx % 8 != 0) return kEShape;
   if (!aligned16(x)) return kEAlign;
@@ -75,6 +76,7 @@ int sixbit_amax_bf16(const void* x, int64_t M, int64_t K, int64_t ldx, float* am
 
 int sixbit_quantize_act_nvfp4(const void* x, int64_t M, int64_t K, int64_t ldx, const float* amax_in, uint8_t* codes,
                               uint8_t* sf, float* g_out, const uint8_t* pred, void* ws, sixbit_stream_t stream) {
+  if (M == 0) return kOk;                 // empty: nothing to do, pointers unused
   if (!x || !codes || !sf || !g_out || M < 0 || K <= 0 || ldx < K) return kEInval;
   if (!amax_in && !ws) return kEInval;
   if (K % 64 != 0 || ldx % 8 != 0) return kEShape;
@@ -107,12 +109,12 @@ int sixbit_quantize_weight_nvfp4(const void* w, int dtype, int64_t N, int64_t K,
 
 int sixbit_quantize_act_int8(const void* x, int64_t M, int64_t K, int64_t ldx, const float* row_amax_in, int8_t* q,
                              uint8_t* planes, float* row_scale, const uint8_t* pred, sixbit_stream_t stream) {
+  if (M == 0) return kOk;                 // empty: nothing to do, pointers unused
   if (!x || !row_scale || (!q && !planes) || M < 0 || K <= 0 || ldx < K) return kEInval;
   if (K % 64 != 0 || K > 16384 || ldx % 8 != 0) return kEShape;
   if (!aligned16(x) || (q && !aligned16(q)) || (planes && !aligned16(planes))) return kEAlign;
   int sms;
   if (device_setup(&sms, nullptr) != kOk) return kELaunch;
-  if (M == 0) return kOk;
   return launch_int8_quant(x, M, K, ldx, row_amax_in, q, planes, row_scale, pred, sms, cs(stream));
 }
 
@@ -134,6 +136,7 @@ int sixbit_qlinear_w4a4(const uint8_t* a_codes, const uint8_t* a_sf, const float
                         const uint8_t* w_codes, const uint8_t* w_sf, const float* g_w, int64_t N, const void* bias,
                         const void* residual, int64_t ldr, int epi, int out_dtype, void* y, int64_t ldy,
                         const uint8_t* pred, sixbit_stream_t stream) {
+  if (M == 0) return kOk;                 // empty: nothing to do, pointers unused
   int rc = check_gemm(a_codes, w_codes, w_sf, g_w, M, K, N, bias, residual, ldr, out_dtype, y, ldy);
   if (rc != kOk) return rc;
   if (!a_sf || !g_a) return kEInval;
@@ -141,7 +144,6 @@ int sixbit_qlinear_w4a4(const uint8_t* a_codes, const uint8_t* a_sf, const float
   int sms;
   int* err;
   if (device_setup(&sms, &err) != kOk) return kELaunch;
-  if (M == 0) return kOk;
   GemmCall c{0, a_codes, a_sf, g_a, nullptr, w_codes, w_sf, g_w, M, N, K, bias, residual, ldr,
              (epi & SIXBIT_EPI_GELU) ? 1 : 0, out_dtype == SIXBIT_BF16 ? 1 : 0, y, ldy, pred, err};
   return launch_gemm_fp4(c, sms, cs(stream));
@@ -151,13 +153,13 @@ int sixbit_qlinear_w4a8(const uint8_t* a_planes, const float* row_scale, int64_t
                         const uint8_t* w_sf, const float* g_w, int64_t N, const void* bias, const void* residual,
                         int64_t ldr, int epi, int out_dtype, void* y, int64_t ldy, const uint8_t* pred,
                         sixbit_stream_t stream) {
+  if (M == 0) return kOk;                 // empty: nothing to do, pointers unused
   int rc = check_gemm(a_planes, w_codes, w_sf, g_w, M, K, N, bias, residual, ldr, out_dtype, y, ldy);
   if (rc != kOk) return rc;
   if (!row_scale) return kEInval;
   int sms;
   int* err;
   if (device_setup(&sms, &err) != kOk) return kELaunch;
-  if (M == 0) return kOk;
   GemmCall c{1, a_planes, nullptr, nullptr, row_scale, w_codes, w_sf, g_w, M, N, K, bias, residual, ldr,
              (epi & SIXBIT_EPI_GELU) ? 1 : 0, out_dtype == SIXBIT_BF16 ? 1 : 0, y, ldy, pred, err};
   return launch_gemm_fp4(c, sms, cs(stream));
@@ -168,6 +170,7 @@ int sixbit_qlinear_qout(int mode, const uint8_t* a, const uint8_t* a_sf, const f
                         const void* bias, int epi, void* y, int64_t ldy, uint8_t* q_codes, uint8_t* q_sf, float* q_g,
                         uint32_t* amax_hist, float headroom, const uint8_t* q_pred, const uint8_t* pred,
                         sixbit_stream_t stream) {
+  if (M == 0) return kOk;                 // empty: nothing to do, pointers unused
   if (mode != SIXBIT_QOUT_W4A4 && mode != SIXBIT_QOUT_W4A8) return kEInval;
   int rc = check_gemm(a, w_codes, w_sf, g_w, M, K, N, bias, nullptr, 0, SIXBIT_BF16, y, ldy);
   if (rc != kOk) return rc;
@@ -181,7 +184,6 @@ int sixbit_qlinear_qout(int mode, const uint8_t* a, const uint8_t* a_sf, const f
   int sms;
   int* err;
   if (device_setup(&sms, &err) != kOk) return kELaunch;
-  if (M == 0) return kOk;
   GemmCall c{mode == SIXBIT_QOUT_W4A4 ? 0 : 1, a, mode == SIXBIT_QOUT_W4A4 ? a_sf : nullptr,
              mode == SIXBIT_QOUT_W4A4 ? g_a : nullptr, mode == SIXBIT_QOUT_W4A4 ? nullptr : row_scale, w_codes, w_sf,
              g_w, M, N, K, bias, nullptr, 0, (epi & SIXBIT_EPI_GELU) ? 1 : 0, 1, y, ldy, pred, err,
@@ -275,12 +277,12 @@ int sixbit_tdc_decide_and_apply_mxcache(const void* in, const void* cache, int64
 
 int sixbit_layernorm_bf16(const void* x, int64_t M, int64_t H, int64_t ldx, float eps, void* y, int64_t ldy,
                           float* amax_out, float* row_amax_out, const uint8_t* pred, sixbit_stream_t stream) {
+  if (M == 0) return kOk;                 // empty: nothing to do, pointers unused
   if (!x || !y || M < 0 || H <= 0 || ldx < H || ldy < H) return kEInval;
   if (H % 8 != 0 || ldx % 8 != 0 || ldy % 8 != 0) return kEShape;
   if (!aligned16(x) || !aligned16(y)) return kEAlign;
   int sms;
   if (device_setup(&sms, nullptr) != kOk) return kELaunch;
-  if (M == 0) return kOk;
   return launch_layernorm(x, M, H, ldx, eps, y, ldy, amax_out, row_amax_out, pred, sms, cs(stream));
 }
 
@@ -288,6 +290,7 @@ int sixbit_layernorm_quant(const void* x, int64_t M, int64_t H, int64_t ldx, flo
                            uint8_t* codes, uint8_t* sf, float* g_out, uint32_t* amax_hist, float headroom,
                            const uint8_t* nv_pred, uint8_t* planes, float* row_scale, const uint8_t* i8_pred,
                            const uint8_t* pred, sixbit_stream_t stream) {
+  if (M == 0) return kOk;                 // empty: nothing to do, pointers unused
   if (!x || M < 0 || H <= 0 || ldx < H || (y && ldy < H)) return kEInval;
   if (!y && !codes && !planes) return kEInval;
   if (codes && (!sf || !g_out || !amax_hist)) return kEInval;
@@ -301,7 +304,6 @@ int sixbit_layernorm_quant(const void* x, int64_t M, int64_t H, int64_t ldx, flo
     return kEAlign;
   int sms;
   if (device_setup(&sms, nullptr) != kOk) return kELaunch;
-  if (M == 0) return kOk;
   LnQuantCall c = {};
   c.x = static_cast<const uint16_t*>(x); c.M = M; c.H = H; c.ldx = ldx; c.eps = eps;
   c.y = static_cast<uint16_t*>(y); c.ldy = ldy;

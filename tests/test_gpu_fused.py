@@ -251,3 +251,31 @@ def test_qlinear_amax_side_output(mode, M, N, K):
     c1, s1, g1 = sb.quantize_act_nvfp4(y, amax_in=sb.amax_hist_value(hist))
     c2, s2, g2 = sb.quantize_act_nvfp4(y)
     assert torch.equal(c1, c2) and torch.equal(s1, s2) and torch.equal(g1, g2)
+
+
+def test_empty_and_zero_inputs():
+    """M = 0: nothing launches and the history is left alone.  An all-zero
+    input has a LayerNorm output of zeros: zero codes and scales, a zero
+    amax recorded, and an INT8 row scale of 0."""
+    sb = _sb()
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    hist = sb.amax_history(1)[0]
+    _set_hist(hist, 2.5)
+    # zero-row views of real buffers (an empty allocation may have a null pointer, which the ABI rejects)
+    x0 = torch.zeros((4, 256), dtype=torch.bfloat16, device="cuda")[:0]
+    c0, s0 = torch.zeros((4, 128), **u8), torch.zeros(sb.sf_bytes(4, 256), **u8)
+    sb.layernorm_quant(x0, nvfp4=(c0[:0], s0, torch.empty(1, device="cuda")), amax_hist=hist)
+    w = synthetic.weights(synthetic.rng(1), 128, 256)
+    wq = sb.quantize_weight_nvfp4(torch.from_numpy(w).cuda())
+    y0 = torch.zeros((4, 128), dtype=torch.bfloat16, device="cuda")[:0]
+    sb.qlinear_qout("w4a4", c0[:0], *wq, None, None, None, hist, a_sf=s0, g_a=torch.ones(1, device="cuda"), y=y0)
+    assert _hist_words(hist) == (np.float32(2.5), 0, 0)
+    M, H = 130, 256
+    z = torch.zeros((M, H), dtype=torch.bfloat16, device="cuda")
+    codes = torch.full((M, H // 2), 0xAB, **u8)
+    sf = torch.full((sb.sf_bytes(M, H),), 0xCD, **u8)
+    planes = torch.full((3, M, H // 2), 0xEF, **u8)
+    rs = torch.full((M,), 7.0, device="cuda")
+    sb.layernorm_quant(z, nvfp4=(codes, sf, torch.empty(1, device="cuda")), amax_hist=hist, int8=(planes, rs))
+    assert not host(codes).any() and not host(sf).any() and not host(planes).any() and not host(rs).any()
+    assert _hist_words(hist) == (np.float32(0.0), 0, 0)

@@ -1,5 +1,8 @@
 // Block-level kernels: Gamma/Delta/r2 pass (a7), DMPQ assignment (a8),
-// TDC decision and reuse (a9), and the LayerNorm of the block harness.
+// TDC decision and reuse (a9), and the LayerNorm of the block harness; the
+// compressed-update-cache versions of a7 / a9, the LayerNorm that quantizes
+// its own output (NVFP4 by delayed scaling, INT8 exact), and the pair
+// statistics of the DMPQ calibration side (E_rel, update similarity).
 //
 // Method: 6Bit-Diffusion, thelatestinai.com page -- Figure 2 (Gamma = block
 // relative L1 input/output distance at the preceding step drives DMPQ; TDC

@@ -14,19 +14,27 @@
 //
 // Structure: persistent, warp-specialized CTA of 16 warps over 128 x 256
 // output tiles, K in steps of KB bytes of codes per row (2*KB elements):
-//   warp 0      TMA producer: A/B code tiles (KB-byte swizzle) and the
-//               scale-factor atoms into a STAGES-deep shared-memory ring;
+//   warps 0, 2  TMA producers (one lane each): the A code tile (or its three
+//               digit planes) and the W code tile, KB-byte swizzle, into a
+//               STAGES-deep shared-memory ring;
+//   warp 3      TMA producer of the E4M3 scale atoms: with the code stages
+//               (W4A8, CTA pairs) or, for W4A4 on one CTA, into a ring of
+//               their own that runs ahead of the code stages;
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::mxf4nvf4
 //               scale_vec::4X (128 x 256 x 64 per instruction) into the TMEM
 //               accumulator, tcgen05.commit to free stages and publish tiles;
-//   warps 4..7  scale warps, one per TMEM lane quarter: move each stage's
-//               E4M3 scale atoms from shared memory into that stage's TMEM
-//               scale columns with tcgen05.st, in the layout a replicating
-//               tcgen05.cp (.32x128b.warpx4) produces;
+//   warps 4..7  scale warps, one per TMEM lane quarter: move each k-step's
+//               scale atoms from shared memory into TMEM scale columns with
+//               tcgen05.st, in the layout a replicating tcgen05.cp
+//               (.32x128b.warpx4) produces;
 //   warps 8..15 epilogue: two warps per TMEM lane quarter, 128 columns each.
 //               They pull the whole accumulator into registers, release TMEM
 //               at once (the next tile's MMAs start), then scale, add bias,
-//               GELU, add residual and store from registers.
+//               GELU (one special-function op an element), add the residual
+//               (a TMA-loaded tile) and write bf16 through 128-byte-swizzled
+//               shared memory with TMA stores.  The QO instantiation can
+//               instead encode the result as NVFP4 for the next layer
+//               (delayed scaling) and report its exact amax.
 // Only MMAs go through the tensor pipe's issue queue: on GB300 one thread
 // issues about one tcgen05.mma/tcgen05.cp per 25 ns, so moving the three
 // scale copies of each 128 x 256 x 64 MMA (66 ns of tensor work) to
@@ -48,7 +56,6 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int kThreads = 512;            // 4 warpgroups: control, scales, 2 x epilogue
-constexpr int kEpiThreads = 256;
 constexpr int kLaunchRegs = 128;         // 65536 / kThreads
 constexpr int kLowRegs = 72, kHighRegs = 184;
 static_assert(2 * 128 * kLowRegs + 2 * 128 * kHighRegs == kThreads * kLaunchRegs, "register split");
@@ -645,7 +652,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;                      // TMEM lane quarter this warp may access
     const int ew = warp - 8;                     // epilogue warp 0..7
     const int half = ew >> 2;                    // columns [128*half, 128*half + 128)
-    const int row = q * 32 + lane;
     // bf16 output leaves through this warp's staging block: 32 rows x 64
     // columns (128 bytes a row, 16-byte chunk j of row r at j ^ (r % 8), the
     // TMA 128-byte swizzle), written by one TMA store per 64 columns.

@@ -483,23 +483,30 @@ __global__ void __launch_bounds__(kThreads) tdc_mx_kernel(const uint16_t* __rest
 //                  own amax (the exact per-token quantizer).
 // hist (nullable) records this call's tensor amax for the next call.
 // H % 16 == 0.
+// Threads per CTA: rows of more than 4 blocks a lane need ~170 registers a
+// thread, so 4-warp CTAs (3 resident per SM) keep more warps in flight than
+// 8-warp ones (1 resident).
 template <int NB>
-__global__ void __launch_bounds__(kThreads) ln_quant_kernel(const LnQuantCall a) {
+constexpr int kLnThreads = NB >= 6 ? 128 : 256;
+
+template <int NB>
+__global__ void __launch_bounds__(kLnThreads<NB>) ln_quant_kernel(const LnQuantCall a) {
+  constexpr int LT = kLnThreads<NB>;
   if (a.pred && *a.pred == 0) return;
   __shared__ uint32_t lut[256];
-  __shared__ float red[kThreads / 32];
+  __shared__ float red[LT / 32];
   const bool nv = a.codes != nullptr && (a.nv_pred == nullptr || *a.nv_pred != 0);
   const bool i8 = a.planes != nullptr && (a.i8_pred == nullptr || *a.i8_pred != 0);
   if (i8) {
-    for (int i = threadIdx.x; i < 256; i += kThreads) lut[i] = digit_entry(int(int8_t(uint8_t(i))));
+    for (int i = threadIdx.x; i < 256; i += LT) lut[i] = digit_entry(int(int8_t(uint8_t(i))));
     __syncthreads();
   }
   const float amax_t = a.hist ? __fmul_rn(a.headroom, hist_prev(a.hist)) : 0.f;
   const float g = nvfp4_global_scale(amax_t);
   if (nv && blockIdx.x == 0 && threadIdx.x == 0) *a.g_out = g;
   const int lane = threadIdx.x & 31;
-  const int64_t warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-  const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
+  const int64_t warp = (int64_t(blockIdx.x) * LT + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * LT) >> 5;
   const int64_t M = a.M, H = a.H, nblk = H / 16, kc4 = H / 16;
   const int64_t Mpad = nv ? cdiv(M, 128) * 128 : M;
   const int64_t plane_stride = M * (H / 2);
@@ -626,7 +633,7 @@ __global__ void __launch_bounds__(kThreads) ln_quant_kernel(const LnQuantCall a)
     __syncthreads();
     if (threadIdx.x == 0) {
       float cmax = 0.f;
-      for (int w = 0; w < kThreads / 32; ++w) cmax = fmaxf(cmax, red[w]);
+      for (int w = 0; w < LT / 32; ++w) cmax = fmaxf(cmax, red[w]);
       if (a.amax_out) atomic_max_nonneg(a.amax_out, cmax);
       if (a.hist) hist_arrive(a.hist, cmax);
     }
@@ -774,11 +781,12 @@ template <int NB>
 void launch_lnq(const LnQuantCall& c, int64_t rows, int num_sms, cudaStream_t s) {
   static int per_sm = 0;
   if (per_sm == 0 &&
-      (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ln_quant_kernel<NB>, kThreads, 0) != cudaSuccess ||
+      (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ln_quant_kernel<NB>, kLnThreads<NB>, 0) !=
+           cudaSuccess ||
        per_sm < 1))
     per_sm = 1;
-  const int64_t want = cdiv(rows, kThreads / 32), cap = int64_t(num_sms) * per_sm;
-  ln_quant_kernel<NB><<<unsigned(want < cap ? (want < 1 ? 1 : want) : cap), kThreads, 0, s>>>(c);
+  const int64_t want = cdiv(rows, kLnThreads<NB> / 32), cap = int64_t(num_sms) * per_sm;
+  ln_quant_kernel<NB><<<unsigned(want < cap ? (want < 1 ? 1 : want) : cap), kLnThreads<NB>, 0, s>>>(c);
 }
 
 int launch_ln_quant(const LnQuantCall& c, int num_sms, cudaStream_t s) {

@@ -351,6 +351,8 @@ int launch_int8_quant(const void* x, int64_t M, int64_t K, int64_t ldx, const fl
       int8_quant_kernel<8, 2, C><<<grid_for(M, 2, num_sms, 16), 128, 0, s>>>(xs, M, K, ldx, row_amax_in, q, planes, row_scale, pred);
     else if (K <= 8192)
       int8_quant_kernel<8, 4, C><<<grid_for(M, 1, num_sms, 16), 128, 0, s>>>(xs, M, K, ldx, row_amax_in, q, planes, row_scale, pred);
+    else if (K <= 12288)   // 12 vectors a lane: fewer registers than 16, more CTAs resident
+      int8_quant_kernel<12, 4, C><<<grid_for(M, 1, num_sms, 16), 128, 0, s>>>(xs, M, K, ldx, row_amax_in, q, planes, row_scale, pred);
     else
       int8_quant_kernel<16, 4, C><<<grid_for(M, 1, num_sms, 12), 128, 0, s>>>(xs, M, K, ldx, row_amax_in, q, planes, row_scale, pred);
   };

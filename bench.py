@@ -749,7 +749,8 @@ def run_ours(args):
     # W4A8 runs three FP4 digit MMAs per product: its ceiling is a third of the FP4 peak
     dom_peak = fp4_peak / 3.0 if dom.startswith("w4a8") else fp4_peak
     achieved = dom_flops / mean_t[dom] / 1e12
-    traffic = dram_traffic(dom)
+    # the committed counters were captured on the 2B-class layer shapes only
+    traffic = dram_traffic(dom) if args.workload == "2b" else None
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": dom_peak, "unit": "TFLOP/s",
                 "frac": achieved / dom_peak, "traffic": traffic,
                 "peak_note": f"{peak_kind} bf16 burst {peaks['bf16_tflops']} TFLOP/s x nominal FP4/BF16 ratio 6"

@@ -17,7 +17,8 @@ def _sb():
     return sb
 
 
-SHAPES = [(256, 256), (1, 64), (200, 320), (129, 1920), (50, 2560), (300, 7680), (33, 10240), (5, 16384)]
+SHAPES = [(256, 256), (1, 64), (200, 320), (129, 1920), (50, 2560), (17, 3584), (9, 5120), (300, 7680),
+          (33, 10240), (5, 16384)]
 
 
 @pytest.mark.parametrize("M,K", SHAPES)

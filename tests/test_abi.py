@@ -37,6 +37,43 @@ def test_binding_covers_header():
     assert set(declared()) == set(sb._SIGS)
 
 
+def _prototypes():
+    """{name: [argument type text, ...]} of every declaration in the header."""
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    out = {}
+    for name, args in re.findall(r"\b(sixbit_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", src):
+        args = " ".join(args.split())
+        out[name] = [] if args in ("", "void") else [a.strip() for a in args.split(",")]
+    return out
+
+
+def _kind(decl):
+    """ctypes type an argument declaration must be marshalled as."""
+    if "*" in decl or decl.startswith("sixbit_stream_t"):
+        return ctypes.c_void_p
+    for ctype, kind in (("int64_t", ctypes.c_int64), ("int32_t", ctypes.c_int32), ("float", ctypes.c_float),
+                        ("int", ctypes.c_int)):
+        if re.match(rf"(const\s+)?{ctype}\b", decl):
+            return kind
+    raise AssertionError(f"unclassified argument: {decl}")
+
+
+def test_binding_signatures_match_header():
+    """Every ctypes signature has the header's argument count and kinds, in
+    order (a drifted signature would only misbehave on a GPU)."""
+    import nvfp4_int8_mixed_gb300 as sb
+    protos = _prototypes()
+    assert set(protos) == set(sb._SIGS)
+    for name, decls in protos.items():
+        want = [_kind(d) for d in decls]
+        got = sb._SIGS[name][0]
+        assert len(got) == len(want), (name, len(got), len(want))
+        for i, (g, w) in enumerate(zip(got, want)):
+            assert g is w, (name, i, decls[i], g, w)
+
+
 def test_host_helpers(lib):
     assert lib.sixbit_version().startswith(b"sixbit")
     assert lib.sixbit_sf_bytes(256, 256) == 256 * 16

@@ -82,6 +82,30 @@ def job_throughput(units_per_rank: float, ws: int, elapsed_max: float) -> float:
     return units_per_rank * ws / elapsed_max
 
 
+def gemm_roofline(mode: str, M: int, N: int, K: int, residual: bool, seconds: float,
+                  fp4_peak_tflops: float, hbm_gbs: float) -> dict:
+    """Roofline of one quantized-linear launch: min(tensor ceiling, HBM x AI).
+
+    Algorithmic bytes: the activation operand (W4A4: E2M1 codes + E4M3 block
+    scales; W4A8: three digit planes + fp32 row scales), the NVFP4 weight
+    (codes + scales), the bf16 output and, with a residual, its bf16 read.
+    W4A8 issues three FP4 MMAs per product, so its tensor ceiling is a third
+    of the FP4 peak."""
+    flops = 2.0 * M * N * K
+    a_bytes = 3 * M * K / 2 + 4 * M if mode == "w4a8" else M * K / 2 + M * K / 16
+    w_bytes = N * K / 2 + N * K / 16
+    y_bytes = 2.0 * M * N * (2 if residual else 1)
+    nbytes = a_bytes + w_bytes + y_bytes
+    ai = flops / nbytes
+    tensor = fp4_peak_tflops / (3.0 if mode == "w4a8" else 1.0)
+    hbm = hbm_gbs * ai / 1e3                    # GB/s x FLOP/B -> TFLOP/s
+    ceiling = min(tensor, hbm)
+    achieved = flops / seconds / 1e12
+    return {"ms": seconds * 1e3, "TFLOP/s": achieved, "bytes": nbytes, "AI": ai,
+            "bound": "tensor" if tensor <= hbm else "hbm", "ceiling": ceiling,
+            "frac_ceiling": achieved / ceiling, "frac_tensor": achieved / tensor}
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -765,8 +789,10 @@ def run_ours(args):
     byte_rows["gamma_delta"] = 8.0 * M * H
     bw = {n: {"ms": mean_t[n] * 1e3, "GB/s": byte_rows[n] / mean_t[n] / 1e9,
               "frac_hbm": byte_rows[n] / mean_t[n] / 1e9 / hbm} for n in byte_rows}
-    tf = {n: {"ms": mean_t[n] * 1e3, "TFLOP/s": flops_layer[[l["name"] for l in L].index(n.split("[")[1][:-1])]
-                    / mean_t[n] / 1e12} for n in gemm_names}
+    tf = {}
+    for n in gemm_names:
+        l = L[[x["name"] for x in L].index(n.split("[")[1][:-1])]
+        tf[n] = gemm_roofline(n.split("[")[0], M, l["N"], l["K"], l["r"] is not None, mean_t[n], fp4_peak, hbm)
 
     producers = time_producers(sb, L, dev, (bin_, bout)) if rank == 0 and args.workload == "2b" else None
 

@@ -681,7 +681,7 @@ def run_ours(args):
     for i in range(n_ev):
         for k, n in enumerate(names):
             per_kernel[n].append(evs[i][k][0].elapsed_time(evs[i][k][1]) / 1e3)
-    mean_t = {n: float(np.mean(v)) for n, v in per_kernel.items()}
+    mean_t = {n: float(np.median(v)) for n, v in per_kernel.items()}   # per launch: median over the K steps
 
     # ---- end to end through the public API: pinned host inputs copied in every step
     pinned = []

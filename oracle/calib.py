@@ -17,13 +17,19 @@ difference.  No formula is printed.  Readings:
   * similarity of updates: cosine <a, b> / (||a|| ||b||) and relative L2
     ||a - b|| / ||b||, a the newer update.
 
-All sums in float64.  Parity: pinned by closed forms (exact lines are
-recovered, a hand-computed three-point fit, orthogonal / parallel / opposite
-vectors, identity and scaling properties of the relative error).
+Sums in float64 (`pair_sums`).  `pair_sums_tree` gives the same four sums
+with each term rounded once in float32 (d = a - b, then d*d; b*b; a*b; a*a)
+and summed by the fixed tree of oracle.gamma: the reduction the device's
+pair statistics are defined by.  Parity: pinned by closed forms (exact lines
+are recovered, a hand-computed three-point fit, orthogonal / parallel /
+opposite vectors, identity and scaling properties of the relative error;
+the tree sums within float32 rounding of the float64 ones).
 """
 from __future__ import annotations
 
 import numpy as np
+
+from .gamma import tree_sum
 
 
 def pair_sums(a, b):
@@ -32,6 +38,15 @@ def pair_sums(a, b):
     b = np.asarray(b, dtype=np.float64).ravel()
     d = a - b
     return np.array([d @ d, b @ b, a @ b, a @ a])
+
+
+def pair_sums_tree(a, b):
+    """[sum (a-b)^2, sum b^2, sum a*b, sum a^2]: float32 terms, fixed tree."""
+    a = np.asarray(a, dtype=np.float32).ravel()
+    b = np.asarray(b, dtype=np.float32).ravel()
+    d = (a - b).astype(np.float32)
+    terms = ((d * d), (b * b), (a * b), (a * a))
+    return np.array([tree_sum(t.astype(np.float32)) for t in terms])
 
 
 def rel_l2(a, b) -> float:

@@ -22,6 +22,81 @@ def test_gamma_closed_forms():
     assert gamma.gamma(z, c[:3, :3]) == 0.0                # ||in|| = 0 -> 0 by definition
 
 
+def _scalar_tree(terms):
+    """The reduction tree of oracle.gamma walked one element at a time (float32
+    lanes, float64 across tiles), written independently of the vectorised
+    version it checks."""
+    terms = [np.float32(v) for v in terms]
+    n = len(terms)
+    tile_sums = []
+    for base in range(0, max(n, 1), 8192):
+        lanes = []
+        for t in range(256):
+            acc = np.float32(0.0)
+            for j in range(4):
+                for e in range(8):
+                    i = base + j * 2048 + 8 * t + e
+                    if i < n:
+                        acc = np.float32(acc + terms[i])
+            lanes.append(acc)
+        for h in (16, 8, 4, 2, 1):
+            lanes = [np.float32(lanes[k] + lanes[k ^ h]) for k in range(256)]
+        groups = [lanes[32 * w] for w in range(8)]
+        for h in (4, 2, 1):
+            for w in range(h):
+                groups[w] = np.float32(groups[w] + groups[w + h])
+        tile_sums.append(float(groups[0]))
+    acc = [0.0] * 256
+    for k, v in enumerate(tile_sums):
+        acc[k % 256] = acc[k % 256] + v
+    h = 128
+    while h >= 1:
+        for k in range(h):
+            acc[k] = acc[k] + acc[k + h]
+        h //= 2
+    return acc[0]
+
+
+def test_tree_sum_matches_a_scalar_walk_of_the_tree():
+    rng = np.random.default_rng(7)
+    # magnitudes over 12 binades, so the float32 result depends on the order
+    n = 2 * 8192 + 1003
+    v = (rng.standard_normal(n) ** 2 * np.exp2(rng.integers(-6, 6, n))).astype(np.float32)
+    got = gamma.tree_sum(v)
+    assert got == _scalar_tree(v)
+    # a different order (one float32 running sum, or float64 throughout) gives other bits
+    seq = np.float32(0.0)
+    for x in v:
+        seq = np.float32(seq + x)
+    assert float(seq) != got and float(np.sum(v.astype(np.float64))) != got
+    assert gamma.tree_sum(v[:5]) == _scalar_tree(v[:5])
+
+
+def test_tree_sum_closed_forms_and_bound():
+    assert gamma.tree_sum(np.ones(8192, np.float32)) == 8192.0
+    assert gamma.tree_sum(np.ones(3 * 8192 + 5, np.float32)) == 3 * 8192 + 5
+    assert gamma.tree_sum(np.zeros(10, np.float32)) == 0.0
+    # 300 tiles: more tiles than float64 lanes, so lanes add several tiles
+    assert gamma.tree_sum(np.full(300 * 8192, 0.5, np.float32)) == 300 * 4096
+    rng = np.random.default_rng(8)
+    v = np.abs(rng.standard_normal(1_000_003)).astype(np.float32)
+    exact = float(np.sum(v.astype(np.float64)))
+    # nonnegative terms: 31 sequential float32 adds per lane, 8 tree levels
+    assert abs(gamma.tree_sum(v) - exact) <= 40 * 2.0 ** -24 * exact
+
+
+def test_gamma_and_r2_within_rounding_of_the_exact_values():
+    rng = np.random.default_rng(9)
+    xin = _bits(rng.standard_normal((37, 1000)))
+    xout = _bits(codecs.bf16_to_f32(xin) + 0.05 * rng.standard_normal((37, 1000)))
+    g, ge = gamma.gamma(xin, xout), gamma.gamma_exact(xin, xout)
+    assert g != 0 and abs(g - ge) <= 1e-5 * ge
+    dn = gamma.delta(xin, xout)
+    dp = _bits(codecs.bf16_to_f32(dn) * (1 + 0.1 * rng.standard_normal((37, 1000))))
+    r, re = gamma.rel_l2_sq(dn, dp), gamma.rel_l2_sq_exact(dn, dp)
+    assert r != 0 and abs(r - re) <= 1e-5 * re
+
+
 def test_delta_and_r2_closed_forms():
     rng = np.random.default_rng(1)
     xin = _bits(rng.standard_normal((5, 16)))

@@ -22,59 +22,81 @@ constexpr int kThreads = 256;
 constexpr int kTile = 8192;                   // elements per tile of the Gamma pass
 constexpr int kVecPerThread = kTile / (8 * kThreads);   // 4 x 16-byte vectors per operand
 constexpr int kGammaCtasPerSm = 3;
-constexpr int kGammaMaxCtas = 1024;           // bounds the partials (and so the scratch)
 
 struct GammaWs {                              // layout of the scratch buffer
   unsigned int counter;                       // CTAs finished (reset by the last one)
   unsigned int pad[3];
 };
 
-// Fixed-order block reduction of 4 floats: warp xor tree, then warps 0..7 in order.
-__device__ __forceinline__ void block_sum4(float v[4], float (*sm)[4]) {
+// The fixed reduction tree of the Gamma pass (and of the pair statistics).
+// Its result depends only on the input, never on the grid:
+//   * lane t of a tile (t = 0..255) owns elements j*2048 + 8t + e (j = 0..3,
+//     e = 0..7) and adds their terms one at a time in increasing element
+//     order, in float32 (round to nearest, no contraction);
+//   * the 256 lane sums: a butterfly inside each warp (partners t^16, t^8,
+//     t^4, t^2, t^1), then the 8 warp sums by w + (w+4), + (w+2), + (w+1);
+//   * tile sums go to scratch as float32; the last CTA widens them to
+//     float64, thread k adds tiles k, k+256, ... in order, and the 256
+//     thread sums are halved (k + (k+128), ..., + (k+1)).
+// All partials of one tile: 4 floats.
+
+// Per-tile combine of 4 lane sums, batched: each warp's butterfly result
+// goes to shared memory slot `it % kBatch` (it = the CTA's tile counter);
+// after every kBatch tiles (and after the last) one CTA barrier, threads
+// 0..4*kBatch-1 each combine one (tile, sum) over the 8 warps and store it,
+// and a second barrier frees the slots.  Two barriers per kBatch tiles
+// instead of one per tile.
+constexpr int kBatch = 32;
+struct TileRed {
+  float w[kBatch][kThreads / 32][4];
+};
+__device__ __forceinline__ void tile_combine4(float v[4], TileRed& red, int it, int64_t t, bool flush,
+                                              float* tile_part, int64_t tile_stride) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) v[i] = warp_sum(v[i]);
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int h = 16; h > 0; h >>= 1) v[i] = __fadd_rn(v[i], __shfl_xor_sync(0xffffffffu, v[i], h));
+  const int slot = it % kBatch;
   if (lane == 0)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) sm[w][i] = v[i];
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < 4; ++i) {
-      float acc = 0.f;
-      for (int k = 0; k < kThreads / 32; ++k) acc += sm[k][i];
-      v[i] = acc;
+    for (int i = 0; i < 4; ++i) red.w[slot][w][i] = v[i];
+  if (slot == kBatch - 1 || flush) {
+    __syncthreads();
+    if (threadIdx.x < 4 * (slot + 1)) {
+      const int b = threadIdx.x >> 2, i = threadIdx.x & 3;
+      float g[kThreads / 32];
+#pragma unroll
+      for (int k = 0; k < kThreads / 32; ++k) g[k] = red.w[b][k][i];
+#pragma unroll
+      for (int h = kThreads / 64; h > 0; h >>= 1)
+#pragma unroll
+        for (int k = 0; k < h; ++k) g[k] = __fadd_rn(g[k], g[k + h]);
+      // slot b held tile t - (slot - b) * tile_stride
+      tile_part[4 * (t - int64_t(slot - b) * tile_stride) + i] = g[0];
     }
+    __syncthreads();
   }
 }
 
-// End of a Gamma pass: CTA partials to scratch as float64; the last CTA to
-// finish sums them in CTA order, writes Gamma / r2, advances the TDC
-// counters and resets the scratch counter.
-__device__ __forceinline__ void gamma_finish(float s1, float s0, float sd, float so, bool do_r2, bool computed,
-                                             float* gamma_out, float* r2_out, int32_t* tdc_state, GammaWs* ws,
-                                             double* partials) {
-  __shared__ float sm[kThreads / 32][4];
+// End of a pass over tile partials: the last CTA to finish reduces them in
+// float64 by the fixed tree and returns true in thread 0 with the 4 sums.
+__device__ __forceinline__ bool tiles_finish(int64_t ntiles, GammaWs* ws, const float* tile_part, double out[4]) {
   __shared__ bool is_last;
-  float v[4] = {s1, s0, sd, so};
-  block_sum4(v, sm);
-  if (threadIdx.x == 0) {
-    double* p = partials + 4 * int64_t(blockIdx.x);
-    p[0] = v[0]; p[1] = v[1]; p[2] = v[2]; p[3] = v[3];
-    __threadfence();
-    const unsigned int ticket = atomicAdd(&ws->counter, 1u);
-    is_last = (ticket == gridDim.x - 1);
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  // Last CTA: float64 sum of the partials, thread t over tiles t, t+256, ...
-  // then a fixed tree.
   __shared__ double dsm[kThreads][4];
-  double acc[4] = {0, 0, 0, 0};
-  for (int64_t t = threadIdx.x; t < gridDim.x; t += kThreads) {
-    const volatile double* p = partials + 4 * t;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] += p[i];
+  if (threadIdx.x < 4) __threadfence();       // this CTA's tile partials, before the ticket
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(&ws->counter, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!is_last) return false;
+  __threadfence();
+  double acc[4] = {0.0, 0.0, 0.0, 0.0};
+  for (int64_t t = threadIdx.x; t < ntiles; t += kThreads) {
+    const float4 p = __ldcg(reinterpret_cast<const float4*>(tile_part) + t);
+    acc[0] += double(p.x);
+    acc[1] += double(p.y);
+    acc[2] += double(p.z);
+    acc[3] += double(p.w);
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) dsm[threadIdx.x][i] = acc[i];
@@ -82,41 +104,51 @@ __device__ __forceinline__ void gamma_finish(float s1, float s0, float sd, float
   for (int h = kThreads / 2; h > 0; h >>= 1) {
     if (threadIdx.x < h)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) dsm[threadIdx.x][i] += dsm[threadIdx.x + h][i];
+      for (int i = 0; i < 4; ++i) dsm[threadIdx.x][i] = __dadd_rn(dsm[threadIdx.x][i], dsm[threadIdx.x + h][i]);
     __syncthreads();
   }
-  if (threadIdx.x == 0) {
-    const double S1 = dsm[0][0], S0 = dsm[0][1], Sd = dsm[0][2], So = dsm[0][3];
-    if (gamma_out) *gamma_out = (S0 == 0.0) ? 0.f : float(S1 / S0);
-    if (do_r2) *r2_out = (So == 0.0) ? __int_as_float(0x7f800000) : float(Sd / So);
-    if (tdc_state) {
-      if (computed) { tdc_state[0] += 1; tdc_state[1] = 0; }
-      else tdc_state[1] += 1;
-    }
-    ws->counter = 0u;
+  if (threadIdx.x != 0) return false;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) out[i] = dsm[0][i];
+  ws->counter = 0u;
+  return true;
+}
+
+// Gamma / r2 from the four sums; TDC counters advanced.
+__device__ __forceinline__ void gamma_publish(const double S[4], bool do_r2, bool computed, float* gamma_out,
+                                              float* r2_out, int32_t* tdc_state) {
+  if (gamma_out) *gamma_out = (S[1] == 0.0) ? 0.f : __double2float_rn(__ddiv_rn(S[0], S[1]));
+  if (do_r2) *r2_out = (S[3] == 0.0) ? __int_as_float(0x7f800000) : __double2float_rn(__ddiv_rn(S[2], S[3]));
+  if (tdc_state) {
+    if (computed) { tdc_state[0] += 1; tdc_state[1] = 0; }
+    else tdc_state[1] += 1;
   }
 }
+
+// acc + x*x with the product rounded once (no contraction into an FMA).
+__device__ __forceinline__ float add_sq(float acc, float x) { return __fadd_rn(acc, __fmul_rn(x, x)); }
 
 // a7: one pass over (in, out, previous Delta).  Per element:
 //   d = f32(out) - f32(in); S1 += |d|; S0 += |in|;
 //   if computed: D_new = bf16(d) (stored over D_old); if r2 wanted:
 //   e = f32(D_new) - f32(D_old); Sd += e*e; So += D_old^2.
-// Persistent CTAs walk the tiles t = blockIdx, blockIdx + grid, ...; each
-// CTA's partials go to scratch as float64 and the last CTA sums them in CTA
-// order, writes Gamma / r2 and advances the TDC counters.  The grid depends
-// only on n and the SM count, so the sums are deterministic.  Three CTAs per
-// SM (<= 80 registers a thread): while some compute, the others' loads are
-// in flight.
+// The sums follow the fixed tree above.  Persistent CTAs walk the tiles
+// t = blockIdx, blockIdx + grid, ...; each tile's float32 partials go to
+// scratch and the last CTA reduces them, writes Gamma / r2 and advances the
+// TDC counters.  Three CTAs per SM: while some compute, the others' loads
+// are in flight.
 __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_kernel(
     const uint16_t* __restrict__ xin, const uint16_t* __restrict__ xout, int64_t n, uint16_t* delta, float* gamma_out,
-    float* r2_out, int32_t* tdc_state, const uint8_t* computed_ptr, GammaWs* ws, double* partials) {
+    float* r2_out, int32_t* tdc_state, const uint8_t* computed_ptr, GammaWs* ws, float* tile_part) {
+  __shared__ TileRed red;
   const bool computed = computed_ptr ? (*computed_ptr != 0) : true;
   const bool do_delta = computed && delta != nullptr;
   const bool do_r2 = do_delta && r2_out != nullptr && (tdc_state ? tdc_state[0] >= 1 : true);
   const int64_t ntiles = cdiv(n, kTile);
-  float s1 = 0.f, s0 = 0.f, sd = 0.f, so = 0.f;
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+  int it = 0;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
     const int64_t base = t * kTile;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};          // lane sums S1, S0, Sd, So of this tile
     uint4 vi[kVecPerThread], vo[kVecPerThread], vd[kVecPerThread];
 #pragma unroll
     for (int i = 0; i < kVecPerThread; ++i) {
@@ -141,36 +173,37 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_kernel(
         for (int e = 0; e < 4; ++e) {
           const float i0 = bf16lo(a[e]), i1 = bf16hi(a[e]);
           const float d0 = __fsub_rn(bf16lo(b[e]), i0), d1 = __fsub_rn(bf16hi(b[e]), i1);
-          s1 += fabsf(d0) + fabsf(d1);
-          s0 += fabsf(i0) + fabsf(i1);
+          v[0] = __fadd_rn(__fadd_rn(v[0], fabsf(d0)), fabsf(d1));
+          v[1] = __fadd_rn(__fadd_rn(v[1], fabsf(i0)), fabsf(i1));
           pw[e] = pack_bf16x2(d0, d1);         // D_new: one rounding of the fp32 difference
           if (do_r2) {
             const float e0 = __fsub_rn(bf16lo(pw[e]), bf16lo(c[e])), e1 = __fsub_rn(bf16hi(pw[e]), bf16hi(c[e]));
-            sd = __fmaf_rn(e1, e1, __fmaf_rn(e0, e0, sd));
-            so = __fmaf_rn(bf16hi(c[e]), bf16hi(c[e]), __fmaf_rn(bf16lo(c[e]), bf16lo(c[e]), so));
+            v[2] = add_sq(add_sq(v[2], e0), e1);
+            v[3] = add_sq(add_sq(v[3], bf16lo(c[e])), bf16hi(c[e]));
           }
         }
         if (do_delta) *reinterpret_cast<uint4*>(delta + idx) = w;
-      } else {                                  // ragged tail (scalar)
+      } else {                                  // ragged tail (scalar, same element order)
         const int cnt = int(n - idx);
         for (int e = 0; e < cnt; ++e) {
           const float fi = bf16_to_f32(xin[idx + e]);
           const float d = __fsub_rn(bf16_to_f32(xout[idx + e]), fi);
-          s1 += fabsf(d);
-          s0 += fabsf(fi);
+          v[0] = __fadd_rn(v[0], fabsf(d));
+          v[1] = __fadd_rn(v[1], fabsf(fi));
           const uint16_t dn = f32_to_bf16(d);
           if (do_r2) {
             const float fd = bf16_to_f32(delta[idx + e]);
-            const float ee = __fsub_rn(bf16_to_f32(dn), fd);
-            sd = __fmaf_rn(ee, ee, sd);
-            so = __fmaf_rn(fd, fd, so);
+            v[2] = add_sq(v[2], __fsub_rn(bf16_to_f32(dn), fd));
+            v[3] = add_sq(v[3], fd);
           }
           if (do_delta) delta[idx + e] = dn;
         }
       }
     }
+    tile_combine4(v, red, it, t, t + gridDim.x >= ntiles, tile_part, gridDim.x);
   }
-  gamma_finish(s1, s0, sd, so, do_r2, computed, gamma_out, r2_out, tdc_state, ws, partials);
+  double S[4];
+  if (tiles_finish(ntiles, ws, tile_part, S)) gamma_publish(S, do_r2, computed, gamma_out, r2_out, tdc_state);
 }
 
 // a7 with the compressed update cache (an extension; layout in common.cuh):
@@ -182,7 +215,8 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_kernel(
 // before its own write).  n % 32 == 0.
 __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_mx_kernel(
     const uint16_t* __restrict__ xin, const uint16_t* __restrict__ xout, int64_t n, uint8_t* cache, float* gamma_out,
-    float* r2_out, int32_t* tdc_state, const uint8_t* computed_ptr, GammaWs* ws, double* partials) {
+    float* r2_out, int32_t* tdc_state, const uint8_t* computed_ptr, GammaWs* ws, float* tile_part) {
+  __shared__ TileRed red;
   const bool computed = computed_ptr ? (*computed_ptr != 0) : true;
   const bool do_delta = computed && cache != nullptr;
   const bool do_r2 = do_delta && r2_out != nullptr && (tdc_state ? tdc_state[0] >= 1 : true);
@@ -190,9 +224,10 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_mx_kernel(
   const int lane = threadIdx.x & 31;
   const bool first = (lane & 3) == 0;
   const int64_t ntiles = cdiv(n, kTile);
-  float s1 = 0.f, s0 = 0.f, sd = 0.f, so = 0.f;
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+  int it = 0;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
     const int64_t base = t * kTile;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};          // lane sums S1, S0, Sd, So of this tile (missing elements add +0)
     uint4 vi[kVecPerThread], vo[kVecPerThread];
     uint2 vc[kVecPerThread];
     uint32_t vs[kVecPerThread];
@@ -222,8 +257,8 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_mx_kernel(
       for (int e = 0; e < 4; ++e) {
         const float i0 = bf16lo(a[e]), i1 = bf16hi(a[e]);
         const float d0 = __fsub_rn(bf16lo(b[e]), i0), d1 = __fsub_rn(bf16hi(b[e]), i1);
-        s1 += fabsf(d0) + fabsf(d1);
-        s0 += fabsf(i0) + fabsf(i1);
+        v[0] = __fadd_rn(__fadd_rn(v[0], fabsf(d0)), fabsf(d1));
+        v[1] = __fadd_rn(__fadd_rn(v[1], fabsf(i0)), fabsf(i1));
         pw[e] = pack_bf16x2(d0, d1);           // D_new: one rounding of the fp32 difference
       }
       if (do_r2) {
@@ -234,8 +269,8 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_mx_kernel(
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float e0 = __fsub_rn(bf16lo(pw[e]), c[2 * e]), e1 = __fsub_rn(bf16hi(pw[e]), c[2 * e + 1]);
-            sd = __fmaf_rn(e1, e1, __fmaf_rn(e0, e0, sd));
-            so = __fmaf_rn(c[2 * e + 1], c[2 * e + 1], __fmaf_rn(c[2 * e], c[2 * e], so));
+            v[2] = add_sq(add_sq(v[2], e0), e1);
+            v[3] = add_sq(add_sq(v[3], c[2 * e]), c[2 * e + 1]);
           }
         }
       }
@@ -258,14 +293,16 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_mx_kernel(
         }
       }
     }
+    tile_combine4(v, red, it, t, t + gridDim.x >= ntiles, tile_part, gridDim.x);
   }
-  gamma_finish(s1, s0, sd, so, do_r2, computed, gamma_out, r2_out, tdc_state, ws, partials);
+  double S[4];
+  if (tiles_finish(ntiles, ws, tile_part, S)) gamma_publish(S, do_r2, computed, gamma_out, r2_out, tdc_state);
 }
 
 // Calibration diagnostic (DMPQ side, Figures 1 and 4): one pass over two
-// tensors, {sum (a-b)^2, sum b^2, sum a*b, sum a^2}.  Same shape as the Gamma
-// pass: persistent CTAs over 8192-element tiles, fp32 per thread, float64
-// per CTA, the last CTA sums the partials in CTA order (deterministic).
+// tensors, {sum (a-b)^2, sum b^2, sum a*b, sum a^2}, each term rounded once
+// (d = a - b, then d*d; b*b; a*b; a*a), summed by the fixed tree of the Gamma
+// pass, so the four float64 sums do not depend on the grid.
 template <typename T>
 __device__ __forceinline__ void load8(const T* p, int64_t i, float (&v)[8]);
 template <>
@@ -286,12 +323,12 @@ template <typename TA, typename TB>
 __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) pair_stats_kernel(const TA* __restrict__ a,
                                                                                const TB* __restrict__ b, int64_t n,
                                                                                double* out, GammaWs* ws,
-                                                                               double* partials) {
-  __shared__ float sm[kThreads / 32][4];
-  __shared__ bool is_last;
+                                                                               float* tile_part) {
+  __shared__ TileRed red;
   const int64_t ntiles = cdiv(n, kTile);
-  float sdd = 0.f, sbb = 0.f, sab = 0.f, saa = 0.f;
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+  int it = 0;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+    float v[4] = {0.f, 0.f, 0.f, 0.f};          // lane sums of (a-b)^2, b^2, a*b, a^2
 #pragma unroll
     for (int i = 0; i < kVecPerThread; ++i) {
       const int64_t idx = t * kTile + (int64_t(i) * kThreads + threadIdx.x) * 8;
@@ -301,36 +338,18 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) pair_stats_kernel(c
       load8(b, idx, vb);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float d = va[e] - vb[e];
-        sdd = __fmaf_rn(d, d, sdd);
-        sbb = __fmaf_rn(vb[e], vb[e], sbb);
-        sab = __fmaf_rn(va[e], vb[e], sab);
-        saa = __fmaf_rn(va[e], va[e], saa);
+        v[0] = add_sq(v[0], __fsub_rn(va[e], vb[e]));
+        v[1] = add_sq(v[1], vb[e]);
+        v[2] = __fadd_rn(v[2], __fmul_rn(va[e], vb[e]));
+        v[3] = add_sq(v[3], va[e]);
       }
     }
+    tile_combine4(v, red, it, t, t + gridDim.x >= ntiles, tile_part, gridDim.x);
   }
-  float v[4] = {sdd, sbb, sab, saa};
-  block_sum4(v, sm);
-  if (threadIdx.x == 0) {
-    double* p = partials + 4 * int64_t(blockIdx.x);
-    p[0] = v[0]; p[1] = v[1]; p[2] = v[2]; p[3] = v[3];
-    __threadfence();
-    is_last = atomicAdd(&ws->counter, 1u) == gridDim.x - 1;
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  if (threadIdx.x == 0) {
-    double acc[4] = {0, 0, 0, 0};
-    for (unsigned c = 0; c < gridDim.x; ++c) {
-      const volatile double* p = partials + 4 * int64_t(c);
+  double S[4];
+  if (tiles_finish(ntiles, ws, tile_part, S))
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] += p[i];
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) out[i] = acc[i];
-    ws->counter = 0u;
-  }
+    for (int i = 0; i < 4; ++i) out[i] = S[i];
 }
 
 // a8: p = f32(f32(alpha*Gamma) + beta); NVFP4 iff step > 0 and p < tau.
@@ -643,17 +662,21 @@ __global__ void __launch_bounds__(kLnThreads<NB>) ln_quant_kernel(const LnQuantC
 }  // namespace
 
 // ---------------------------------------------------------------------------
+// Scratch of a pass over n elements: the CTA counter, then 4 floats a tile.
+constexpr size_t kWsHeader = 256;
+size_t tiles_ws_bytes(int64_t n) { return kWsHeader + size_t(cdiv(n, kTile)) * 4 * sizeof(float); }
+
 // Scratch-free Gamma pass.  Some callers cannot give this library scratch
 // memory: their device memory is entirely planned by another allocator, or
 // they run where allocating is not allowed (a plugin's enqueue step, a
 // latency-critical loop that cannot afford cudaMalloc's implicit device
-// synchronization).  For them the pass keeps its CTA counter and float64
+// synchronization).  For them the pass keeps its CTA counter and per-tile
 // partial sums in this fixed device array instead of caller scratch.  The
 // array lives on every device that loads the library, until the process
 // exits, and bounds the tensor size to kNoAllocMaxElems.
 constexpr int64_t kNoAllocMaxElems = int64_t(1) << 27;                  // 134,217,728 elements
-constexpr size_t kNoAllocBytes = 262400;                                 // counter + partials of <= 8192 CTAs
-static_assert(kNoAllocBytes >= 256 + size_t(kGammaMaxCtas) * 4 * sizeof(double), "no-alloc scratch");
+constexpr size_t kNoAllocBytes = kWsHeader + size_t(kNoAllocMaxElems / kTile) * 4 * sizeof(float);   // 262,400
+static_assert(kNoAllocBytes == 262400, "no-alloc scratch: header + 16384 tiles x 16 bytes");
 static __device__ __align__(256) unsigned char g_gamma_scratch[kNoAllocBytes];
 
 namespace {
@@ -692,54 +715,49 @@ int launch_block_gamma_noalloc(const void* xin, const void* xout, int64_t n, voi
 
 int gamma_grid(int64_t n, int num_sms) {
   const int64_t tiles = cdiv(n, kTile);
-  int64_t g = int64_t(num_sms) * kGammaCtasPerSm;
-  if (g > kGammaMaxCtas) g = kGammaMaxCtas;
+  const int64_t g = int64_t(num_sms) * kGammaCtasPerSm;
   return int(tiles < g ? tiles : g);
 }
 
-size_t gamma_ws_bytes(int64_t n) {
-  const int64_t tiles = cdiv(n, kTile);
-  const int64_t ctas = tiles < kGammaMaxCtas ? tiles : kGammaMaxCtas;
-  return 256 + size_t(ctas) * 4 * sizeof(double);
-}
+size_t gamma_ws_bytes(int64_t n) { return tiles_ws_bytes(n); }
 
 int launch_block_gamma(const void* xin, const void* xout, int64_t n, void* delta, float* gamma_out, float* r2_out,
                        int32_t* tdc_state, const uint8_t* computed, void* ws, int num_sms, cudaStream_t s) {
   GammaWs* w = static_cast<GammaWs*>(ws);
-  double* partials = reinterpret_cast<double*>(static_cast<char*>(ws) + 256);
-  gamma_kernel<<<unsigned(gamma_grid(n, num_sms)), kThreads, 0, s>>>(static_cast<const uint16_t*>(xin), static_cast<const uint16_t*>(xout),
-                                                    n, static_cast<uint16_t*>(delta), gamma_out, r2_out, tdc_state,
-                                                    computed, w, partials);
+  float* parts = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
+  gamma_kernel<<<unsigned(gamma_grid(n, num_sms)), kThreads, 0, s>>>(
+      static_cast<const uint16_t*>(xin), static_cast<const uint16_t*>(xout), n, static_cast<uint16_t*>(delta),
+      gamma_out, r2_out, tdc_state, computed, w, parts);
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 
 int launch_block_gamma_mx(const void* xin, const void* xout, int64_t n, void* cache, float* gamma_out, float* r2_out,
                           int32_t* tdc_state, const uint8_t* computed, void* ws, int num_sms, cudaStream_t s) {
   GammaWs* w = static_cast<GammaWs*>(ws);
-  double* partials = reinterpret_cast<double*>(static_cast<char*>(ws) + 256);
+  float* parts = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
   gamma_mx_kernel<<<unsigned(gamma_grid(n, num_sms)), kThreads, 0, s>>>(
       static_cast<const uint16_t*>(xin), static_cast<const uint16_t*>(xout), n, static_cast<uint8_t*>(cache),
-      gamma_out, r2_out, tdc_state, computed, w, partials);
+      gamma_out, r2_out, tdc_state, computed, w, parts);
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 
 int launch_pair_stats(const void* a, int a_f32, const void* b, int b_f32, int64_t n, double* out, void* ws,
                       int num_sms, cudaStream_t s) {
   GammaWs* w = static_cast<GammaWs*>(ws);
-  double* partials = reinterpret_cast<double*>(static_cast<char*>(ws) + 256);
+  float* parts = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
   const unsigned grid = unsigned(gamma_grid(n, num_sms));
   if (!a_f32 && !b_f32)
     pair_stats_kernel<uint16_t, uint16_t><<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(a),
-                                                                    static_cast<const uint16_t*>(b), n, out, w, partials);
+                                                                    static_cast<const uint16_t*>(b), n, out, w, parts);
   else if (!a_f32)
     pair_stats_kernel<uint16_t, float><<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(a),
-                                                                 static_cast<const float*>(b), n, out, w, partials);
+                                                                 static_cast<const float*>(b), n, out, w, parts);
   else if (!b_f32)
     pair_stats_kernel<float, uint16_t><<<grid, kThreads, 0, s>>>(static_cast<const float*>(a),
-                                                                 static_cast<const uint16_t*>(b), n, out, w, partials);
+                                                                 static_cast<const uint16_t*>(b), n, out, w, parts);
   else
     pair_stats_kernel<float, float><<<grid, kThreads, 0, s>>>(static_cast<const float*>(a), static_cast<const float*>(b),
-                                                              n, out, w, partials);
+                                                              n, out, w, parts);
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 

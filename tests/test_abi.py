@@ -79,11 +79,11 @@ def test_host_helpers(lib):
     assert lib.sixbit_sf_bytes(256, 256) == 256 * 16
     assert lib.sixbit_sf_bytes(200, 1920) == 256 * 120        # rows padded to 128
     assert lib.sixbit_sf_bytes(1, 64) == 128 * 4
-    # Gamma pass scratch: a 256-byte header plus 4 float64 partials per CTA of
-    # a persistent grid of at most 1024 CTAs (8192-element tiles)
-    ws = lib.sixbit_workspace_size(17776, 1920)
-    assert 256 + 4 * 8 * 1024 <= ws <= 256 + 4 * 8 * 1024 + 512
-    assert lib.sixbit_workspace_size(1, 64) >= 256 + 4 * 8
+    # Gamma pass scratch: a 256-byte header plus 4 float32 tile sums per
+    # 8192-element tile (17776 * 1920 elements: 4167 tiles)
+    assert lib.sixbit_workspace_size(17776, 1920) == 256 + 16 * 4167
+    assert lib.sixbit_workspace_size(1, 64) == 512                  # at least 512 bytes (the amax slot)
+    assert lib.sixbit_workspace_size(1 << 27, 1) == 262400          # the scratch-free variant's limit
 
 
 def test_argument_errors_before_launch(lib):

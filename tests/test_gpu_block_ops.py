@@ -1,6 +1,6 @@
 """GPU parity of the Gamma/Delta pass (a7), DMPQ (a8), TDC (a9) and the
-block harness LayerNorm.  Delta bits, flags and skip decisions are
-bit-exact; Gamma and r2 agree with the oracle's float64 sums to 2e-6."""
+block harness LayerNorm.  Delta bits, Gamma and r2 (both reduced by the
+fixed tree the oracle defines), flags and skip decisions are bit-exact."""
 import numpy as np
 import pytest
 import torch
@@ -10,7 +10,6 @@ from oracle import block as o_block, codecs, dmpq as o_dmpq, gamma as o_gamma, t
 from tests.helpers import dev, dev_bf16, host, host_bf16_bits
 
 pytestmark = pytest.mark.gpu
-RTOL = 2e-6
 
 
 def _sb():
@@ -18,7 +17,8 @@ def _sb():
     return sb
 
 
-@pytest.mark.parametrize("M,H", [(256, 256), (1, 8), (3, 5000), (17, 1920), (synthetic.M_2B, 1920)])
+@pytest.mark.parametrize("M,H", [(256, 256), (1, 8), (3, 5000), (7, 333), (3, 8191), (17, 1920),
+                                 (synthetic.M_2B, 1920)])
 def test_gamma_delta_r2(M, H):
     sb = _sb()
     p = synthetic.gamma_pair(M * 7 + H, M, H)
@@ -29,8 +29,7 @@ def test_gamma_delta_r2(M, H):
     rg = o_gamma.gamma(p["xin"], p["xout"])
     rdn = o_gamma.delta(p["xin"], p["xout"])
     rr2 = o_gamma.rel_l2_sq(rdn, p["delta_prev"])
-    assert abs(host(g)[0] - rg) <= RTOL * abs(rg)
-    assert abs(host(r2)[0] - rr2) <= RTOL * abs(rr2) + 1e-12
+    assert host(g)[0] == rg and host(r2)[0] == rr2
     assert np.array_equal(host_bf16_bits(dprev), rdn)
     assert host(state).tolist() == [2, 0]
 
@@ -152,8 +151,7 @@ def test_gamma_mxcache_parity(M, H):
     rdn = o_gamma.delta(p["xin"], p["xout"])
     rr2 = o_gamma.rel_l2_sq(rdn, prev_val.reshape(M, H))
     rg = o_gamma.gamma(p["xin"], p["xout"])
-    assert abs(host(g)[0] - rg) <= RTOL * abs(rg)
-    assert abs(host(r2)[0] - rr2) <= RTOL * abs(rr2) + 1e-12
+    assert host(g)[0] == rg and host(r2)[0] == rr2
     codes, sc = mxcache.encode(codecs.bf16_to_f32(rdn))
     assert np.array_equal(host(cache), mxcache.to_bytes(codes, sc))       # the new update, encoded
     assert host(state).tolist() == [2, 0]

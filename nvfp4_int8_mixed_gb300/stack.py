@@ -177,14 +177,18 @@ class DiTStack:
         quantize_act_int8(self.u, want_q=False, pred=gates[3, 1:2], out=(None, planes_u, self.rs))
         qlinear_w4a8(planes_u, self.rs, *wd, residual=self.x1, out=out, pred=gates[3, 1:2])
 
-    def enqueue_step(self, hook=None):
+    def enqueue_step(self, hook=None, block_hook=None):
         """Enqueue one denoising step on the current stream (graph-capturable).
         hook (eager calibration runs only): called as hook(block, layer_index,
-        x) with each linear layer's bf16 input before the layer runs."""
+        x) with each linear layer's bf16 input before the layer runs.
+        block_hook (eager runs only): called as block_hook(block, x_in, x_out)
+        just before the block's Gamma pass, when the update cache still holds
+        the previous update; work it enqueues on the stream sees the block's
+        input and output."""
         if self.fused:
             if hook is not None:
                 raise ValueError("calibration hooks need the unfused stack (fused=False)")
-            return self._enqueue_fused()
+            return self._enqueue_fused(block_hook)
         H = self.H
         call = (lambda l, i, x: hook(l, i, x)) if hook is not None else (lambda l, i, x: None)
         dmpq_assign(self.gamma, self.alpha, self.beta, self.layer_block, self.tau, self.step_dev,
@@ -211,12 +215,14 @@ class DiTStack:
             call(l, 3, self.u)
             self._ql(self.u, self.wq[l]["down"], g(3, 0), g(3, 1), out, residual=self.x1,
                      amax_in=amax_hist_value(self.u_amax))
+            if block_hook is not None:
+                block_hook(l, h, out)
             block_gamma(h, out, delta=self.delta[l], gamma_out=self.gamma[l:l + 1], r2_out=self.r2[l:l + 1],
                         tdc_state=self.state[l], computed=c)
             h = out
         self.out = h
 
-    def _enqueue_fused(self):
+    def _enqueue_fused(self, block_hook=None):
         H = self.H
         dmpq_assign(self.gamma, self.alpha, self.beta, self.layer_block, self.tau, self.step_dev,
                     use_nvfp4=self.use_nvfp4, gates=self.gates)
@@ -234,6 +240,8 @@ class DiTStack:
             self._ql(v, self.wq[l]["out"], g(1, 0), g(1, 1), self.x1, residual=h)
             self._ln_q(self.x1, 2, l, gates, c, keep_bf16=False)
             self._up_down_fused(l, gates, out)
+            if block_hook is not None:
+                block_hook(l, h, out)
             block_gamma(h, out, delta=self.delta[l], gamma_out=self.gamma[l:l + 1], r2_out=self.r2[l:l + 1],
                         tdc_state=self.state[l], computed=c)
             h = out
@@ -296,123 +304,3 @@ class DiTStack:
                 log["r2"].append(self.r2.clone())
                 log["state"].append(self.state.clone())
         return outs, log
-
-
-def calibrate_tau(stack: DiTStack, xs, frac: float = 0.6) -> float:
-    """DMPQ threshold from an all-INT8 run: the `frac` quantile of the
-    predictions alpha * Gamma_{t-1} + beta over (layer, step >= 1)."""
-    tau0, tdc0 = stack.tau, stack.max_skip
-    stack.tau, stack.max_skip = float("-inf"), 0
-    stack.graph = None
-    stack.reset()
-    _, log = stack.run(xs, record=True)
-    g = torch.stack(log["gamma"][:-1]).cpu().numpy()                # Gamma_{t-1} for t = 1..T-1
-    lb = stack.layer_block.cpu().numpy()
-    a, b = stack.alpha.cpu().numpy(), stack.beta.cpu().numpy()
-    p = (a[None, :] * g[:, lb]).astype(np.float32) + b[None, :]
-    stack.tau, stack.max_skip = tau0, tdc0
-    stack.graph = None
-    stack.reset()
-    return float(np.float32(np.quantile(p.astype(np.float64), frac)))
-
-
-def calibrate_lines(stack: DiTStack, xs, weights, steps=None):
-    """The calibration side of DMPQ (thelatestinai.com page, Figures 1, 3, 4)
-    on the synthetic stack.
-
-    Runs the stack eagerly with every layer in INT8 and TDC off (the same
-    trajectory calibrate_tau uses).  For every step t and linear layer it
-    measures E_rel = ||Y_q - Y|| / ||Y|| for both activation formats, with
-    Y = x W^T in fp32 from the layer's actual bf16 input and the unquantized
-    weights (a plain library GEMM: this is an offline diagnostic) and Y_q the
-    W4A4 / W4A8 product of the same input.  Also per block: Gamma_t and the
-    similarity of consecutive updates (cosine, relative L2).  Each layer's
-    line E_rel_NVFP4(t) ~ alpha * Gamma_{b(l)}(t-1) + beta is then fitted by
-    least squares over t >= 1.
-
-    weights: the per-block dicts the stack was built from (fp32).  Returns a
-    dict of numpy arrays: e_rel_nvfp4, e_rel_int8 [T, layers], gamma [T,
-    blocks], delta_cos, delta_rel [T, blocks] (NaN at t = 0), alpha, beta,
-    r2 [layers].
-    """
-    from . import pair_stats, qlinear_w4a4, qlinear_w4a8
-    if stack.tdc_cache != "bf16":
-        raise ValueError("calibration compares bf16 updates: build the stack with tdc_cache='bf16'")
-    T = len(xs) if steps is None else min(steps, len(xs))
-    nb = stack.nb
-    names = ("qkv", "out", "up", "down")
-    dev = stack.dev
-    w32 = [{k: torch.as_tensor(b[k]).to(dev, torch.float32) for k in names} for b in weights]
-    e4 = np.full((T, 4 * nb), np.nan)
-    e8 = np.full((T, 4 * nb), np.nan)
-    gam = np.zeros((T, nb))
-    dcos = np.full((T, nb), np.nan)
-    drel = np.full((T, nb), np.nan)
-    stats = torch.empty((T, 4 * nb, 2, 4), dtype=torch.float64, device=dev)
-
-    def hook(t):
-        def measure(l, i, x):
-            w = w32[l][names[i]]
-            y_ref = x.float() @ w.t()
-            codes, sf, ga = quantize_act_nvfp4(x)
-            y4 = qlinear_w4a4(codes, sf, ga, *stack.wq[l][names[i]], out_dtype=torch.float32)
-            _, planes, s = quantize_act_int8(x, want_q=False)
-            y8 = qlinear_w4a8(planes, s, *stack.wq[l][names[i]], out_dtype=torch.float32)
-            pair_stats(y4, y_ref, out=stats[t, 4 * l + i, 0])
-            pair_stats(y8, y_ref, out=stats[t, 4 * l + i, 1])
-        return measure
-
-    tau0, skip0, graph0 = stack.tau, stack.max_skip, stack.graph
-    stack.tau, stack.max_skip, stack.graph = float("-inf"), 0, None
-    stack.reset()
-    prev = [None] * nb
-    dstats = torch.full((T, nb, 4), float("nan"), dtype=torch.float64, device=dev)
-    for t in range(T):
-        stack.x_in.copy_(xs[t])
-        stack.step_dev.fill_(t)
-        old = [d.clone() for d in stack.delta] if t >= 1 else None
-        stack.enqueue_step(hook=hook(t))
-        if old is not None:                        # Delta_{t-1} existed: compare Delta_t with it
-            for l in range(nb):
-                pair_stats(stack.delta[l], old[l], out=dstats[t, l])
-        gam[t] = stack.gamma.cpu().numpy()
-    torch.cuda.synchronize()
-    st = stats.cpu().numpy()
-    with np.errstate(divide="ignore", invalid="ignore"):
-        e4[:] = np.sqrt(st[:, :, 0, 0] / st[:, :, 0, 1])
-        e8[:] = np.sqrt(st[:, :, 1, 0] / st[:, :, 1, 1])
-        ds = dstats.cpu().numpy()
-        drel[:] = np.sqrt(ds[:, :, 0] / ds[:, :, 1])
-        dcos[:] = ds[:, :, 2] / np.sqrt(ds[:, :, 3] * ds[:, :, 1])
-    lb = stack.layer_block.cpu().numpy()
-    alpha = np.zeros(4 * nb)
-    beta = np.zeros(4 * nb)
-    r2 = np.zeros(4 * nb)
-    for k in range(4 * nb):
-        x = gam[:T - 1, lb[k]]                     # Gamma_{t-1}
-        y = e4[1:T, k]                             # E_rel at t
-        alpha[k], beta[k] = _fit_line(x, y)
-        r2[k] = _r_squared(x, y, alpha[k], beta[k])
-    stack.tau, stack.max_skip, stack.graph = tau0, skip0, graph0
-    stack.reset()
-    return dict(e_rel_nvfp4=e4, e_rel_int8=e8, gamma=gam, delta_cos=dcos, delta_rel=drel, alpha=alpha, beta=beta,
-                r2=r2)
-
-
-def _fit_line(x, y):
-    """Least-squares alpha, beta of y ~ alpha x + beta (float64); constant x -> (0, mean y)."""
-    x = np.asarray(x, np.float64)
-    y = np.asarray(y, np.float64)
-    mx, my = x.mean(), y.mean()
-    sxx = ((x - mx) ** 2).sum()
-    if sxx == 0.0:
-        return 0.0, float(my)
-    a = ((x - mx) * (y - my)).sum() / sxx
-    return float(a), float(my - a * mx)
-
-
-def _r_squared(x, y, a, b):
-    y = np.asarray(y, np.float64)
-    res = y - (a * np.asarray(x, np.float64) + b)
-    tot = ((y - y.mean()) ** 2).sum()
-    return 1.0 if tot == 0.0 else float(1.0 - (res @ res) / tot)

@@ -1,6 +1,10 @@
 """GPU parity of the DiT block stack with DMPQ and TDC (reduced config-4
 shape) against the oracle.
 
+Gamma and r2 are checked bit for bit: the oracle's fixed reduction tree
+applied to each block's device input and output must give the device's
+values, so the flags that follow from them are the oracle's too.
+
 Decisions are checked as decisions: the device's DMPQ flags must equal the
 oracle's rule applied to the device's own Gamma of the previous step, and
 its TDC skips the oracle's rule applied to the device's counters and r2.
@@ -18,7 +22,8 @@ pytestmark = pytest.mark.gpu
 
 
 def _run(tau_tdc, max_skip, nb=3, M=300, H=256, F=512, steps=6, seed=7, refresh=0, fused=False, cache="bf16"):
-    from nvfp4_int8_mixed_gb300.stack import DiTStack, calibrate_tau
+    from nvfp4_int8_mixed_gb300.calibration import calibrate_tau
+    from nvfp4_int8_mixed_gb300.stack import DiTStack
     st = synthetic.stack_setup(seed, nb, H, F)
     xs = synthetic.stack_inputs(st["noise_seed"], M, H, steps)
     xs_dev = [dev_bf16(x) for x in xs]
@@ -86,3 +91,49 @@ def test_stack_graph_replay_is_deterministic():
         assert np.array_equal(a, b)
     for a, b in zip(rec1["gamma"], rec2["gamma"]):
         assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("fused,cache", [(False, "bf16"), (True, "bf16"), (False, "mx")])
+def test_stack_gamma_and_r2_bits_on_the_device_tensors(fused, cache):
+    """Eager run with a hook that copies every block's input, output and
+    previous update just before its Gamma pass: the oracle's Gamma / r2 of
+    those tensors equal the device's bit for bit."""
+    from nvfp4_int8_mixed_gb300.calibration import calibrate_tau
+    from nvfp4_int8_mixed_gb300.stack import DiTStack
+    from oracle import gamma as o_gamma, mxcache
+    nb, M, H, F, steps = 3, 300, 256, 512, 5
+    st = synthetic.stack_setup(7, nb, H, F)
+    xs = synthetic.stack_inputs(st["noise_seed"], M, H, steps)
+    xs_dev = [dev_bf16(x) for x in xs]
+    stack = DiTStack(st["blocks"], st["alpha"], st["beta"], M, H, F, tau=0.0, tau_tdc=10.0, max_skip=1,
+                     fused=fused, tdc_cache=cache)
+    stack.tau = calibrate_tau(stack, xs_dev)
+    stack.reset()
+    seen = []
+
+    def hook(l, h, out):
+        seen.append((l, h.clone(), out.clone(), stack.delta[l].clone(), stack.state[l].clone(),
+                     stack.cflag[l:l + 1].clone()))
+
+    per_step = []
+    for t in range(steps):
+        stack.x_in.copy_(xs_dev[t])
+        stack.step_dev.fill_(t)
+        seen.clear()
+        stack.enqueue_step(block_hook=hook)
+        torch.cuda.synchronize()
+        per_step.append(([tuple(host(v) if v.dtype != torch.bfloat16 else host_bf16_bits(v) for v in rec[1:])
+                          for rec in seen], host(stack.gamma), host(stack.r2)))
+    n_r2 = 0
+    for t, (blocks, g_dev, r2_dev) in enumerate(per_step):
+        for l, (h, out, prev, state, cflag) in enumerate(blocks):
+            assert g_dev[l] == o_gamma.gamma(h, out), (t, l)
+            if cflag[0] and state[0] >= 1:
+                if cache == "bf16":
+                    prev_val = prev
+                else:
+                    n = M * H
+                    prev_val = mxcache.decode(prev[:n], prev[n:])
+                assert r2_dev[l] == o_gamma.rel_l2_sq(o_gamma.delta(h, out), prev_val), (t, l)
+                n_r2 += 1
+    assert n_r2 >= nb                                  # every block had a computed step with a previous update

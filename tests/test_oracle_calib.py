@@ -51,14 +51,34 @@ def test_pair_sums_hand_values():
 
 
 def test_product_line_fit_matches_oracle():
-    # host logic of the calibration driver (nvfp4_int8_mixed_gb300.stack) against the oracle
-    from nvfp4_int8_mixed_gb300 import stack
+    # The calibration module's own least-squares solve and R^2 (squared
+    # correlation) against the oracle's centred closed forms: two different
+    # computations of the same fit.
+    from nvfp4_int8_mixed_gb300 import calibration
     rng = np.random.default_rng(5)
     for _ in range(5):
         x = rng.uniform(0, 0.3, 40)
         y = 0.7 * x + 0.02 + 0.01 * rng.standard_normal(40)
-        a, b = stack._fit_line(x, y)
+        a, b = calibration.fit_line(x, y)
         ra, rb = calib.fit_line(x, y)
-        assert a == pytest.approx(ra, rel=1e-12) and b == pytest.approx(rb, rel=1e-12)
-        assert stack._r_squared(x, y, a, b) == pytest.approx(calib.r_squared(x, y, ra, rb), rel=1e-12)
-    assert stack._fit_line([0.2, 0.2], [1.0, 3.0]) == calib.fit_line([0.2, 0.2], [1.0, 3.0])
+        assert a == pytest.approx(ra, rel=1e-9) and b == pytest.approx(rb, rel=1e-9)
+        assert calibration.r_squared(x, y) == pytest.approx(calib.r_squared(x, y, ra, rb), rel=1e-9)
+    assert calibration.fit_line([0.2, 0.2], [1.0, 3.0]) == calib.fit_line([0.2, 0.2], [1.0, 3.0])
+    assert calibration.r_squared([0.2, 0.2], [1.0, 3.0]) == calib.r_squared([0.2, 0.2], [1.0, 3.0], 0.0, 2.0)
+    assert calibration.r_squared([0.1, 0.2, 0.3], [5.0, 5.0, 5.0]) == 1.0
+    # an exact line: slope, intercept and R^2 = 1
+    a, b = calibration.fit_line([0.0, 0.1, 0.4], [0.5, 0.8, 1.7])
+    assert a == pytest.approx(3.0, rel=1e-12) and b == pytest.approx(0.5, rel=1e-12)
+
+
+def test_pair_sums_tree_within_float32_rounding_of_float64_sums():
+    rng = np.random.default_rng(5)
+    b = rng.standard_normal(50_003).astype(np.float32)
+    a = (b + 0.1 * rng.standard_normal(50_003)).astype(np.float32)
+    t, e = calib.pair_sums_tree(a, b), calib.pair_sums(a, b)
+    for i in (0, 1, 3):                        # nonnegative terms
+        assert abs(t[i] - e[i]) <= 50 * 2.0 ** -24 * e[i]
+    # the signed sum: bounded by the sum of |a*b|
+    assert abs(t[2] - e[2]) <= 50 * 2.0 ** -24 * float(np.abs(a.astype(np.float64) * b).sum())
+    assert calib.pair_sums_tree(np.ones(8192 * 2 + 8, np.float32), np.zeros(8192 * 2 + 8, np.float32)).tolist() == \
+        [16392.0, 0.0, 0.0, 16392.0]

@@ -152,8 +152,16 @@ int sixbit_qlinear_w4a8(const uint8_t* a_planes, const float* row_scale, int64_t
  * r2_out[0] = ||D_new-D_old||^2/||D_old||^2 (+inf if ||D_old|| = 0) is
  * written.  tdc_state (nullable) int32[2] = {fresh_count, consec}:
  * computed -> {fresh+1, 0}; skipped -> {fresh, consec+1}.
- * Deterministic: fixed 16384-element tiles, fp32 inside a tile, fp64
- * across tiles.  ws: sixbit_workspace_size(n, 1) bytes. */
+ * Reduction (a reading: the pages fix no precision): float32 terms
+ * (d = out - in, |d|, |in|; e = D_new - D_old, e*e, D_old*D_old, each rounded
+ * once), summed by one fixed tree -- 8192-element tiles; in a tile, lane t
+ * of 256 adds elements j*2048 + 8t + e (j < 4, e < 8) in order in float32;
+ * lanes combine by a butterfly within each 32 (t^16, ..., t^1), then the 8
+ * group sums by halving; tile sums are added in float64 by 256 lanes (tile
+ * k to lane k % 256, in order) and halved; Gamma = f32(S1/S0),
+ * r2 = f32(Sd/So).  The result depends only on the input, never on the
+ * grid or the GPU.  ws: sixbit_workspace_size(n, 1) bytes (256 + 16 per
+ * tile). */
 int sixbit_block_gamma(const void* in, const void* out, int64_t n, void* delta,
                        float* gamma_out, float* r2_out, int32_t* tdc_state,
                        const uint8_t* computed, void* ws, sixbit_stream_t stream);
@@ -172,7 +180,9 @@ int sixbit_block_gamma(const void* in, const void* out, int64_t n, void* delta,
  * stream capture.  Every call clears the array's counter (an async memset on
  * `stream`) and then reuses it, so calls whose kernels overlap on the GPU --
  * on different streams, or on different host threads -- race and must be
- * avoided.  Allocates no device memory. */
+ * avoided.  Allocates no device memory.  262,400 bytes = a 256-byte header
+ * plus 16 bytes for each of the 16,384 tiles of 8192 elements that the
+ * 2^27-element limit allows. */
 #define SIXBIT_NOALLOC_GAMMA_MAX_ELEMS (((int64_t)1) << 27)
 int sixbit_block_gamma_noalloc(const void* in, const void* out, int64_t n, void* delta,
                                float* gamma_out, float* r2_out, int32_t* tdc_state,
@@ -184,9 +194,10 @@ int sixbit_block_gamma_noalloc(const void* in, const void* out, int64_t n, void*
  * SIXBIT_F32; n % 8 == 0; 16-byte aligned):
  *   out[0..3] = float64 {sum (a-b)^2, sum b^2, sum a*b, sum a^2}
  * so ||a-b||/||b|| = sqrt(out[0]/out[1]) and cos = out[2]/sqrt(out[3]*out[1]).
- * Sums: fp32 per thread, float64 across CTAs in a fixed order
- * (deterministic).  ws: sixbit_workspace_size(n, 1) bytes of scratch; out:
- * 4 device doubles. */
+ * Each term is rounded once in float32 (d = a - b, then d*d; b*b; a*b;
+ * a*a) and the sums follow the fixed tree of sixbit_block_gamma, so the
+ * result depends only on the input.  ws: sixbit_workspace_size(n, 1) bytes
+ * of scratch; out: 4 device doubles. */
 int sixbit_pair_stats(const void* a, int a_dtype, const void* b, int b_dtype, int64_t n,
                       double* out, void* ws, sixbit_stream_t stream);
 
@@ -316,6 +327,17 @@ int sixbit_qlinear_qout(int mode, const uint8_t* a, const uint8_t* a_sf, const f
                         const void* bias, int epi, void* y, int64_t ldy,
                         uint8_t* q_codes, uint8_t* q_sf, float* q_g, uint32_t* amax_hist, float headroom,
                         const uint8_t* q_pred, const uint8_t* pred, sixbit_stream_t stream);
+
+/* Test switch of the failure path (no counterpart in the pages).  on != 0:
+ * every linear-layer launch on the current device that follows makes its
+ * MMA-issuing thread wait on a barrier nothing signals, so that bounded wait
+ * expires (after its normal poll cap): the kernel records SIXBIT_EDEVICE in
+ * the device error word, tells its other roles to stop, waits for its own
+ * copies and MMAs in flight, frees its tensor memory and exits, leaving the
+ * output undefined.  on = 0 restores normal operation.  Synchronous (a
+ * copy to a device variable); allocates nothing.  For tests of the
+ * sixbit_get_error() contract only. */
+int sixbit_debug_stall_gemm(int on);
 
 /* Synchronizes `stream`, returns SIXBIT_EDEVICE if a device wait gave up
  * since the last call (and clears the word), else the stream's CUDA status

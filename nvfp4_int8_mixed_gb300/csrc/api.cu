@@ -1,6 +1,8 @@
 // C ABI of the sixbit library: argument checks on the host, then launches.
 // Nothing here allocates device memory.
 #include <cstdint>
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 #include "../../include/sixbit.h"
@@ -15,30 +17,38 @@ __device__ int g_sixbit_error = 0;
 namespace {
 
 constexpr int kMaxDevices = 64;
-int g_num_sms[kMaxDevices] = {0};
-int* g_err_ptr[kMaxDevices] = {nullptr};
+struct DeviceInfo {
+  int num_sms;
+  int* err;
+};
+std::mutex g_dev_mu;
+DeviceInfo g_dev[kMaxDevices] = {};
 
 // Per-device setup with the device current: SM count and the device address
 // of the error word (host code must not take the address of a __device__
-// variable directly).
+// variable directly).  Filled once per device under a lock, so host threads
+// calling the library at the same time see a complete entry.
 int device_setup(int* num_sms, int** err) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return kELaunch;
-  if (g_num_sms[dev] == 0) {
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.num_sms == 0) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return kELaunch;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_sixbit_error) != cudaSuccess) return kELaunch;
-    g_err_ptr[dev] = static_cast<int*>(p);
-    g_num_sms[dev] = n;
+    d.err = static_cast<int*>(p);
+    d.num_sms = n;
   }
-  *num_sms = g_num_sms[dev];
-  if (err) *err = g_err_ptr[dev];
+  *num_sms = d.num_sms;
+  if (err) *err = d.err;
   return kOk;
 }
 
-// Scratch layout: [0, 4) Gamma-pass CTA counter, [64, 68) tensor amax,
-// [256, ...) Gamma-pass partial sums.
+// Scratch layout: [0, 4) CTA counter of the Gamma pass (and of the pair
+// statistics), [64, 68) tensor amax, [256, ...) 4 floats per 8192-element
+// tile of those passes.
 constexpr size_t kWsAmaxOffset = 64;
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -70,7 +80,6 @@ int sixbit_amax_bf16(const void* x, int64_t M, int64_t K, int64_t ldx, float* am
   if (!aligned16(x)) return kEAlign;
   int sms;
   if (device_setup(&sms, nullptr) != kOk) return kELaunch;
-  if (M == 0) return amax_out ? (cudaMemsetAsync(amax_out, 0, 4, cs(stream)) == cudaSuccess ? kOk : kELaunch) : kOk;
   return launch_amax(x, SIXBIT_BF16, M, K, ldx, amax_out, row_amax_out, nullptr, sms, cs(stream));
 }
 
@@ -310,6 +319,12 @@ int sixbit_layernorm_quant(const void* x, int64_t M, int64_t H, int64_t ldx, flo
   c.codes = codes; c.sf = sf; c.g_out = g_out; c.hist = amax_hist; c.headroom = headroom; c.nv_pred = nv_pred;
   c.planes = planes; c.row_scale = row_scale; c.i8_pred = i8_pred; c.pred = pred;
   return launch_ln_quant(c, sms, cs(stream));
+}
+
+int sixbit_debug_stall_gemm(int on) {
+  int sms;
+  if (device_setup(&sms, nullptr) != kOk) return kELaunch;
+  return set_gemm_stall(on ? 1 : 0);
 }
 
 int sixbit_get_error(sixbit_stream_t stream) {

@@ -52,6 +52,16 @@
 #include "kernels.h"
 
 namespace sixbit {
+
+// Test switch (set through sixbit_debug_stall_gemm): nonzero makes the MMA
+// issuer of every GEMM launched afterwards wait on a barrier that is never
+// signalled, so its bounded wait expires and the device-error path runs.
+__device__ int g_sixbit_stall_mma = 0;
+
+int set_gemm_stall(int on) {
+  return cudaMemcpyToSymbol(g_sixbit_stall_mma, &on, sizeof(on)) == cudaSuccess ? kOk : kELaunch;
+}
+
 namespace {
 
 constexpr int BM = 128;
@@ -63,7 +73,10 @@ constexpr uint32_t kSpinCap = 1u << 22;  // polls of a bounded mbarrier wait
 constexpr uint32_t kTmemCols = 512;
 
 #ifndef GEMM_PAIR
-#define GEMM_PAIR false  // true: CTA pairs with cta_group::2 MMAs (256 x 256 tiles)
+#define GEMM_PAIR false  // W4A8: true = CTA pairs with cta_group::2 MMAs (256 x 256 tiles)
+#endif
+#ifndef W4A4_PAIR
+#define W4A4_PAIR true   // W4A4: CTA pairs (each CTA streams half of W: ~145 instead of ~206 GB/s per SM)
 #endif
 #ifndef W4A8_NC
 #define W4A8_NC 1
@@ -238,8 +251,12 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
+// Arrival on a barrier of the other CTA of a pair.  The default semantics
+// (release at CTA scope) keep the issuing thread's cost near 60 ns; the
+// cluster-scope release form stalled the issuing thread for 280-440 ns.
+// Callers order their tcgen05 work first (tcgen05.wait + fence).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
@@ -372,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // barriers: full[S] empty[S] sfready[R] tfull tempty drain resid[8] sffull[R] sfempty[R], R = kSfSlots
   constexpr int R = C::kSfSlots;
   uint64_t* bars = reinterpret_cast<uint64_t*>(extra);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 3 * R + 11);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 3 * R + 12);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -387,10 +404,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto resid_bar = [&](int w) { return bar0 + 8u * uint32_t(2 * STAGES + R + 3 + w); };
   auto sffull_bar = [&](int s) { return bar0 + 8u * uint32_t(2 * STAGES + R + 11 + s); };   // ring only
   auto sfempty_bar = [&](int s) { return bar0 + 8u * uint32_t(2 * STAGES + 2 * R + 11 + s); };
+  const uint32_t never_bar = bar0 + 8u * uint32_t(2 * STAGES + 3 * R + 11);   // initialised, never arrived on
   // Arrival on a barrier of the issuing CTA (rank 0): local, or across the pair.
   auto arrive_leader = [&](uint32_t bar) {
-    if constexpr (PAIR) mbar_arrive_remote(map_rank(bar, 0));
-    else mbar_arrive(bar);
+    if constexpr (PAIR) {
+      if (rank == 0) mbar_arrive(bar);
+      else mbar_arrive_remote(map_rank(bar, 0));
+    } else {
+      mbar_arrive(bar);
+    }
   };
   constexpr int kCtas = PAIR ? 2 : 1;
 
@@ -410,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(tempty_bar, 8 * kCtas);          // one arrival per epilogue warp of the pair
     mbar_init(drain_bar, 1);
     for (int w = 0; w < 8; ++w) mbar_init(resid_bar(w), 1);
+    mbar_init(never_bar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_tmap(&tmA);
@@ -453,6 +476,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0, slot = 0;
     uint32_t phase = 0, sphase = 0, acc_phase = 0;
     bool ok = true;
+    if (g_sixbit_stall_mma) {
+      // Test switch: wait for an arrival that never comes, so the bounded wait
+      // gives up and the abort path (error word, drain, TMEM release) runs.
+      if (!mbar_wait<PAIR>(never_bar, 0, abort_flag)) { fail(); ok = false; }
+    }
     for (int tile = blockIdx.x / kCtas; tile < ntiles && ok; tile += gridDim.x / kCtas) {
       // the epilogue warps (of both CTAs) have pulled the previous tile out of TMEM
       if (!mbar_wait<PAIR>(tempty_bar, acc_phase ^ 1u, abort_flag)) { fail(); ok = false; break; }
@@ -474,6 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < C::kMmaK; ++j) {
             const int a = c * C::kMmaK + j;            // MMA index within the stage = scale atom index
+            if ((kt * NC * C::kMmaK + a) * 64 >= p.K) continue;   // all 64 elements past K (zero fill)
             const uint64_t bdesc = bdesc_s0 + soff + uint64_t((c * C::kChunkB + 32 * j) >> 4);
             const uint32_t sfb = sfb_t + 4 * C::kRT * a;
             if (MODE == 0) {
@@ -659,6 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stg_s = smem_u32(stg);
     const uint32_t rbar = resid_bar(ew);
     uint32_t acc_phase = 0, r_phase = 0;
+    bool r_pending = false;                      // a residual load issued and not yet seen landed
     bool ok = true;
     const float gw = *p.g_w;
     const float gscale = MODE == 0 ? __fmul_rn(*p.g_a, gw) : gw;
@@ -760,11 +790,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_expect_tx(rbar, 4096);
               tma_load_2d(stg_s, &tmR, n0, m0, rbar);   // rows >= M and columns >= N read as 0
             }
+            r_pending = true;
             if (!__all_sync(0xffffffffu, mbar_wait(rbar, r_phase, abort_flag))) {
               if (lane == 0) fail();
               ok = false;
               break;
             }
+            r_pending = false;
             r_phase ^= 1u;
           }
 #pragma unroll
@@ -877,6 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (r_pending) mbar_wait(rbar, r_phase, nullptr);   // an aborted tile's residual load has landed
     if (lane == 0) bulk_wait0();                 // this warp's output stores are complete
     if (qo) {
       const float a = warp_max(__uint_as_float(max(q_run & 0xFFFFu, q_run >> 16) << 16));
@@ -1053,11 +1086,11 @@ int launch_gemm_fp4(const GemmCall& c, int num_sms, cudaStream_t s) {
   // when not taken, slowed the plain epilogue (the critical path of the
   // K = 1920 layers) by 5-10%.
   if (c.q_hist) {
-    if (c.mode == 0) return run<256, 0, GEMM_PAIR ? 5 : 3, 128, 1, GEMM_PAIR, true>(c, num_sms, s);
+    if (c.mode == 0) return run<256, 0, W4A4_PAIR ? 5 : 3, 128, 1, W4A4_PAIR, true>(c, num_sms, s);
     return chunked ? run<256, 1, W4A8_STAGES, 64, W4A8_NC, GEMM_PAIR, true>(c, num_sms, s)
                    : run<256, 1, W4A8_STAGES, 64, 1, GEMM_PAIR, true>(c, num_sms, s);
   }
-  if (c.mode == 0) return run<256, 0, GEMM_PAIR ? 5 : 3, 128, 1, GEMM_PAIR, false>(c, num_sms, s);
+  if (c.mode == 0) return run<256, 0, W4A4_PAIR ? 5 : 3, 128, 1, W4A4_PAIR, false>(c, num_sms, s);
   return chunked ? run<256, 1, W4A8_STAGES, 64, W4A8_NC, GEMM_PAIR, false>(c, num_sms, s)
                  : run<256, 1, W4A8_STAGES, 64, 1, GEMM_PAIR, false>(c, num_sms, s);
 }

@@ -96,5 +96,7 @@ struct GemmCall {
   const uint8_t* q_pred;
 };
 int launch_gemm_fp4(const GemmCall& c, int num_sms, cudaStream_t s);
+// Test switch of the GEMM's abort path (see sixbit_debug_stall_gemm).
+int set_gemm_stall(int on);
 
 }  // namespace sixbit

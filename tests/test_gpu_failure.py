@@ -1,0 +1,68 @@
+"""The device-error path of the linear layers, made to run on purpose.
+
+Every mbarrier wait in the GEMM is bounded.  The test switch
+sixbit_debug_stall_gemm(1) makes the MMA-issuing thread wait on a barrier
+that nothing signals, so that wait gives up after its normal poll cap: the
+kernel must record SIXBIT_EDEVICE, stop its other roles, wait for its own
+copies and MMAs in flight, free its tensor memory and exit.  The host then
+reads the error through sixbit_get_error(), and the next normal call on the
+same stream must run and match the oracle.  No fault or hang is involved:
+the wait that expires is the kernel's own bounded one."""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+from oracle import codecs, gemm as o_gemm, int8 as o_int8, nvfp4 as o_nvfp4
+from tests.helpers import assert_gemm_close, dev, dev_bf16, host
+
+pytestmark = pytest.mark.gpu
+
+
+def _layer(residual):
+    import nvfp4_int8_mixed_gb300 as sb
+    M, K, N = 300, 256, 512                               # two 256-row CTA-pair tiles, a ragged M tail
+    lay = synthetic.gemm_layer(21, M, K, N, residual)
+    x = dev_bf16(lay["a"])
+    wc, wsf, gw = sb.quantize_weight_nvfp4(dev(lay["w"]))
+    codes, sf, ga = sb.quantize_act_nvfp4(x)
+    _, planes, s = sb.quantize_act_int8(x, want_q=False)
+    r = dev_bf16(lay["residual"]) if residual else None
+    return lay, x, r, (wc, wsf, gw), (codes, sf, ga), (planes, s)
+
+
+@pytest.mark.parametrize("residual", [False, True])
+def test_expired_wait_reports_edevice_then_the_next_call_is_clean(residual):
+    import nvfp4_int8_mixed_gb300 as sb
+    lib = sb.lib()
+    lay, x, r, (wc, wsf, gw), (codes, sf, ga), (planes, s) = _layer(residual)
+    stream = sb._stream()
+    assert lib.sixbit_get_error(stream) == sb.OK            # nothing pending before the test
+    y = torch.empty((x.shape[0], wc.shape[0]), dtype=torch.bfloat16, device="cuda")
+    assert lib.sixbit_debug_stall_gemm(1) == sb.OK
+    try:
+        for run in (lambda: sb.qlinear_w4a4(codes, sf, ga, wc, wsf, gw, residual=r, out=y),
+                    lambda: sb.qlinear_w4a8(planes, s, wc, wsf, gw, residual=r, out=y)):
+            t0 = time.perf_counter()
+            run()                                          # the launch itself succeeds
+            rc = lib.sixbit_get_error(stream)
+            dt = time.perf_counter() - t0
+            assert rc == sb.EDEVICE, rc
+            assert dt < 60.0, dt                           # the wait gave up in bounded time
+            print(f"expired wait reported after {dt:.2f} s")
+            assert lib.sixbit_get_error(stream) == sb.OK   # reading the error cleared it
+    finally:
+        assert lib.sixbit_debug_stall_gemm(0) == sb.OK
+    # the same stream runs normal layers again, with correct results
+    af = codecs.bf16_to_f32(lay["a"])
+    rwc, rwsf, rgw, _ = o_nvfp4.quantize(lay["w"])
+    rac, rasf, rga, _ = o_nvfp4.quantize(af)
+    rq, rs, _ = o_int8.quantize(af)
+    y4 = sb.qlinear_w4a4(codes, sf, ga, wc, wsf, gw, residual=r, out_dtype=torch.float32)
+    y8 = sb.qlinear_w4a8(planes, s, wc, wsf, gw, residual=r, out_dtype=torch.float32)
+    assert lib.sixbit_get_error(stream) == sb.OK
+    res = lay["residual"] if residual else None
+    assert_gemm_close(host(y4), o_gemm.w4a4(rac, rasf, rga, rwc, rwsf, rgw, residual=res), "f32")
+    assert_gemm_close(host(y8), o_gemm.w4a8(rq, rs, rwc, rwsf, rgw, residual=res), "f32")

@@ -52,36 +52,58 @@ def layernorm(x_bits, eps: float = LN_EPS):
     return f64_to_bf16((x - mu) / np.sqrt(var + eps))
 
 
-def quantize_weights(w_f32):
-    codes, sf, g, _ = nvfp4.quantize(np.asarray(w_f32, dtype=np.float32))
-    return dict(codes=codes, sf=sf, g=g)
+def quantize_weights(w_f32, chunk_rows=None, keep_dequantized=False):
+    """NVFP4 weight: codes, scale bytes, g.  chunk_rows: quantize that many
+    rows at a time with the whole matrix's amax (the same result, less
+    memory for large matrices).  keep_dequantized: also keep the decoded
+    float64 matrix ("deq") for repeated products."""
+    w = np.asarray(w_f32, dtype=np.float32)
+    if chunk_rows is None:
+        codes, sf, g, _ = nvfp4.quantize(w)
+    else:
+        amax = nvfp4.tensor_amax(w)
+        parts = [nvfp4.quantize(w[i:i + chunk_rows], amax) for i in range(0, w.shape[0], chunk_rows)]
+        codes = np.concatenate([p[0] for p in parts])
+        sf = np.concatenate([p[1] for p in parts])
+        g = parts[0][2]
+    wq = dict(codes=codes, sf=sf, g=g)
+    if keep_dequantized:
+        wq["deq"] = nvfp4.dequantize(codes, sf)
+    return wq
 
 
 def qlinear(h_bits, wq, use_nvfp4: bool, gelu=False, residual=None, amax_t=None):
-    """amax_t: the NVFP4 tensor amax to quantize with (None: the input's own)."""
+    """amax_t: the NVFP4 tensor amax to quantize with (None: the input's own;
+    given when h_bits is a row subset of the layer's whole input)."""
     h = bf16_to_f32(h_bits)
     if use_nvfp4:
         codes, sf, g, _ = nvfp4.quantize(h, amax_t)
         return gemm.w4a4(codes, sf, g, wq["codes"], wq["sf"], wq["g"], gelu=gelu,
-                         residual=residual, out_dtype="bf16")
+                         residual=residual, out_dtype="bf16", w_deq=wq.get("deq"))
     q, s, _ = int8.quantize(h)
     return gemm.w4a8(q, s, wq["codes"], wq["sf"], wq["g"], gelu=gelu,
-                     residual=residual, out_dtype="bf16")
+                     residual=residual, out_dtype="bf16", w_deq=wq.get("deq"))
 
 
-def block_forward(x_bits, wq_block, flags, amax_hist=None, headroom=2.0):
+def block_forward(x_bits, wq_block, flags, amax_hist=None, headroom=2.0, layer_amax=None):
     """flags: 4 uint8 (qkv, out, up, down); 1 = NVFP4.
 
     amax_hist (fused producers): float32 [3] history of the tensor amaxes of
     h1, h2, u; their NVFP4 layers quantize with headroom * history, and the
-    array is overwritten with this call's exact amaxes."""
+    array is overwritten with this call's exact amaxes.
+    layer_amax (unfused, optional): the NVFP4 tensor amaxes of the four layer
+    inputs (h1, v, h2, u) when x_bits is a row subset of the block input:
+    the one quantity of the block that is not computed row by row."""
     H = x_bits.shape[1]
     fused = amax_hist is not None
     used = [F32(F32(headroom) * F32(a)) for a in amax_hist] if fused else [None] * 3
+    la = [None] * 4 if layer_amax is None else [F32(a) for a in layer_amax]
+    if not fused and layer_amax is not None:
+        used = [la[0], la[2], la[3]]
     h1 = layernorm(x_bits)
     qkv = qlinear(h1, wq_block["qkv"], bool(flags[0]), amax_t=used[0])
     v = np.ascontiguousarray(qkv[:, 2 * H:3 * H])
-    x1 = qlinear(v, wq_block["out"], bool(flags[1]), residual=x_bits)
+    x1 = qlinear(v, wq_block["out"], bool(flags[1]), residual=x_bits, amax_t=la[1])
     h2 = layernorm(x1)
     u = qlinear(h2, wq_block["up"], bool(flags[2]), gelu=True, amax_t=used[1])
     out = qlinear(u, wq_block["down"], bool(flags[3]), residual=x1, amax_t=used[2])

@@ -49,18 +49,21 @@ def epilogue(acc, bias=None, gelu=False, residual=None, out_dtype="f32"):
     raise ValueError(out_dtype)
 
 
-def w4a4(a_codes, a_sf, g_a, w_codes, w_sf, g_w, bias=None, gelu=False, residual=None, out_dtype="f32"):
-    """a_codes [M,K/2], a_sf [M,K/16] (plain layout), w likewise with N rows."""
+def w4a4(a_codes, a_sf, g_a, w_codes, w_sf, g_w, bias=None, gelu=False, residual=None, out_dtype="f32",
+         w_deq=None):
+    """a_codes [M,K/2], a_sf [M,K/16] (plain layout), w likewise with N rows.
+    w_deq (optional): nvfp4.dequantize(w_codes, w_sf) computed once by the
+    caller, for repeated products with one weight."""
     A = nvfp4.dequantize(a_codes, a_sf)             # float64, without g
-    W = nvfp4.dequantize(w_codes, w_sf)
+    W = nvfp4.dequantize(w_codes, w_sf) if w_deq is None else w_deq
     acc = (A @ W.T) * (float(g_a) * float(g_w))
     return epilogue(acc, bias, gelu, residual, out_dtype)
 
 
-def w4a8(q, s_a, w_codes, w_sf, g_w, bias=None, gelu=False, residual=None, out_dtype="f32"):
-    """q int8 [M,K], s_a float32 [M]; w codes/scales as in w4a4."""
+def w4a8(q, s_a, w_codes, w_sf, g_w, bias=None, gelu=False, residual=None, out_dtype="f32", w_deq=None):
+    """q int8 [M,K], s_a float32 [M]; w codes/scales (and w_deq) as in w4a4."""
     A = np.asarray(q, dtype=np.float64)
-    W = nvfp4.dequantize(w_codes, w_sf)
+    W = nvfp4.dequantize(w_codes, w_sf) if w_deq is None else w_deq
     acc = (A @ W.T) * (np.asarray(s_a, dtype=np.float64)[:, None] * float(g_w))
     return epilogue(acc, bias, gelu, residual, out_dtype)
 

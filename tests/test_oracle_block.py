@@ -85,3 +85,39 @@ def test_block_out_proj_reads_the_v_slice():
     out_v = block.block_forward(x, dict(base, qkv=block.quantize_weights(w_v)), [1, 1, 1, 1])
     assert np.array_equal(out_qk, x)
     assert not np.array_equal(out_v, x)
+
+
+def test_chunked_weight_quantization_and_dequantized_cache_change_nothing():
+    rng = np.random.default_rng(3)
+    w = (0.02 * rng.standard_normal((300, 128))).astype(np.float32)
+    full = block.quantize_weights(w)
+    chunked = block.quantize_weights(w, chunk_rows=128, keep_dequantized=True)
+    assert np.array_equal(full["codes"], chunked["codes"]) and np.array_equal(full["sf"], chunked["sf"])
+    assert full["g"] == chunked["g"]
+    h = codecs.f32_to_bf16(rng.standard_normal((9, 128)).astype(np.float32))
+    for nv in (True, False):
+        assert np.array_equal(block.qlinear(h, full, nv, gelu=True), block.qlinear(h, chunked, nv, gelu=True))
+
+
+def test_block_on_a_row_subset_with_the_full_tensor_amaxes():
+    # Only the NVFP4 tensor amaxes couple the rows of a block: given the
+    # whole tensors' amaxes, a row subset reproduces those rows exactly.
+    from oracle import nvfp4
+    st = synthetic.stack_setup(5, 1, 64, 128)
+    wq = {k: block.quantize_weights(v) for k, v in st["blocks"][0].items()}
+    x = synthetic.stack_inputs(st["noise_seed"], 96, 64, 1)[0]
+    flags = np.array([1, 1, 1, 1], np.uint8)
+    full = block.block_forward(x, wq, flags)
+    # the full block's layer inputs, rebuilt step by step to take their amaxes
+    h1 = block.layernorm(x)
+    qkv = block.qlinear(h1, wq["qkv"], True)
+    v = np.ascontiguousarray(qkv[:, 128:192])
+    x1 = block.qlinear(v, wq["out"], True, residual=x)
+    h2 = block.layernorm(x1)
+    u = block.qlinear(h2, wq["up"], True, gelu=True)
+    amax = [nvfp4.tensor_amax(codecs.bf16_to_f32(t)) for t in (h1, v, h2, u)]
+    rows = np.array([0, 7, 50, 95])
+    sub = block.block_forward(x[rows], wq, flags, layer_amax=amax)
+    assert np.array_equal(sub, full[rows])
+    # without them the subset takes its own (smaller) amaxes and differs
+    assert not np.array_equal(block.block_forward(x[rows], wq, flags), full[rows])

@@ -84,26 +84,76 @@ def job_throughput(units_per_rank: float, ws: int, elapsed_max: float) -> float:
 
 def gemm_roofline(mode: str, M: int, N: int, K: int, residual: bool, seconds: float,
                   fp4_peak_tflops: float, hbm_gbs: float) -> dict:
-    """Roofline of one quantized-linear launch: min(tensor ceiling, HBM x AI).
+    """Roofline of one quantized-linear launch against the method's own work.
 
-    Algorithmic bytes: the activation operand (W4A4: E2M1 codes + E4M3 block
-    scales; W4A8: three digit planes + fp32 row scales), the NVFP4 weight
-    (codes + scales), the bf16 output and, with a residual, its bf16 read.
-    W4A8 issues three FP4 MMAs per product, so its tensor ceiling is a third
-    of the FP4 peak."""
+    FLOPs: 2MNK.  Algorithmic bytes: the activation operand in the method's
+    format (W4A4: E2M1 codes + E4M3 block scales; W4A8: int8 codes + fp32 row
+    scales), the NVFP4 weight (codes + scales), the bf16 output and, with a
+    residual, its bf16 read.  Ceiling: min(dense FP4 tensor peak, HBM x AI).
+    W4A8 runs on the FP4 pipe as three exact digit-plane MMAs per product,
+    so its `fp4_pipe_frac` (3 x its FLOP rate / FP4 peak) is how busy that
+    pipe is, and `design_ceiling` = FP4 peak / 3 is the most this design can
+    reach; `bytes_moved` counts the digit planes (1.5 B/element) it streams
+    instead of the 1-byte codes."""
     flops = 2.0 * M * N * K
-    a_bytes = 3 * M * K / 2 + 4 * M if mode == "w4a8" else M * K / 2 + M * K / 16
     w_bytes = N * K / 2 + N * K / 16
     y_bytes = 2.0 * M * N * (2 if residual else 1)
+    if mode == "w4a8":
+        a_bytes, a_moved = M * K + 4 * M, 1.5 * M * K + 4 * M
+    else:
+        a_bytes = a_moved = M * K / 2 + M * K / 16
     nbytes = a_bytes + w_bytes + y_bytes
     ai = flops / nbytes
-    tensor = fp4_peak_tflops / (3.0 if mode == "w4a8" else 1.0)
     hbm = hbm_gbs * ai / 1e3                    # GB/s x FLOP/B -> TFLOP/s
-    ceiling = min(tensor, hbm)
+    ceiling = min(fp4_peak_tflops, hbm)
     achieved = flops / seconds / 1e12
-    return {"ms": seconds * 1e3, "TFLOP/s": achieved, "bytes": nbytes, "AI": ai,
-            "bound": "tensor" if tensor <= hbm else "hbm", "ceiling": ceiling,
-            "frac_ceiling": achieved / ceiling, "frac_tensor": achieved / tensor}
+    r = {"ms": seconds * 1e3, "TFLOP/s": achieved, "bytes": nbytes, "bytes_moved": a_moved + w_bytes + y_bytes,
+         "AI": ai, "bound": "tensor" if fp4_peak_tflops <= hbm else "hbm", "ceiling": ceiling,
+         "frac_ceiling": achieved / ceiling, "frac_fp4_peak": achieved / fp4_peak_tflops}
+    if mode == "w4a8":
+        r["fp4_pipe_frac"] = 3.0 * achieved / fp4_peak_tflops
+        r["design_ceiling"] = fp4_peak_tflops / 3.0
+    return r
+
+
+def quant_bytes(kind: str, M: int, K: int) -> float:
+    """Algorithmic bytes of an activation quantizer over [M, K]: read bf16 x
+    once, write the method's format (NVFP4: 0.5 B codes + 1/16 B E4M3 scales
+    per element; INT8: 1 B codes per element + a 4-byte row scale)."""
+    if kind == "nvfp4":
+        return (2 + 0.5 + 1 / 16) * M * K
+    return 3.0 * M * K + 4.0 * M
+
+
+def stack_ideal_seconds(M: int, H: int, F: int, nv_computed, i8_computed, computed, skipped,
+                        fp4_peak_tflops: float, hbm_gbs: float) -> float:
+    """Sum of per-kernel roofline times of a DiT stack run (the time-weighted
+    bound): for every computed block evaluation two LayerNorms (bf16 in and
+    out, with their amax side outputs), per layer the quantizer of its format
+    (NVFP4: the V slice's own amax pass, then 2.5625 B/element; INT8:
+    3 B/element) and its GEMM at min(FP4 peak, HBM x AI) (W4A8 at a third of
+    the FP4 peak: its three digit-plane MMAs), the Gamma/Delta pass (8 B per
+    element); for a skipped block the TDC reuse (6 B/element) and the Gamma
+    pass.  nv_computed / i8_computed: per layer kind (qkv, out, up, down) the
+    number of computed evaluations in that format; computed / skipped: block
+    evaluation counts."""
+    shapes = {"qkv": (H, 3 * H, False), "out": (H, H, True), "up": (H, F, False), "down": (F, H, True)}
+    t = 0.0
+    for k, (K, N, res) in shapes.items():
+        for mode, count in (("w4a4", nv_computed[k]), ("w4a8", i8_computed[k])):
+            if not count:
+                continue
+            g = gemm_roofline(mode, M, N, K, res, 1.0, fp4_peak_tflops, hbm_gbs)
+            tensor = fp4_peak_tflops / (3.0 if mode == "w4a8" else 1.0)
+            gemm_s = 2.0 * M * N * K / (min(tensor, g["ceiling"]) * 1e12)
+            qb = quant_bytes("nvfp4" if mode == "w4a4" else "int8", M, K)
+            if mode == "w4a4" and k == "out":
+                qb += 2.0 * M * K                  # the V slice's tensor amax pass (no producer supplies it)
+            t += count * (gemm_s + qb / (hbm_gbs * 1e9))
+    ln = 2 * (4.0 * M * H)                        # two LayerNorms, bf16 in and out
+    t += computed * (ln + 8.0 * M * H) / (hbm_gbs * 1e9)
+    t += skipped * (6.0 * M * H + 8.0 * M * H) / (hbm_gbs * 1e9)
+    return t
 
 
 # ---------------------------------------------------------------- clocks
@@ -320,7 +370,7 @@ def time_producers(sb, L, dev, gpair, reps=20):
         "gamma_delta_mx_cache": (lambda: gamma_call(mcache), 4 * elt + 2 * int(sb.lib().sixbit_mxcache_bytes(elt))),
         "layernorm_bf16": (lambda: sb.layernorm(x, out=y), 4 * elt),
         "layernorm_nvfp4": (lambda: sb.layernorm_quant(x, nvfp4=(codes, sf, g), amax_hist=hist[0]), 2.5625 * elt),
-        "layernorm_int8": (lambda: sb.layernorm_quant(x, int8=(planes, rs)), 3.5 * elt + 4 * M),
+        "layernorm_int8": (lambda: sb.layernorm_quant(x, int8=(planes, rs)), quant_bytes("int8", M, H)),
         "layernorm_bf16_nvfp4": (lambda: sb.layernorm_quant(x, y=y, nvfp4=(codes, sf, g), amax_hist=hist[0]),
                                  4.5625 * elt),
         "qout_w4a4[ffn_up]": (lambda: sb.qlinear_qout("w4a4", up["codes"], up["wc"], up["wsf"], up["gw"], qc, qsf, qg,
@@ -416,7 +466,7 @@ def bf16_stack_context(weights, xs, H):
     return {"blocks_per_s": len(weights) * len(xs) / sec, "ms_per_step": sec / len(xs) * 1e3}
 
 
-def run_stack_bench(name: str, dev, cpu_oracle: bool = False):
+def run_stack_bench(name: str, dev, cpu_oracle: bool = False, modes=None):
     """Blocks/s of the synthetic DiT stack with DMPQ+TDC and with DMPQ only.
 
     Weights N(0, 0.02) and the input drift x_t = x_{t-1} + sigma_t N(0,1)
@@ -431,11 +481,18 @@ def run_stack_bench(name: str, dev, cpu_oracle: bool = False):
     the next layer's NVFP4 / INT8 input; delayed NVFP4 scaling), and the
     "_mxcache" modes: the update cache stored as E4M3 codes with a
     power-of-two scale per 32 elements.  Timed: every step's graph replay
-    plus its input copy."""
+    plus its input copy.  modes: the subset of modes to run (None = all).
+    Each mode also reports `roofline_frac`: the sum of its kernels' roofline
+    times (stack_ideal_seconds, from the formats and skips it actually ran)
+    over the measured time."""
     import torch
     from nvfp4_int8_mixed_gb300 import lib as _lib
-    from nvfp4_int8_mixed_gb300.stack import DiTStack, calibrate_lines, calibrate_tau
+    from nvfp4_int8_mixed_gb300.calibration import calibrate_lines, calibrate_tau
+    from nvfp4_int8_mixed_gb300.stack import DiTStack
     sb_mx_bytes = lambda n: _lib().sixbit_mxcache_bytes(n)
+    peaks, _ = load_peaks()
+    fp4_peak = float(peaks["bf16_tflops"]) * FP4_OVER_BF16
+    hbm = float(peaks["hbm_gbs"])
     c = STACKS[name]
     nb, M, H, F, T = c["n_blocks"], c["M"], c["H"], c["F"], c["steps"]
     gen = torch.Generator(device=dev).manual_seed(c["seed"])
@@ -460,7 +517,9 @@ def run_stack_bench(name: str, dev, cpu_oracle: bool = False):
     runs = [("dmpq_tdc", 1, 0, None), ("dmpq_only", 0, 0, None), ("pdr_skip2_refresh4", 2, 4, None),
             ("dmpq_tdc_fused_quant", 1, 0, None), ("dmpq_tdc_mxcache", 1, 0, None),
             ("dmpq_tdc_fused_quant_mxcache", 1, 0, None)]
-    if c.get("calib_steps"):
+    if modes is not None:
+        runs = [r for r in runs if r[0] in modes]
+    if c.get("calib_steps") and (modes is None or "measured_lines" in modes):
         cal = calibrate_lines(stack, xs, weights, steps=c["calib_steps"])
         lines = (cal["alpha"].astype(np.float32), cal["beta"].astype(np.float32))
         fin = lambda a: float(np.nanmean(a))
@@ -487,8 +546,9 @@ def run_stack_bench(name: str, dev, cpu_oracle: bool = False):
         stack.reset()
         stack.capture()
         stack.reset()
-        skips = torch.zeros(nb, dtype=torch.int32, device=dev)
-        nv = torch.zeros(4 * nb, dtype=torch.int32, device=dev)
+        comp = torch.zeros(nb, dtype=torch.int32, device=dev)
+        nv = torch.zeros(4 * nb, dtype=torch.int32, device=dev)      # NVFP4 flags of computed blocks
+        nv_all = torch.zeros(4 * nb, dtype=torch.int32, device=dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         e0.record()
@@ -496,14 +556,24 @@ def run_stack_bench(name: str, dev, cpu_oracle: bool = False):
             stack.x_in.copy_(xs[t])
             stack.step_dev.fill_(t)
             stack.graph.replay()
-            skips += (1 - stack.cflag).int()
-            nv += stack.use_nvfp4.int()
+            cf = stack.cflag.int()
+            comp += cf
+            nv += stack.use_nvfp4.int() * cf.repeat_interleave(4)
+            nv_all += stack.use_nvfp4.int()
         e1.record()
         torch.cuda.synchronize()
         sec = e0.elapsed_time(e1) / 1e3
+        comp_h = comp.cpu().numpy()
+        nv_k = nv.view(nb, 4).sum(0).cpu().numpy()
+        comp_total = int(comp_h.sum())
+        kinds = ("qkv", "out", "up", "down")
+        ideal = stack_ideal_seconds(M, H, F, {k: int(nv_k[i]) for i, k in enumerate(kinds)},
+                                    {k: comp_total - int(nv_k[i]) for i, k in enumerate(kinds)},
+                                    comp_total, nb * T - comp_total, fp4_peak, hbm)
         res[mode] = {"blocks_per_s": nb * T / sec, "ms_per_step": sec / T * 1e3,
-                     "skipped_fraction": float(skips.sum()) / (nb * T),
-                     "nvfp4_fraction_after_step0": float(nv.sum()) / (4 * nb * (T - 1))}
+                     "skipped_fraction": 1.0 - comp_total / (nb * T),
+                     "nvfp4_fraction_after_step0": float(nv_all.sum()) / (4 * nb * (T - 1)),
+                     "roofline_frac": ideal / sec, "roofline_ideal_ms_per_step": ideal / T * 1e3}
     # HBM footprint of the quantized stack vs a bf16 one (weights, TDC cache, block activations)
     w_params = nb * (3 * H * H + H * H + 2 * F * H)
     w_nvfp4 = sum(int(t.numel() * t.element_size()) for b in stack.wq for wl in b.values() for t in wl)
@@ -519,6 +589,226 @@ def run_stack_bench(name: str, dev, cpu_oracle: bool = False):
 
 
 # ---------------------------------------------------------------- our arm
+def setup_gemm_set(sb, workload: str, dev):
+    """Device inputs of one GEMM-set step (untimed): per layer the bf16
+    activations (and residual), the weights quantized once, and the
+    quantizer / GEMM outputs; plus a block input/output pair for the
+    Gamma / DMPQ / TDC tail.  Seeds: 1 for the 2B set, 2 for the 5B set."""
+    import torch
+    layers = workload_layers(workload)
+    M = synthetic.M_2B
+    H = layers[0][1]
+    seed = 1 if workload == "2b" else 2
+    to_dev = lambda bits: torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    L, host_inputs = [], []
+    for name, K, N, gelu, res in layers:
+        lay = synthetic.gemm_layer(seed, M, K, N, res)
+        x = to_dev(lay["a"])
+        r = to_dev(lay["residual"]) if res else None
+        wc, wsf, gw = sb.quantize_weight_nvfp4(torch.from_numpy(lay["w"]).to(dev))
+        L.append(dict(name=name, K=K, N=N, gelu=gelu, x=x, r=r, wc=wc, wsf=wsf, gw=gw,
+                      codes=torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
+                      sf=torch.empty(sb.sf_bytes(M, K), dtype=torch.uint8, device=dev),
+                      ga=torch.empty(1, dtype=torch.float32, device=dev),
+                      planes=torch.empty((3, M, K // 2), dtype=torch.uint8, device=dev),
+                      s=torch.empty(M, dtype=torch.float32, device=dev),
+                      y4=torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+                      y8=torch.empty((M, N), dtype=torch.bfloat16, device=dev)))
+        host_inputs.append((lay["a"], lay["residual"]))
+    gp = synthetic.gamma_pair(7, M, H)
+    tail = dict(bin=to_dev(gp["xin"]), bout=to_dev(gp["xout"]), delta=to_dev(gp["delta_prev"]),
+                gamma=torch.zeros(4, dtype=torch.float32, device=dev),
+                state=torch.tensor([1, 0], dtype=torch.int32, device=dev),
+                step=torch.ones(1, dtype=torch.int32, device=dev),
+                alpha=torch.linspace(0.5, 1.5, 4, device=dev), beta=torch.full((4,), 0.005, device=dev),
+                lb=torch.zeros(4, dtype=torch.int32, device=dev), flags=torch.empty(4, dtype=torch.uint8, device=dev),
+                gates=torch.empty((4, 2), dtype=torch.uint8, device=dev),
+                cflag=torch.empty(1, dtype=torch.uint8, device=dev))
+    tail["tdc_out"] = torch.empty_like(tail["bin"])
+    sb.workspace(int(sb.lib().sixbit_workspace_size(M * H, 1)))
+    return dict(L=L, M=M, H=H, layers=layers, tail=tail, gp=gp, host_inputs=host_inputs)
+
+
+def gemm_set_step(sb, G):
+    """step(evs=None, inp=None): one pass of the path over the set -- per layer
+    tensor amax + NVFP4 quantize -> W4A4 GEMM, INT8 quantize -> W4A8 GEMM --
+    then the Gamma/Delta pass, DMPQ and TDC.  evs: [launch][start, end]
+    events recorded around every call; inp: device inputs to use instead of
+    the defaults ({x, r: per layer, bin, bout})."""
+    import torch
+    L, T = G["L"], G["tail"]
+
+    def step(evs=None, inp=None):
+        cur = torch.cuda.current_stream()        # the capture stream while a graph is being captured
+        k = 0
+        ops = []
+        for li, l in enumerate(L):
+            x = inp["x"][li] if inp else l["x"]
+            r = inp["r"][li] if inp else l["r"]
+            ops += [
+                lambda l=l, x=x: sb.quantize_act_nvfp4(x, out=(l["codes"], l["sf"], l["ga"])),
+                lambda l=l, r=r: sb.qlinear_w4a4(l["codes"], l["sf"], l["ga"], l["wc"], l["wsf"], l["gw"], residual=r,
+                                                 gelu=l["gelu"], out=l["y4"]),
+                lambda l=l, x=x: sb.quantize_act_int8(x, out=(None, l["planes"], l["s"])),
+                lambda l=l, r=r: sb.qlinear_w4a8(l["planes"], l["s"], l["wc"], l["wsf"], l["gw"], residual=r,
+                                                 gelu=l["gelu"], out=l["y8"]),
+            ]
+        b_in, b_out = (inp["bin"], inp["bout"]) if inp else (T["bin"], T["bout"])
+        g = T["gamma"]
+        ops += [
+            lambda: sb.block_gamma(b_in, b_out, delta=T["delta"], gamma_out=g[0:1], r2_out=g[1:2],
+                                   tdc_state=T["state"]),
+            lambda: sb.dmpq_assign(g[0:1], T["alpha"], T["beta"], T["lb"], 0.1, T["step"], use_nvfp4=T["flags"],
+                                   gates=T["gates"]),
+            lambda: sb.tdc_decide_and_apply(b_in, T["delta"], g[1:2], 0.05, 1, T["state"], T["cflag"], T["tdc_out"],
+                                            gates=T["gates"]),
+        ]
+        for op in ops:
+            if evs is not None:
+                evs[k][0].record(cur)
+            op()
+            if evs is not None:
+                evs[k][1].record(cur)
+            k += 1
+
+    names = []
+    for l in L:
+        names += [f"quant_nvfp4[{l['name']}]", f"w4a4[{l['name']}]", f"quant_int8[{l['name']}]", f"w4a8[{l['name']}]"]
+    names += ["gamma_delta", "dmpq", "tdc"]
+    return step, names
+
+
+def time_gemm_set(sb, G, steps: int, warmup: int, ws: int, dev, clocks=False):
+    """Time `steps` steps of the GEMM set: captured as one CUDA graph of the
+    kernels alone, replayed once between CUDA events on the launching stream
+    (barrier + synchronize on both sides, max over ranks).  Per-launch
+    durations come from a second graph of the same steps with timing events
+    around every launch, replayed after the timed region (median over the
+    steps)."""
+    import torch
+    import torch.distributed as dist
+    step, names = gemm_set_step(sb, G)
+    for _ in range(max(warmup, 3)):
+        step()
+    sb.get_error()
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        mk_ev = lambda: torch.cuda.Event(enable_timing=True, external=True)
+        in_graph_events = True
+    except TypeError:
+        in_graph_events = False
+    evs = [[[mk_ev(), mk_ev()] for _ in names] for _ in range(steps)] if in_graph_events else None
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(steps):
+            step()
+    graph_ev = None
+    if in_graph_events:
+        graph_ev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_ev):
+            for i in range(steps):
+                step(evs[i])
+    sampler = None
+    if clocks:
+        props = torch.cuda.get_device_properties(dev)
+        uuid = str(getattr(props, "uuid", ""))
+        sampler = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or str(dev.index)))
+        time.sleep(0.3)
+    stream = torch.cuda.current_stream()
+    barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    graph.replay()
+    t1.record(stream)
+    barrier()
+    clk = sampler.stop() if sampler is not None else None
+    sb.get_error()
+    elapsed = max_over_ranks(t0.elapsed_time(t1) / 1e3, ws, dev)
+    n_ev = steps
+    if graph_ev is not None:
+        graph_ev.replay()
+        torch.cuda.synchronize()
+    else:
+        n_ev = min(steps, 20)
+        evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in names]
+               for _ in range(n_ev)]
+        for i in range(n_ev):
+            step(evs[i])
+        torch.cuda.synchronize()
+    per = {n: [evs[i][k][0].elapsed_time(evs[i][k][1]) / 1e3 for i in range(n_ev)] for k, n in enumerate(names)}
+    mean_t = {n: float(np.median(v)) for n, v in per.items()}
+    del graph, graph_ev
+    return dict(step=step, names=names, elapsed=elapsed, mean_t=mean_t, clocks=clk, in_graph_events=in_graph_events,
+                launches_per_step=len(names) + len(G["L"]))   # + one tensor-amax pass per NVFP4 quantization
+
+
+def gemm_set_report(G, T, fp4_peak: float, hbm: float, workload: str):
+    """Per-kernel roofline figures of one timed GEMM set."""
+    L, M, mean_t = G["L"], G["M"], T["mean_t"]
+    gemm = {}
+    for n in mean_t:
+        if n.startswith("w4a"):
+            l = L[[x["name"] for x in L].index(n.split("[")[1][:-1])]
+            gemm[n] = gemm_roofline(n.split("[")[0], M, l["N"], l["K"], l["r"] is not None, mean_t[n], fp4_peak, hbm)
+    bw = {}
+    for l in L:
+        for kind in ("nvfp4", "int8"):
+            n = f"quant_{kind}[{l['name']}]"
+            nb = quant_bytes(kind, M, l["K"])
+            moved = nb if kind == "nvfp4" else (2 + 1.5) * M * l["K"] + 4 * M
+            bw[n] = {"ms": mean_t[n] * 1e3, "bytes": nb, "GB/s": nb / mean_t[n] / 1e9,
+                     "frac_hbm": nb / mean_t[n] / 1e9 / hbm,
+                     "note": ("tensor amax pass + encode (two launches, no producer amax)" if kind == "nvfp4" else
+                              f"writes the 3 E2M1 digit planes the W4A8 GEMM reads: {moved / nb:.3f}x the bytes")}
+    nb = 8.0 * M * G["H"]
+    bw["gamma_delta"] = {"ms": mean_t["gamma_delta"] * 1e3, "bytes": nb, "GB/s": nb / mean_t["gamma_delta"] / 1e9,
+                         "frac_hbm": nb / mean_t["gamma_delta"] / 1e9 / hbm}
+    pairs = {}
+    for l in L:                                   # quantizer + GEMM back to back on one stream
+        for kind, mode in (("nvfp4", "w4a4"), ("int8", "w4a8")):
+            t = mean_t[f"quant_{kind}[{l['name']}]"] + mean_t[f"{mode}[{l['name']}]"]
+            pairs[f"{mode}[{l['name']}]"] = {"ms": t * 1e3, "TFLOP/s": 2.0 * M * l["N"] * l["K"] / t / 1e12}
+    return {"gemm": gemm, "bandwidth": bw, "quantizer_plus_gemm": pairs, "dmpq_ms": mean_t["dmpq"] * 1e3,
+            "tdc_ms": mean_t["tdc"] * 1e3}
+
+
+def time_nvfp4_amax_given(sb, G, dev, reps=20):
+    """The NVFP4 quantizer's encode pass alone, with the tensor amax supplied
+    (as a producer supplies it), on each distinct K of the set: one launch
+    timed with CUDA events after a 256 MB L2 flush (median of `reps`)."""
+    import torch
+    peak = float(load_peaks()[0]["hbm_gbs"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out, seen = {}, set()
+    for l in G["L"]:
+        if l["K"] in seen:
+            continue
+        seen.add(l["K"])
+        amax, _ = sb.amax(l["x"])
+        fn = lambda l=l, amax=amax: sb.quantize_act_nvfp4(l["x"], amax_in=amax, out=(l["codes"], l["sf"], l["ga"]))
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / 1e3)
+        t = float(np.median(ts))
+        nb = quant_bytes("nvfp4", G["M"], l["K"])
+        out[f"K={l['K']}"] = {"us": t * 1e6, "GB/s": nb / t / 1e9, "frac_hbm": nb / t / 1e9 / peak}
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -534,178 +824,50 @@ def run_ours(args):
         from nvfp4_int8_mixed_gb300 import build as _b
         _b.build()
     sb.lib()
+    peaks, peak_kind = load_peaks()
+    fp4_peak = float(peaks["bf16_tflops"]) * FP4_OVER_BF16
+    hbm = float(peaks["hbm_gbs"])
 
-    layers = workload_layers(args.workload)
-    M = synthetic.M_2B
-    H = layers[0][1]
-    to_dev = lambda bits: torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
-
-    # ---- setup (untimed): inputs in HBM, weights quantized once
-    L = []
-    host_inputs = []
-    for li, (name, K, N, gelu, res) in enumerate(layers):
-        lay = synthetic.gemm_layer(1, M, K, N, res)
-        x = to_dev(lay["a"])
-        r = to_dev(lay["residual"]) if res else None
-        wc, wsf, gw = sb.quantize_weight_nvfp4(torch.from_numpy(lay["w"]).to(dev))
-        L.append(dict(name=name, K=K, N=N, gelu=gelu, x=x, r=r, wc=wc, wsf=wsf, gw=gw,
-                      codes=torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
-                      sf=torch.empty(sb.sf_bytes(M, K), dtype=torch.uint8, device=dev),
-                      ga=torch.empty(1, dtype=torch.float32, device=dev),
-                      planes=torch.empty((3, M, K // 2), dtype=torch.uint8, device=dev),
-                      s=torch.empty(M, dtype=torch.float32, device=dev),
-                      y4=torch.empty((M, N), dtype=torch.bfloat16, device=dev),
-                      y8=torch.empty((M, N), dtype=torch.bfloat16, device=dev)))
-        host_inputs.append((lay["a"], lay["residual"]))
-    gp = synthetic.gamma_pair(7, M, H)
-    bin_, bout, bdelta = to_dev(gp["xin"]), to_dev(gp["xout"]), to_dev(gp["delta_prev"])
-    gamma_t = torch.zeros(4, dtype=torch.float32, device=dev)   # [gamma, r2, ...]
-    state = torch.tensor([1, 0], dtype=torch.int32, device=dev)
-    step_t = torch.ones(1, dtype=torch.int32, device=dev)
-    alpha = torch.linspace(0.5, 1.5, 4, device=dev)
-    beta = torch.full((4,), 0.005, device=dev)
-    lbk = torch.zeros(4, dtype=torch.int32, device=dev)
-    flags = torch.empty(4, dtype=torch.uint8, device=dev)
-    gates = torch.empty((4, 2), dtype=torch.uint8, device=dev)
-    cflag = torch.empty(1, dtype=torch.uint8, device=dev)
-    tdc_out = torch.empty_like(bin_)
-    sb.workspace(int(sb.lib().sixbit_workspace_size(M * H, 1)))
-
+    # ---- headline workload: setup (untimed), then the K timed steps
+    G = setup_gemm_set(sb, args.workload, dev)
+    L, M, layers = G["L"], G["M"], G["layers"]
     flops_layer = [2 * M * l["N"] * l["K"] for l in L]
     flops_step = 2 * sum(flops_layer)
-    names = []
-    for l in L:
-        names += [f"quant_nvfp4[{l['name']}]", f"w4a4[{l['name']}]", f"quant_int8[{l['name']}]", f"w4a8[{l['name']}]"]
-    names += ["gamma_delta", "dmpq", "tdc"]
-    launches_per_step = 4 * 5 + 3      # amax + nvfp4 quant + w4a4 + int8 quant + w4a8 per layer; gamma, dmpq, tdc
+    T = time_gemm_set(sb, G, args.steps, args.warmup, ws, dev, clocks=True)
+    elapsed, mean_t, step = T["elapsed"], T["mean_t"], T["step"]
+    in_graph, launches_step, clocks = T["in_graph_events"], T["launches_per_step"], T["clocks"]
+    value = job_throughput(flops_step * args.steps, ws, elapsed) / 1e12
     stream = torch.cuda.current_stream()
-
-    def step(evs=None, inp=None):
-        """One pass of the path; `inp` (optional) is a set of device inputs
-        {x: [per layer], r: [per layer], bin, bout} to use instead of the defaults."""
-        cur = torch.cuda.current_stream()        # the capture stream while a graph is being captured
-        k = 0
-        for li, l in enumerate(L):
-            x = inp["x"][li] if inp else l["x"]
-            r = inp["r"][li] if inp else l["r"]
-            ops = [
-                lambda: sb.quantize_act_nvfp4(x, out=(l["codes"], l["sf"], l["ga"])),
-                lambda: sb.qlinear_w4a4(l["codes"], l["sf"], l["ga"], l["wc"], l["wsf"], l["gw"], residual=r,
-                                        gelu=l["gelu"], out=l["y4"]),
-                lambda: sb.quantize_act_int8(x, out=(None, l["planes"], l["s"])),
-                lambda: sb.qlinear_w4a8(l["planes"], l["s"], l["wc"], l["wsf"], l["gw"], residual=r,
-                                        gelu=l["gelu"], out=l["y8"]),
-            ]
-            for op in ops:
-                if evs is not None:
-                    evs[k][0].record(cur)
-                op()
-                if evs is not None:
-                    evs[k][1].record(cur)
-                k += 1
-        b_in, b_out = (inp["bin"], inp["bout"]) if inp else (bin_, bout)
-        tail = [
-            lambda: sb.block_gamma(b_in, b_out, delta=bdelta, gamma_out=gamma_t[0:1], r2_out=gamma_t[1:2],
-                                   tdc_state=state),
-            lambda: sb.dmpq_assign(gamma_t[0:1], alpha, beta, lbk, 0.1, step_t, use_nvfp4=flags, gates=gates),
-            lambda: sb.tdc_decide_and_apply(b_in, bdelta, gamma_t[1:2], 0.05, 1, state, cflag, tdc_out, gates=gates),
-        ]
-        for op in tail:
-            if evs is not None:
-                evs[k][0].record(cur)
-            op()
-            if evs is not None:
-                evs[k][1].record(cur)
-            k += 1
-
-    for _ in range(max(args.warmup, 3)):
-        step()
-    sb.get_error()
 
     def barrier():
         if ws > 1:
             dist.barrier()
         torch.cuda.synchronize()
 
-    # ---- device-resident timing (headline value): the K timed steps captured
-    # as one CUDA graph and replayed once, so Python enqueue cost never starves
-    # the GPU.  The timed graph holds the kernels alone; per-kernel durations
-    # come from a second graph of the same steps with timing events around
-    # every launch (external event nodes, where this torch supports them),
-    # replayed after the timed region.
-    try:
-        torch.cuda.Event(enable_timing=True, external=True)
-        mk_ev = lambda: torch.cuda.Event(enable_timing=True, external=True)
-        in_graph_events = True
-    except TypeError:
-        in_graph_events = False
-    evs = [[[mk_ev(), mk_ev()] for _ in names] for _ in range(args.steps)] if in_graph_events else None
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        for i in range(args.steps):
-            step()
-    graph_ev = None
-    if in_graph_events:
-        graph_ev = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph_ev):
-            for i in range(args.steps):
-                step(evs[i])
-    props = torch.cuda.get_device_properties(dev)
-    uuid = str(getattr(props, "uuid", ""))
-    sampler = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or str(local)))
-    time.sleep(0.3)
-    barrier()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    graph.replay()
-    t_end.record(stream)
-    barrier()
-    clocks = sampler.stop()
-    sb.get_error()
-    elapsed = max_over_ranks(t_start.elapsed_time(t_end) / 1e3, ws, dev)
-    value = job_throughput(flops_step * args.steps, ws, elapsed) / 1e12
-    n_ev = args.steps
-    if graph_ev is not None:
-        graph_ev.replay()
-        torch.cuda.synchronize()
-    else:
-        # per-kernel durations from eager steps with CUDA events around every launch
-        n_ev = min(args.steps, 20)
-        evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in names]
-               for _ in range(n_ev)]
-        for i in range(n_ev):
-            step(evs[i])
-        torch.cuda.synchronize()
-    per_kernel = {n: [] for n in names}
-    for i in range(n_ev):
-        for k, n in enumerate(names):
-            per_kernel[n].append(evs[i][k][0].elapsed_time(evs[i][k][1]) / 1e3)
-    mean_t = {n: float(np.median(v)) for n, v in per_kernel.items()}   # per launch: median over the K steps
-
     # ---- end to end through the public API: pinned host inputs copied in every step
+    tl = G["tail"]
     pinned = []
     h2d = 0
-    for (a, r), l in zip(host_inputs, L):
+    for (a, r), l in zip(G["host_inputs"], L):
         ha = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
         hr = torch.from_numpy(r.view(np.int16)).view(torch.bfloat16).pin_memory() if r is not None else None
         pinned.append((ha, hr))
         h2d += ha.numel() * 2 + (hr.numel() * 2 if hr is not None else 0)
-    hb = [torch.from_numpy(gp[k].view(np.int16)).view(torch.bfloat16).pin_memory() for k in ("xin", "xout")]
+    hb = [torch.from_numpy(G["gp"][k].view(np.int16)).view(torch.bfloat16).pin_memory() for k in ("xin", "xout")]
     h2d += sum(t.numel() * 2 for t in hb)
     res_host = torch.empty(4 + 4 + 1, dtype=torch.uint8).pin_memory()
-    d2h = res_host.numel() + 8
     out_host = torch.empty(2, dtype=torch.float32).pin_memory()
+    d2h = res_host.numel() + out_host.numel() * 4
 
     # Inputs are double-buffered on the device: while the compute stream runs
     # step s on one set, two copy streams bring step s+1's inputs into the
     # other.  Every step copies all of its inputs from pinned host memory and
     # reads its decisions back inside the timed region; events order a set's
     # copies after the step that last read it.
-    sets = [dict(x=[l["x"] for l in L], r=[l["r"] for l in L], bin=bin_, bout=bout),
+    sets = [dict(x=[l["x"] for l in L], r=[l["r"] for l in L], bin=tl["bin"], bout=tl["bout"]),
             dict(x=[torch.empty_like(l["x"]) for l in L],
                  r=[torch.empty_like(l["r"]) if l["r"] is not None else None for l in L],
-                 bin=torch.empty_like(bin_), bout=torch.empty_like(bout))]
+                 bin=torch.empty_like(tl["bin"]), bout=torch.empty_like(tl["bout"]))]
     copy_streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
     ready = [[torch.cuda.Event() for _ in copy_streams] for _ in sets]
     free = [torch.cuda.Event() for _ in sets]
@@ -737,10 +899,10 @@ def run_ours(args):
             stream.wait_event(ev)
         step(inp=sets[si])
         free[si].record(stream)
-        out_host.copy_(gamma_t[0:2], non_blocking=True)
-        res_host[0:4].copy_(flags, non_blocking=True)
-        res_host[4:8].copy_(gates.view(-1)[0:4], non_blocking=True)
-        res_host[8:9].copy_(cflag, non_blocking=True)
+        out_host.copy_(tl["gamma"][0:2], non_blocking=True)
+        res_host[0:4].copy_(tl["flags"], non_blocking=True)
+        res_host[4:8].copy_(tl["gates"].view(-1)[0:4], non_blocking=True)
+        res_host[8:9].copy_(tl["cflag"], non_blocking=True)
         if not last:
             load((s + 1) % 2)
 
@@ -759,46 +921,50 @@ def run_ours(args):
     barrier()
     e2e_elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, ws, dev)
     e2e_value = job_throughput(flops_step * e2e_steps, ws, e2e_elapsed) / 1e12
+    del sets, pinned
 
-    # ---- roofline of the dominant kernel
-    peaks, peak_kind = load_peaks()
-    fp4_peak = float(peaks["bf16_tflops"]) * FP4_OVER_BF16
-    family = {}
-    for n, t in mean_t.items():
-        family.setdefault(n.split("[")[0], []).append((n, t))
-    gemm_names = [n for n in names if n.startswith("w4a")]
+    # ---- roofline of the dominant kernel: the longest launch of the step,
+    # its method FLOPs (2MNK) against the dense FP4 tensor peak
+    report = gemm_set_report(G, T, fp4_peak, hbm, args.workload)
+    gemm_names = [n for n in T["names"] if n.startswith("w4a")]
     dom = max(gemm_names, key=lambda n: mean_t[n])
-    li = [l["name"] for l in L].index(dom.split("[")[1][:-1])
-    dom_flops = flops_layer[li]
-    # W4A8 runs three FP4 digit MMAs per product: its ceiling is a third of the FP4 peak
-    dom_peak = fp4_peak / 3.0 if dom.startswith("w4a8") else fp4_peak
-    achieved = dom_flops / mean_t[dom] / 1e12
-    # the committed counters were captured on the 2B-class layer shapes only
+    dr = report["gemm"][dom]
     traffic = dram_traffic(dom) if args.workload == "2b" else None
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": dom_peak, "unit": "TFLOP/s",
-                "frac": achieved / dom_peak, "traffic": traffic,
-                "peak_note": f"{peak_kind} bf16 burst {peaks['bf16_tflops']} TFLOP/s x nominal FP4/BF16 ratio 6"
-                             + ("; / 3 for the three digit-plane MMAs of W4A8" if dom.startswith("w4a8") else "")}
-    hbm = float(peaks["hbm_gbs"])
-    byte_rows = {}
-    for l in L:
-        n_el = M * l["K"]
-        # algorithmic minimum: read x once, write the quantized form
-        byte_rows[f"quant_nvfp4[{l['name']}]"] = (2 + 0.5 + 1 / 16) * n_el      # x, codes, E4M3 scales
-        byte_rows[f"quant_int8[{l['name']}]"] = (2 + 1.5) * n_el + 4 * M         # x, 3 digit planes, row scales
-    byte_rows["gamma_delta"] = 8.0 * M * H
-    bw = {n: {"ms": mean_t[n] * 1e3, "GB/s": byte_rows[n] / mean_t[n] / 1e9,
-              "frac_hbm": byte_rows[n] / mean_t[n] / 1e9 / hbm} for n in byte_rows}
-    tf = {}
-    for n in gemm_names:
-        l = L[[x["name"] for x in L].index(n.split("[")[1][:-1])]
-        tf[n] = gemm_roofline(n.split("[")[0], M, l["N"], l["K"], l["r"] is not None, mean_t[n], fp4_peak, hbm)
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": dr["TFLOP/s"], "peak": fp4_peak, "unit": "TFLOP/s",
+                "frac": dr["TFLOP/s"] / fp4_peak, "traffic": traffic,
+                "peak_note": f"dense FP4 tensor peak: {peak_kind} bf16 burst {peaks['bf16_tflops']} TFLOP/s x the "
+                             f"nominal FP4/BF16 ratio 6; achieved = the method's 2MNK / the launch's median time"}
+    if dom.startswith("w4a8"):
+        roofline["fp4_pipe_frac"] = dr["fp4_pipe_frac"]
+        roofline["fp4_pipe_note"] = ("W4A8 issues three exact E2M1 digit-plane MMAs per product on the FP4 pipe: "
+                                     "3 x achieved / peak is that pipe's busy fraction; its design ceiling is peak/3")
+    w4a4 = {n: v["frac_fp4_peak"] for n, v in report["gemm"].items() if n.startswith("w4a4")}
 
-    producers = time_producers(sb, L, dev, (bin_, bout)) if rank == 0 and args.workload == "2b" else None
+    extra = {}
+    if rank == 0 and args.workload == "2b":
+        extra["quantizing_producers"] = time_producers(sb, L, dev, (tl["bin"], tl["bout"]))
+        extra["quant_nvfp4_amax_given"] = time_nvfp4_amax_given(sb, G, dev)
+    del G, T
+    torch.cuda.empty_cache()
 
-    stack_res = None
+    # ---- the 5B-class GEMM set (quantizer and GEMM timed separately and back to back)
+    set5 = None
+    if rank == 0 and args.workload == "2b" and not args.no_5b:
+        G5 = setup_gemm_set(sb, "5b", dev)
+        T5 = time_gemm_set(sb, G5, args.steps, args.warmup, 1, dev)
+        f5 = 2 * sum(2 * G5["M"] * l["N"] * l["K"] for l in G5["L"])
+        rep5 = gemm_set_report(G5, T5, fp4_peak, hbm, "5b")
+        set5 = {"config": workload_config("5b", G5["M"], G5["layers"], 1)["workload"],
+                "value": f5 * args.steps / T5["elapsed"] / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": T5["elapsed"] / args.steps * 1e3, "per_kernel": rep5}
+        del G5, T5
+        torch.cuda.empty_cache()
+
+    stacks = {}
     if rank == 0 and args.stack != "none":
-        stack_res = run_stack_bench(args.stack, dev, cpu_oracle=not args.no_cpu_baseline)
+        stacks["2b"] = run_stack_bench(args.stack, dev, cpu_oracle=not args.no_cpu_baseline)
+        if args.stack == "2b" and not args.no_5b:
+            stacks["5b_cfg"] = run_stack_bench("5b", dev, cpu_oracle=False, modes=("dmpq_tdc", "dmpq_only"))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -816,15 +982,18 @@ def run_ours(args):
                 "config": dict(workload_config(args.workload, M, layers, ws),
                                timing="the K steps captured as one CUDA graph, replayed once between CUDA events; "
                                       + ("per-launch durations from a second, instrumented graph of the same steps"
-                                         if in_graph_events
-                                         else "per-launch events from eager steps after the timed region")),
+                                         if in_graph else "per-launch events from eager steps")),
                 "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
-                        "d2h_bytes_per_step": int(d2h)},
-                "gpu_launches": launches_per_step * args.steps,
-                "clocks": clocks, "roofline": roofline, "cpu_baseline": cpu,
-                "dit_stack": stack_res,
-                "per_kernel": {"gemm": tf, "bandwidth": bw, "dmpq_ms": mean_t["dmpq"] * 1e3,
-                               "tdc_ms": mean_t["tdc"] * 1e3, "quantizing_producers": producers}}
+                        "d2h_bytes_per_step": int(d2h),
+                        "d2h_note": "the step's decisions (Gamma, r2, DMPQ flags and gates, TDC compute bit) are read "
+                                    "back; the eight GEMM outputs stay in device memory, where the next layer of the "
+                                    "network would read them"},
+                "gpu_launches": launches_step * args.steps,
+                "clocks": clocks, "roofline": roofline, "w4a4_frac_fp4_peak": w4a4,
+                "cpu_baseline": cpu,
+                "gemm_set_5b": set5,
+                "dit_stack": stacks.get("2b"), "dit_stack_5b_cfg": stacks.get("5b_cfg"),
+                "per_kernel": dict(report, **extra)}
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
@@ -840,6 +1009,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--stack", choices=["2b", "5b", "none"], default="2b",
                     help="DiT block stack measured after the GEMM-set step (blocks/s with DMPQ+TDC)")
+    ap.add_argument("--no-5b", action="store_true",
+                    help="skip the 5B-class GEMM set and the 5B CFG stack that the default run also measures")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -113,6 +113,18 @@ int sixbit_quantize_act_int8(const void* x, int64_t M, int64_t K, int64_t ldx,
                              const float* row_amax_in, int8_t* q, uint8_t* planes,
                              float* row_scale, const uint8_t* pred, sixbit_stream_t stream);
 
+/* The W4A8 operand form of plain INT8 activations, for callers that hold
+ * per-token int8 codes from elsewhere (their own quantizer, a previous
+ * layer): q int8 [M, K] (row stride ldq, ldq % 16 == 0), K % 64 == 0, ->
+ * planes [3][M][K/2], the exact digit split q = 64a + 8b + c that
+ * sixbit_quantize_act_int8 writes (digits in [-4, 4] as E2M1 codes, element
+ * 2j in the low nibble).  Codes outside [-127, 127] (-128) are split
+ * exactly too (a = -2, b = 0, c = 0).  With the row scales the caller already
+ * has, sixbit_qlinear_w4a8 then runs on these planes.  One streaming pass:
+ * 1 byte read and 1.5 bytes written per element. */
+int sixbit_int8_digit_planes(const int8_t* q, int64_t M, int64_t K, int64_t ldq, uint8_t* planes,
+                             sixbit_stream_t stream);
+
 /* a5 -- W4A4 linear: y = g_a g_w sum_k (E2M1*S)_a (E2M1*S)_w + bias,
  * optional tanh-GELU, optional + residual; fp32 accumulation on tcgen05
  * block-scaled FP4 tensor cores.  Source: uniform W4A4 of Table 3, NVFP4

@@ -54,6 +54,7 @@ _SIGS = {
     "sixbit_qlinear_qout": ([_INT, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _I64, _P, _INT, _P, _I64, _P, _P, _P, _P,
                              _F, _P, _P, _P], _INT),
     "sixbit_debug_stall_gemm": ([_INT], _INT),
+    "sixbit_int8_digit_planes": ([_P, _I64, _I64, _I64, _P, _P], _INT),
     "sixbit_get_error": ([_P], _INT),
 }
 
@@ -182,6 +183,16 @@ def quantize_act_int8(x: torch.Tensor, row_amax=None, want_q=True, want_planes=T
 
 
 # --------------------------------------------------------------- GEMMs
+def int8_digit_planes(q: torch.Tensor, out=None):
+    """Plain int8 codes [M, K] -> the W4A8 operand planes u8 [3, M, K/2] (exact digit split)."""
+    _need_cuda(q)
+    M, K = q.shape
+    planes = torch.empty((3, M, K // 2), dtype=torch.uint8, device=q.device) if out is None else out
+    _check("sixbit_int8_digit_planes",
+           lib().sixbit_int8_digit_planes(_ptr(q), M, K, q.stride(0), _ptr(planes), _stream()))
+    return planes
+
+
 def _out(M, N, dtype, device, out):
     if out is not None:
         return out

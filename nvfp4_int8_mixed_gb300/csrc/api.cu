@@ -127,6 +127,17 @@ int sixbit_quantize_act_int8(const void* x, int64_t M, int64_t K, int64_t ldx, c
   return launch_int8_quant(x, M, K, ldx, row_amax_in, q, planes, row_scale, pred, sms, cs(stream));
 }
 
+int sixbit_int8_digit_planes(const int8_t* q, int64_t M, int64_t K, int64_t ldq, uint8_t* planes,
+                             sixbit_stream_t stream) {
+  if (M == 0) return kOk;                 // empty: nothing to do, pointers unused
+  if (!q || !planes || M < 0 || K <= 0 || ldq < K) return kEInval;
+  if (K % 64 != 0 || ldq % 16 != 0) return kEShape;
+  if (!aligned16(q) || !aligned16(planes)) return kEAlign;
+  int sms;
+  if (device_setup(&sms, nullptr) != kOk) return kELaunch;
+  return launch_int8_planes(q, M, K, ldq, planes, sms, cs(stream));
+}
+
 static int check_gemm(const uint8_t* a, const uint8_t* w, const uint8_t* w_sf, const float* g_w, int64_t M, int64_t K,
                       int64_t N, const void* bias, const void* residual, int64_t ldr, int out_dtype, void* y,
                       int64_t ldy) {

@@ -10,6 +10,8 @@ int launch_amax(const void* x, int dtype, int64_t M, int64_t K, int64_t ldx, flo
                 const uint8_t* pred, int num_sms, cudaStream_t s);
 int launch_nvfp4_quant(const void* x, int dtype, int64_t M, int64_t K, int64_t ldx, const float* amax,
                        uint8_t* codes, uint8_t* sf, float* g_out, const uint8_t* pred, int num_sms, cudaStream_t s);
+int launch_int8_planes(const int8_t* q, int64_t M, int64_t K, int64_t ldq, uint8_t* planes, int num_sms,
+                       cudaStream_t s);
 int launch_int8_quant(const void* x, int64_t M, int64_t K, int64_t ldx, const float* row_amax_in, int8_t* q,
                       uint8_t* planes, float* row_scale, const uint8_t* pred, int num_sms, cudaStream_t s);
 

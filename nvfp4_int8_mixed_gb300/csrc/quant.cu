@@ -154,6 +154,25 @@ template <> struct Block16<float> {
   __device__ float at(int i) const { return __uint_as_float((&v[i >> 2].x)[i & 3]); }
 };
 
+// Work item = (row, pair of 32-block spans): a warp's two 16-byte loads per
+// lane per block for 2 x 32 consecutive blocks (2 KB of bf16).  Warps are
+// persistent and walk the items t = warp, warp + nwarps, ...; the next
+// item's loads are issued before the current item is encoded and stored, so
+// every warp always has a load in flight.  Consecutive warps take
+// consecutive items (adjacent memory).
+template <typename T>
+__device__ __forceinline__ void nvfp4_load_item(const T* __restrict__ x, int64_t item, int64_t ppr, int nspan,
+                                                int nblk, int64_t M, int64_t ldx, int lane, Block16<T> (&blk)[2]) {
+  const int64_t m = item / ppr;
+  const int sp0 = int(item - m * ppr) * 2;
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int b = (sp0 + u) * 32 + lane;
+    if (m < M && sp0 + u < nspan && b < nblk) blk[u].load(x + m * ldx + int64_t(b) * 16);
+    else blk[u].zero();
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(const T* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
                                                                const float* __restrict__ amax_ptr,
@@ -167,43 +186,41 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(const T* __restri
   const int64_t kc4 = K / 16;                 // K % 64 == 0 -> a multiple of 4
   const int nblk = int(K / 16);
   const int nspan = (nblk + 31) / 32;
+  const int64_t ppr = (nspan + 1) / 2;        // items (span pairs) per row
+  const int64_t items = Mpad * ppr;
   const int64_t warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
-  constexpr int kU = 2;
-  for (int64_t m = warp; m < Mpad; m += nwarps) {
+  Block16<T> cur[2], nxt[2];
+  if (warp < items) nvfp4_load_item(x, warp, ppr, nspan, nblk, M, ldx, lane, cur);
+  for (int64_t it = warp; it < items; it += nwarps) {
+    if (it + nwarps < items) nvfp4_load_item(x, it + nwarps, ppr, nspan, nblk, M, ldx, lane, nxt);
+    const int64_t m = it / ppr;
+    const int sp0 = int(it - m * ppr) * 2;
     const bool row_ok = m < M;
-    const T* row = x + m * ldx;
-    for (int sp0 = 0; sp0 < nspan; sp0 += kU) {
-      Block16<T> blk[kU];
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int b = (sp0 + u) * 32 + lane;
-        if (row_ok && b < nblk) blk[u].load(row + int64_t(b) * 16);
-        else blk[u].zero();
+    for (int u = 0; u < 2; ++u) {
+      if (sp0 + u >= nspan) break;            // warp-uniform
+      const int b = (sp0 + u) * 32 + lane;
+      float r;
+      const uint32_t sb = nvfp4_block_scale(cur[u].amax(), amax_t, g, r);
+      uint32_t w0 = 0, w1 = 0;
+      if (r != 0.f) {
+        float y[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) y[e] = __fmul_rn(cur[u].at(e), r);
+        w0 = e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
+        w1 = e2m1x8(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
       }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        if (sp0 + u >= nspan) break;          // warp-uniform
-        const int b = (sp0 + u) * 32 + lane;
-        float r;
-        const uint32_t sb = nvfp4_block_scale(blk[u].amax(), amax_t, g, r);
-        uint32_t w0 = 0, w1 = 0;
-        if (r != 0.f) {
-          float y[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) y[e] = __fmul_rn(blk[u].at(e), r);
-          w0 = e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
-          w1 = e2m1x8(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
-        }
-        // 4 consecutive blocks (lanes 4j..4j+3) form one 32-bit word of the swizzled scale buffer
-        uint32_t word = sb | (__shfl_down_sync(0xffffffffu, sb, 1) << 8);
-        word |= __shfl_down_sync(0xffffffffu, word, 2) << 16;
-        if (b < nblk) {
-          if (row_ok) *reinterpret_cast<uint2*>(codes + m * (K / 2) + int64_t(b) * 8) = make_uint2(w0, w1);
-          if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset(m, b, kc4)) = row_ok ? word : 0u;
-        }
+      // 4 consecutive blocks (lanes 4j..4j+3) form one 32-bit word of the swizzled scale buffer
+      uint32_t word = sb | (__shfl_down_sync(0xffffffffu, sb, 1) << 8);
+      word |= __shfl_down_sync(0xffffffffu, word, 2) << 16;
+      if (b < nblk) {
+        if (row_ok) *reinterpret_cast<uint2*>(codes + m * (K / 2) + int64_t(b) * 8) = make_uint2(w0, w1);
+        if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset(m, b, kc4)) = row_ok ? word : 0u;
       }
     }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) cur[u] = nxt[u];
   }
 }
 
@@ -293,6 +310,37 @@ __global__ void __launch_bounds__(128) int8_quant_kernel(const uint16_t* __restr
   }
 }
 
+// Plain INT8 codes -> the three E2M1 digit planes the W4A8 GEMM reads (for
+// callers that hold int8 activations from elsewhere).  Exact: a table
+// lookup per code.  One thread per 16 codes (a 16-byte load, three 8-byte
+// stores), grid-stride over rows of K/16 groups.
+__global__ void __launch_bounds__(kThreads) int8_planes_kernel(const int8_t* __restrict__ q, int64_t M, int64_t K,
+                                                               int64_t ldq, uint8_t* __restrict__ planes) {
+  __shared__ uint32_t lut[256];
+  for (int i = threadIdx.x; i < 256; i += kThreads) lut[i] = digit_entry(int(int8_t(uint8_t(i))));
+  __syncthreads();
+  const int64_t gpr = K / 16;                      // 16-code groups per row
+  const int64_t total = M * gpr;
+  const int64_t plane_stride = M * (K / 2);
+  for (int64_t gi = int64_t(blockIdx.x) * kThreads + threadIdx.x; gi < total; gi += int64_t(gridDim.x) * kThreads) {
+    const int64_t m = gi / gpr, c = gi - m * gpr;
+    const uint4 v = ldg_nc_v4(q + m * ldq + c * 16);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t p0[2], p1[2], p2[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t qb[8];                              // int8_planes8 reads the code from each entry's low byte
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qb[e] = (w[2 * h + (e >> 2)] >> (8 * (e & 3))) & 0xFFu;
+      int8_planes8(qb, lut, p0[h], p1[h], p2[h]);
+    }
+    uint8_t* base = planes + m * (K / 2) + c * 8;
+    *reinterpret_cast<uint2*>(base) = make_uint2(p0[0], p0[1]);
+    *reinterpret_cast<uint2*>(base + plane_stride) = make_uint2(p1[0], p1[1]);
+    *reinterpret_cast<uint2*>(base + 2 * plane_stride) = make_uint2(p2[0], p2[1]);
+  }
+}
+
 int grid_for(int64_t work_items, int per_block, int num_sms, int waves = 8) {
   int64_t want = cdiv(work_items, per_block);
   int64_t cap = int64_t(num_sms) * waves;
@@ -326,13 +374,28 @@ int launch_amax(const void* x, int dtype, int64_t M, int64_t K, int64_t ldx, flo
 int launch_nvfp4_quant(const void* x, int dtype, int64_t M, int64_t K, int64_t ldx, const float* amax,
                        uint8_t* codes, uint8_t* sf, float* g_out, const uint8_t* pred, int num_sms, cudaStream_t s) {
   const int64_t Mpad = cdiv(M, 128) * 128;
-  const int grid = grid_for(Mpad, kThreads / 32, num_sms, 16);
+  const int64_t items = Mpad * cdiv(cdiv(K / 16, 32), 2);
+  // persistent: as many CTAs as are resident (each warp walks many items)
+  static int per_sm[2] = {0, 0};
+  int& ps = per_sm[dtype == 1 ? 0 : 1];
+  if (ps == 0) {
+    const bool ok = dtype == 1 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, nvfp4_quant_kernel<uint16_t>, kThreads, 0) == cudaSuccess
+                               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, nvfp4_quant_kernel<float>, kThreads, 0) == cudaSuccess;
+    if (!ok || ps < 1) ps = 1;
+  }
+  const int grid = grid_for(items, kThreads / 32, num_sms, ps);
   if (dtype == 1)
     nvfp4_quant_kernel<uint16_t><<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), M, K, ldx, amax, codes, sf,
                                                            g_out, pred, Mpad);
   else
     nvfp4_quant_kernel<float><<<grid, kThreads, 0, s>>>(static_cast<const float*>(x), M, K, ldx, amax, codes, sf, g_out,
                                                         pred, Mpad);
+  return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
+}
+
+int launch_int8_planes(const int8_t* q, int64_t M, int64_t K, int64_t ldq, uint8_t* planes, int num_sms,
+                       cudaStream_t s) {
+  int8_planes_kernel<<<grid_for(M * (K / 16), kThreads, num_sms, 8), kThreads, 0, s>>>(q, M, K, ldq, planes);
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 

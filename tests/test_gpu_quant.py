@@ -7,7 +7,7 @@ import torch
 
 import synthetic
 from oracle import codecs, int8 as o_int8, nvfp4 as o_nvfp4
-from tests.helpers import dev, dev_bf16, host
+from tests.helpers import assert_gemm_close, dev, dev_bf16, host
 
 pytestmark = pytest.mark.gpu
 
@@ -137,3 +137,27 @@ def _quantizers_full_shape(*Ks):
         assert np.array_equal(host(q)[rows], rq) and np.array_equal(host(s)[rows], rs)
         pad = host(sf).reshape(-1)
         assert pad.size == o_nvfp4.sf_padded_shape(synthetic.M_2B, K)[0] * (K // 16)
+
+
+@pytest.mark.parametrize("M,K,ldq", [(1, 64, 64), (129, 320, 320), (300, 1920, 2048)])
+def test_int8_digit_planes_of_plain_codes(M, K, ldq):
+    """Plain int8 codes from anywhere (here every byte value, -128 included,
+    with a row stride) -> the exact digit planes; the W4A8 GEMM on them
+    equals the oracle's int8 x W4 product."""
+    from oracle import gemm as o_gemm
+    sb = _sb()
+    g = synthetic.rng(300 + M)
+    full = g.integers(-128, 128, size=(M, ldq)).astype(np.int8)
+    full[0, :min(K, 256)] = np.arange(-128, 128)[:min(K, 256)]           # every code value
+    qd = dev(full)[:, :K]
+    planes = sb.int8_digit_planes(qd)
+    q = full[:, :K]
+    pa, pb, pc = o_int8.digit_codes(q)
+    assert np.array_equal(host(planes), np.stack([codecs.pack_e2m1(pa), codecs.pack_e2m1(pb), codecs.pack_e2m1(pc)]))
+    # the W4A8 layer on planes made from plain codes
+    s = g.uniform(0.001, 0.01, M).astype(np.float32)
+    w = synthetic.weights(g, 128, K)
+    wc, wsf, gw = sb.quantize_weight_nvfp4(dev(w))
+    y = sb.qlinear_w4a8(planes, dev(s), wc, wsf, gw, out_dtype=torch.float32)
+    rwc, rwsf, rgw, _ = o_nvfp4.quantize(w)
+    assert_gemm_close(host(y), o_gemm.w4a8(q, s, rwc, rwsf, rgw), "f32")

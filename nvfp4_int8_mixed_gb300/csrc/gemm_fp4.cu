@@ -73,7 +73,7 @@ constexpr uint32_t kSpinCap = 1u << 22;  // polls of a bounded mbarrier wait
 constexpr uint32_t kTmemCols = 512;
 
 #ifndef GEMM_PAIR
-#define GEMM_PAIR false  // W4A8: true = CTA pairs with cta_group::2 MMAs (256 x 256 tiles)
+#define GEMM_PAIR true   // W4A8: CTA pairs with cta_group::2 MMAs (256 x 256 tiles; 5 stages fit instead of 4)
 #endif
 #ifndef W4A4_PAIR
 #define W4A4_PAIR true   // W4A4: CTA pairs (each CTA streams half of W: ~145 instead of ~206 GB/s per SM)

@@ -151,6 +151,8 @@ QOUT_CASES = [
     ("w4a8", 200, 192, 320, True, False),
     ("w4a4", 1, 128, 64, False, False),
     ("w4a8", 129, 256, 1920, False, True),
+    ("w4a4", 300, 384, 256, True, True),                # half-width last column tiles
+    ("w4a8", 300, 320, 448, False, True),
     ("w4a4", 17776, 7680, 1920, True, False),          # the FFN up-projection of the 2B block
     ("w4a8", 17776, 7680, 1920, True, False),
 ]
@@ -228,7 +230,8 @@ def test_qout_feeds_the_next_layer():
     assert_gemm_close(host(out), ref, "f32")
 
 
-@pytest.mark.parametrize("mode,M,N,K", [("w4a4", 300, 512, 256), ("w4a8", 129, 144, 320), ("w4a4", 17776, 7680, 1920)])
+@pytest.mark.parametrize("mode,M,N,K", [("w4a4", 300, 512, 256), ("w4a8", 129, 144, 320), ("w4a8", 260, 384, 256),
+                                        ("w4a4", 17776, 7680, 1920)])
 def test_qlinear_amax_side_output(mode, M, N, K):
     """No NVFP4 outputs: the plain layer (bit-identical y) plus the exact
     max |y| in the history's first word, usable as a quantizer's amax_in."""

@@ -43,6 +43,10 @@ CASES = [
     (129, 256, 1920, True, False, True, "bf16"),      # K = 1920: half a K step at the end
     (1, 128, 64, False, False, False, "f32"),
     (384, 384, 7680, False, True, True, "f32"),
+    # a ragged last column of <= 128 columns runs as half-width tiles after all full tiles
+    (300, 320, 448, True, True, True, "bf16"),       # 64 valid columns: one CTA's W half lies wholly past N
+    (520, 1920, 256, False, True, True, "bf16"),     # 7 full column tiles + 1 half, 3 row tiles
+    (600, 5760, 128, False, False, False, "f32"),    # the QKV width: 22 full column tiles + 1 half
 ]
 
 

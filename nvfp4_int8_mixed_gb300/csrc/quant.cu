@@ -174,7 +174,7 @@ __device__ __forceinline__ void nvfp4_load_item(const T* __restrict__ x, int64_t
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, sizeof(T) == 2 ? 4 : 2) nvfp4_quant_kernel(const T* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
+__global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(const T* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
                                                                const float* __restrict__ amax_ptr,
                                                                uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                                                                float* g_out, const uint8_t* pred, int64_t Mpad) {

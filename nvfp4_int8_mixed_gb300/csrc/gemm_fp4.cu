@@ -21,8 +21,10 @@
 //               (W4A8, CTA pairs) or, for W4A4 on one CTA, into a ring of
 //               their own that runs ahead of the code stages;
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::mxf4nvf4
-//               scale_vec::4X (128 x 256 x 64 per instruction) into the TMEM
-//               accumulator, tcgen05.commit to free stages and publish tiles;
+//               scale_vec::4X (128 x 256 x 64 per instruction, 256 x 256 on a
+//               CTA pair) into the TMEM accumulator, tcgen05.commit to free
+//               stages and publish tiles; the whole warp runs the loop and
+//               lane 0 issues;
 //   warps 4..7  scale warps, one per TMEM lane quarter: move each k-step's
 //               scale atoms from shared memory into TMEM scale columns with
 //               tcgen05.st, in the layout a replicating tcgen05.cp
@@ -30,7 +32,7 @@
 //   warps 8..15 epilogue: two warps per TMEM lane quarter, 128 columns each.
 //               They pull the whole accumulator into registers, release TMEM
 //               at once (the next tile's MMAs start), then scale, add bias,
-//               GELU (one special-function op an element), add the residual
+//               GELU (two special-function ops an element), add the residual
 //               (a TMA-loaded tile) and write bf16 through 128-byte-swizzled
 //               shared memory with TMA stores.  The QO instantiation can
 //               instead encode the result as NVFP4 for the next layer
@@ -360,34 +362,30 @@ __host__ __device__ constexpr uint32_t idesc_fp4(int m, int n) {
 }
 
 // tanh-form GELU, 0.5 x (1 + tanh(u)) with u = sqrt(2/pi) (x + 0.044715 x^3),
-// written as x / (1 + 2^t), t = -2 u log2(e) (the same function), for two
-// elements at a time.  2^t is the hardware approximation (ex2.approx, one
-// special-function op an element); the reciprocal is computed on the FMA
-// pipe: the seed 2*bits(1.0) - bits(d) (exact at powers of two, at most
-// 12.5 % high in between), then three Newton steps r += r (1 - d r), which
-// take the relative error to 1.6e-2, 2.4e-4 and 6e-8.  Two special-function
-// ops an element (exp and reciprocal) bounded the FFN-up epilogue.  t is
-// clamped at 126 so d stays finite (a large negative x gives ~x * 2^-126).
+// written as x / (1 + 2^t), t = -2 u log2(e) = x (c1 + c2 x^2) (the same
+// function), for two elements at a time: t on the packed f32x2 pipe, then
+// the hardware approximations 2^t (ex2.approx) and 1 / (1 + 2^t)
+// (rcp.approx), each accurate to about an fp32 unit in the last place.
+// Unlike 1 + tanh(u) this form has no cancellation for negative x, so the
+// result keeps fp32 relative accuracy everywhere.  For t >= 128 (x below
+// about -10) 2^t is +inf and the result is -0, the bf16 rounding of the
+// exact value.  Against an exponent-flip seed with three Newton steps on
+// the FMA pipe: identical bf16 outputs except one-ulp differences at
+// rounding ties (3e-5 of the 2B FFN-up outputs) and -0 where that form's
+// clamp of t at 126 left ~-1e-37; the W4A4 FFN-up ran 150.1 -> 127.6 us.
 __device__ __forceinline__ void gelu_tanh2(float& x0, float& x1) {
   const uint64_t x = f2_pack(x0, x1);
-  const uint64_t xx = f2_mul(x, x);
-  const uint64_t p = f2_fma(xx, f2_pack(0.044715f, 0.044715f), f2_pack(1.f, 1.f));   // 1 + 0.044715 x^2
-  // t = -2 sqrt(2/pi) log2(e) x (1 + 0.044715 x^2)
-  const uint64_t t2 = f2_mul(f2_mul(x, p), f2_pack(-2.302208198f, -2.302208198f));
-  float t0, t1;
-  f2_unpack(t2, t0, t1);
-  float e0, e1;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(e0) : "f"(fminf(t0, 126.f)));
-  asm("ex2.approx.f32 %0, %1;" : "=f"(e1) : "f"(fminf(t1, 126.f)));
-  const uint64_t one = f2_pack(1.f, 1.f);
-  const uint64_t d = f2_add(f2_pack(e0, e1), one);
-  float d0, d1;
-  f2_unpack(d, d0, d1);
-  uint64_t r = f2_pack(__int_as_float(0x7F000000 - __float_as_int(d0)), __int_as_float(0x7F000000 - __float_as_int(d1)));
-  const uint64_t nd = f2_sub(0, d);                                                // -d
-#pragma unroll
-  for (int it = 0; it < 3; ++it) r = f2_fma(r, f2_fma(nd, r, one), r);
-  f2_unpack(f2_mul(x, r), x0, x1);
+  // c1 = -2 sqrt(2/pi) log2(e), c2 = 0.044715 c1
+  const uint64_t t = f2_mul(x, f2_fma(f2_mul(x, x), f2_pack(-0.10294324f, -0.10294324f),
+                                      f2_pack(-2.302208198f, -2.302208198f)));
+  float t0, t1, e0, e1, d0, d1, r0, r1;
+  f2_unpack(t, t0, t1);
+  asm("ex2.approx.f32 %0, %1;" : "=f"(e0) : "f"(t0));
+  asm("ex2.approx.f32 %0, %1;" : "=f"(e1) : "f"(t1));
+  f2_unpack(f2_add(f2_pack(e0, e1), f2_pack(1.f, 1.f)), d0, d1);
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(d0));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(d1));
+  f2_unpack(f2_mul(x, f2_pack(r0, r1)), x0, x1);
 }
 
 struct Params {

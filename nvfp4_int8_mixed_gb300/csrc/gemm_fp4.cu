@@ -428,6 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int R = C::kSfSlots;
   uint64_t* bars = reinterpret_cast<uint64_t*>(extra);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 3 * R + 12);
+  static_assert((2 * STAGES + 3 * R + 12) * 8 + 8 <= 512, "barriers, TMEM address and abort flag below the r table");
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -749,6 +750,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float q_g = nvfp4_global_scale(q_amax_t);
     if (q_nv && blockIdx.x == 0 && ew == 0 && lane == 0) *p.q_g = q_g;
     const int q_mpad = ((p.M + 127) / 128) * 128;   // rows of the padded scale layout
+    // 1 / (S g) for every E4M3 block scale S a satfinite encode can give
+    // (codes 0..126), computed once per CTA exactly as the per-block form
+    // would: the upper half of the barrier area holds it.
+    float* const q_rtab = reinterpret_cast<float*>(extra + 512);
+    if constexpr (QO) {
+      if (q_nv) {
+        const int i = ew * 32 + lane;
+        if (i < 128) {
+          const float d = __fmul_rn(e4m3_decode(uint32_t(i)), q_g);
+          q_rtab[i] = d != 0.f ? __frcp_rn(d) : 0.f;
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");   // the 8 epilogue warps of this CTA
+      }
+    }
     uint32_t q_run = 0;                          // |y| max as two bf16 halves
     for (int tile = blockIdx.x / kCtas; tile < ntiles && ok; tile += gridDim.x / kCtas) {
       const int mt = tile / p.NT, nt = tile - mt * p.NT;
@@ -776,6 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float scale = MODE == 0 ? gscale : (m < p.M ? __fmul_rn(p.row_scale[m], gw) : 0.f);
         const int64_t kc4 = p.N / 16;
         uint32_t sfw = 0;
+        const uint64_t sc2 = f2_pack(scale, scale);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const uint32_t* rc = c == 0 ? r0 : (c == 1 ? r1 : (c == 2 ? r2 : r3));
@@ -783,7 +799,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (n0 >= p.N) break;                  // N % 64 == 0: whole 64-column pairs
           float v[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(__uint_as_float(rc[i]), scale);
+          for (int i = 0; i < 32; i += 2)
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(rc[i]), __uint_as_float(rc[i + 1])), sc2), v[i], v[i + 1]);
           if (p.bias) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -803,12 +820,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pk[16];                       // the bf16 values the unfused path would store
 #pragma unroll
           for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-          float ra, rb;
-          const uint32_t sa = nvfp4_block_scale(fmaxf(bf16x8_absmax(pk), bf16x8_absmax(pk + 4)), q_amax_t, q_g, ra);
-          const uint32_t sb = nvfp4_block_scale(fmaxf(bf16x8_absmax(pk + 8), bf16x8_absmax(pk + 12)), q_amax_t, q_g, rb);
+          // block scales: S = E4M3((amax_b 448) / amax_t), r = 1 / (S g) from the table
+          const float ba = fmaxf(bf16x8_absmax(pk), bf16x8_absmax(pk + 4));
+          const float bb = fmaxf(bf16x8_absmax(pk + 8), bf16x8_absmax(pk + 12));
+          const uint32_t sa = e4m3_encode(q_amax_t == 0.f ? 0.f : __fdiv_rn(__fmul_rn(ba, 448.f), q_amax_t));
+          const uint32_t sb = e4m3_encode(q_amax_t == 0.f ? 0.f : __fdiv_rn(__fmul_rn(bb, 448.f), q_amax_t));
+          const float ra = q_rtab[sa], rb = q_rtab[sb];
           if (m < p.M) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) q_run = __vmaxu2(q_run, pk[j] & 0x7FFF7FFFu);
+            q_run = __vmaxu2(q_run, __float_as_uint(fmaxf(ba, bb)) >> 16);   // the chunk's |bf16 y| max
             uint4 w;
             w.x = nvfp4_codes8(pk, ra);
             w.y = nvfp4_codes8(pk + 4, ra);

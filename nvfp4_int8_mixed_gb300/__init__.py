@@ -274,9 +274,12 @@ def mxcache(n: int, device=None) -> torch.Tensor:
     return torch.zeros(nb, dtype=torch.uint8, device=dev)
 
 
-def block_gamma(xin, xout, delta=None, gamma_out=None, r2_out=None, tdc_state=None, computed=None):
+def block_gamma(xin, xout, delta=None, gamma_out=None, r2_out=None, tdc_state=None, computed=None, ws=None):
     """a7: Gamma (and Delta in place, r2, TDC counters). Returns (gamma [1], r2 [1]).
-    delta: the bf16 update, or a uint8 compressed cache (mxcache)."""
+    delta: the bf16 update, or a uint8 compressed cache (mxcache).  ws: scratch
+    of sixbit_workspace_size(n, 1) bytes, zeroed before its first use (default:
+    the device's shared scratch; a pass running on another stream at the same
+    time as other library calls needs its own)."""
     _need_cuda(xin, xout)
     n = xin.numel()
     dev = xin.device
@@ -284,7 +287,7 @@ def block_gamma(xin, xout, delta=None, gamma_out=None, r2_out=None, tdc_state=No
     r2 = r2_out if r2_out is not None else torch.full((1,), float("nan"), dtype=torch.float32, device=dev)
     name = "sixbit_block_gamma_mxcache" if delta is not None and delta.dtype == torch.uint8 else "sixbit_block_gamma"
     _check(name, getattr(lib(), name)(_ptr(xin), _ptr(xout), n, _ptr(delta), _ptr(g), _ptr(r2), _ptr(tdc_state),
-                                      _ptr(computed), _ptr(_ws_for(n)), _stream()))
+                                      _ptr(computed), _ptr(ws if ws is not None else _ws_for(n)), _stream()))
     return g, r2
 
 

@@ -34,6 +34,26 @@ def test_gamma_delta_r2(M, H):
     assert host(state).tolist() == [2, 0]
 
 
+@pytest.mark.parametrize("M,H", [(7, 333), (synthetic.M_2B, 1920)])
+def test_gamma_with_caller_scratch(M, H):
+    """The pass with its own scratch (`ws`, zeroed, sixbit_workspace_size(n, 1)
+    bytes) matches the oracle bit for bit, twice in a row on the same
+    scratch (the last CTA leaves its counter at zero for the next call)."""
+    sb = _sb()
+    p = synthetic.gamma_pair(M + 3 * H, M, H)
+    ws = torch.zeros(int(sb.lib().sixbit_workspace_size(M * H, 1)), dtype=torch.uint8, device="cuda")
+    rg = o_gamma.gamma(p["xin"], p["xout"])
+    rdn = o_gamma.delta(p["xin"], p["xout"])
+    rr2 = o_gamma.rel_l2_sq(rdn, p["delta_prev"])
+    for _ in range(2):
+        xin, xout, dprev = dev_bf16(p["xin"]), dev_bf16(p["xout"]), dev_bf16(p["delta_prev"])
+        state = torch.tensor([1, 0], dtype=torch.int32, device="cuda")
+        g, r2 = sb.block_gamma(xin, xout, delta=dprev, tdc_state=state, ws=ws)
+        torch.cuda.synchronize()
+        assert host(g)[0] == rg and host(r2)[0] == rr2
+        assert np.array_equal(host_bf16_bits(dprev), rdn)
+
+
 def test_gamma_deterministic_and_skipped_block():
     sb = _sb()
     p = synthetic.gamma_pair(3, 1000, 333)

@@ -161,10 +161,8 @@ template <> struct Block16<float> {
 // every warp always has a load in flight.  Consecutive warps take
 // consecutive items (adjacent memory).
 template <typename T>
-__device__ __forceinline__ void nvfp4_load_item(const T* __restrict__ x, int64_t item, int64_t ppr, int nspan,
-                                                int nblk, int64_t M, int64_t ldx, int lane, Block16<T> (&blk)[2]) {
-  const int64_t m = item / ppr;
-  const int sp0 = int(item - m * ppr) * 2;
+__device__ __forceinline__ void nvfp4_load_item(const T* __restrict__ x, int64_t m, int sp0, int nspan, int nblk,
+                                                int64_t M, int64_t ldx, int lane, Block16<T> (&blk)[2]) {
 #pragma unroll
   for (int u = 0; u < 2; ++u) {
     const int b = (sp0 + u) * 32 + lane;
@@ -190,12 +188,20 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(const T* __restri
   const int64_t items = Mpad * ppr;
   const int64_t warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
+  // Item it = (row m, span pair pr), it = m * ppr + pr.  A warp's items are
+  // nwarps apart, i.e. dq rows and dr pairs: (m, pr) advance by additions.
+  const int64_t dq = nwarps / ppr;
+  const int dr = int(nwarps - dq * ppr);
+  int64_t m = warp / ppr;
+  int pr = int(warp - m * ppr);
   Block16<T> cur[2], nxt[2];
-  if (warp < items) nvfp4_load_item(x, warp, ppr, nspan, nblk, M, ldx, lane, cur);
+  if (warp < items) nvfp4_load_item(x, m, 2 * pr, nspan, nblk, M, ldx, lane, cur);
   for (int64_t it = warp; it < items; it += nwarps) {
-    if (it + nwarps < items) nvfp4_load_item(x, it + nwarps, ppr, nspan, nblk, M, ldx, lane, nxt);
-    const int64_t m = it / ppr;
-    const int sp0 = int(it - m * ppr) * 2;
+    int64_t mn = m + dq;                      // the next item, it + nwarps
+    int prn = pr + dr;
+    if (prn >= int(ppr)) { prn -= int(ppr); ++mn; }
+    if (it + nwarps < items) nvfp4_load_item(x, mn, 2 * prn, nspan, nblk, M, ldx, lane, nxt);
+    const int sp0 = 2 * pr;
     const bool row_ok = m < M;
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
@@ -204,7 +210,11 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(const T* __restri
       float r;
       const uint32_t sb = nvfp4_block_scale(cur[u].amax(), amax_t, g, r);
       uint32_t w0 = 0, w1 = 0;
-      if (r != 0.f) {
+      if constexpr (sizeof(T) == 2) {
+        // bf16 pairs times r on the f32x2 pipe (no add follows, so no fusion)
+        w0 = nvfp4_codes8(&cur[u].v[0].x, r);
+        w1 = nvfp4_codes8(&cur[u].v[1].x, r);
+      } else if (r != 0.f) {
         float y[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) y[e] = __fmul_rn(cur[u].at(e), r);
@@ -221,6 +231,8 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(const T* __restri
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u) cur[u] = nxt[u];
+    m = mn;
+    pr = prn;
   }
 }
 

@@ -334,8 +334,13 @@ __global__ void __launch_bounds__(kThreads) int8_planes_kernel(const int8_t* __r
   const int64_t gpr = K / 16;                      // 16-code groups per row
   const int64_t total = M * gpr;
   const int64_t plane_stride = M * (K / 2);
-  for (int64_t gi = int64_t(blockIdx.x) * kThreads + threadIdx.x; gi < total; gi += int64_t(gridDim.x) * kThreads) {
-    const int64_t m = gi / gpr, c = gi - m * gpr;
+  // group gi = (row m, group c), gi = m * gpr + c; the grid stride is dq rows
+  // and dc groups, so (m, c) advance by additions
+  const int64_t stride = int64_t(gridDim.x) * kThreads;
+  const int64_t dq = stride / gpr, dc = stride - dq * gpr;
+  const int64_t g0 = int64_t(blockIdx.x) * kThreads + threadIdx.x;
+  int64_t m = g0 / gpr, c = g0 - m * gpr;
+  for (int64_t gi = g0; gi < total; gi += stride) {
     const uint4 v = ldg_nc_v4(q + m * ldq + c * 16);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t p0[2], p1[2], p2[2];
@@ -350,6 +355,12 @@ __global__ void __launch_bounds__(kThreads) int8_planes_kernel(const int8_t* __r
     *reinterpret_cast<uint2*>(base) = make_uint2(p0[0], p0[1]);
     *reinterpret_cast<uint2*>(base + plane_stride) = make_uint2(p1[0], p1[1]);
     *reinterpret_cast<uint2*>(base + 2 * plane_stride) = make_uint2(p2[0], p2[1]);
+    m += dq;
+    c += dc;
+    if (c >= gpr) {
+      c -= gpr;
+      ++m;
+    }
   }
 }
 

@@ -180,6 +180,14 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(const T* __restri
   const float amax_t = *amax_ptr;
   const float g = nvfp4_global_scale(amax_t);
   if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+  // 1 / (S g) for every E4M3 scale a satfinite encode can give (codes
+  // 0..126), computed once per CTA exactly as the per-block form would
+  __shared__ float rtab[128];
+  if (threadIdx.x < 128) {
+    const float d = __fmul_rn(e4m3_decode(threadIdx.x), g);
+    rtab[threadIdx.x] = d != 0.f ? __frcp_rn(d) : 0.f;
+  }
+  __syncthreads();
   const int lane = threadIdx.x & 31;
   const int64_t kc4 = K / 16;                 // K % 64 == 0 -> a multiple of 4
   const int nblk = int(K / 16);
@@ -208,7 +216,9 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(const T* __restri
       if (sp0 + u >= nspan) break;            // warp-uniform
       const int b = (sp0 + u) * 32 + lane;
       float r;
-      const uint32_t sb = nvfp4_block_scale(cur[u].amax(), amax_t, g, r);
+      const float amax_b = cur[u].amax();
+      const uint32_t sb = e4m3_encode(amax_t == 0.f ? 0.f : __fdiv_rn(__fmul_rn(amax_b, 448.f), amax_t));
+      r = rtab[sb];
       uint32_t w0 = 0, w1 = 0;
       if constexpr (sizeof(T) == 2) {
         // bf16 pairs times r on the f32x2 pipe (no add follows, so no fusion)

@@ -523,6 +523,16 @@ __global__ void __launch_bounds__(kLnThreads<NB>) ln_quant_kernel(const LnQuantC
   const float amax_t = a.hist ? __fmul_rn(a.headroom, hist_prev(a.hist)) : 0.f;
   const float g = nvfp4_global_scale(amax_t);
   if (nv && blockIdx.x == 0 && threadIdx.x == 0) *a.g_out = g;
+  // 1 / (S g) for every E4M3 scale a satfinite encode can give (codes
+  // 0..126), computed once per CTA exactly as the per-block form would
+  __shared__ float rtab[128];
+  if (nv) {
+    for (int i = threadIdx.x; i < 128; i += LT) {
+      const float d = __fmul_rn(e4m3_decode(uint32_t(i)), g);
+      rtab[i] = d != 0.f ? __frcp_rn(d) : 0.f;
+    }
+    __syncthreads();
+  }
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t(blockIdx.x) * LT + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * LT) >> 5;
@@ -635,8 +645,8 @@ __global__ void __launch_bounds__(kLnThreads<NB>) ln_quant_kernel(const LnQuantC
       for (int i = 0; i < NB; ++i) {
         if (i * 32 >= nblk) break;               // warp-uniform
         const int64_t b = int64_t(i) * 32 + lane;
-        float r;
-        const uint32_t sb = nvfp4_block_scale(bmax[i], amax_t, g, r);
+        const uint32_t sb = e4m3_encode(amax_t == 0.f ? 0.f : __fdiv_rn(__fmul_rn(bmax[i], 448.f), amax_t));
+        const float r = rtab[sb];
         const uint32_t w0 = nvfp4_codes8(&v[i][0].x, r), w1 = nvfp4_codes8(&v[i][1].x, r);
         uint32_t word = sb | (__shfl_down_sync(0xffffffffu, sb, 1) << 8);
         word |= __shfl_down_sync(0xffffffffu, word, 2) << 16;

@@ -169,11 +169,11 @@ int sixbit_qlinear_w4a8(const uint8_t* a_planes, const float* row_scale, int64_t
  * once), summed by one fixed tree -- 8192-element tiles; in a tile, lane t
  * of 256 adds elements j*2048 + 8t + e (j < 4, e < 8) in order in float32;
  * lanes combine by a butterfly within each 32 (t^16, ..., t^1), then the 8
- * group sums by halving; tile sums are added in float64 by 256 lanes (tile
- * k to lane k % 256, in order) and halved; Gamma = f32(S1/S0),
- * r2 = f32(Sd/So).  The result depends only on the input, never on the
- * grid or the GPU.  ws: sixbit_workspace_size(n, 1) bytes (256 + 16 per
- * tile). */
+ * group sums by halving; tile sums are added in float64 into 256 chains
+ * (tile k to chain k % 256, in order) and the chain sums are halved;
+ * Gamma = f32(S1/S0), r2 = f32(Sd/So).  The result depends only on the
+ * input, never on the GPU.  ws: sixbit_workspace_size(n, 1) bytes (a
+ * 256-byte header and 4 doubles a chain: 8448 bytes whatever n). */
 int sixbit_block_gamma(const void* in, const void* out, int64_t n, void* delta,
                        float* gamma_out, float* r2_out, int32_t* tdc_state,
                        const uint8_t* computed, void* ws, sixbit_stream_t stream);
@@ -184,18 +184,17 @@ int sixbit_block_gamma(const void* in, const void* out, int64_t n, void* delta,
  * or code running where allocation is not allowed (a plugin's enqueue step,
  * a latency-critical loop that cannot take cudaMalloc's implicit device
  * synchronization).  Same arguments and results as sixbit_block_gamma
- * without `ws`; n <= SIXBIT_NOALLOC_GAMMA_MAX_ELEMS, else SIXBIT_ESHAPE and
- * nothing is launched.  The scratch is a fixed 262,400-byte device array
- * inside the library that every device loading the library holds until the
+ * without `ws`; n <= SIXBIT_NOALLOC_GAMMA_MAX_ELEMS (the limit of
+ * sixbit_block_gamma), else SIXBIT_ESHAPE and nothing is launched.  The
+ * scratch is a fixed 8448-byte device array inside the library (the same
+ * layout as `ws`) that every device loading the library holds until the
  * process exits.  The first call on a device looks up that array's device
  * address (with the device current), so make that first call before any
  * stream capture.  Every call clears the array's counter (an async memset on
  * `stream`) and then reuses it, so calls whose kernels overlap on the GPU --
  * on different streams, or on different host threads -- race and must be
- * avoided.  Allocates no device memory.  262,400 bytes = a 256-byte header
- * plus 16 bytes for each of the 16,384 tiles of 8192 elements that the
- * 2^27-element limit allows. */
-#define SIXBIT_NOALLOC_GAMMA_MAX_ELEMS (((int64_t)1) << 27)
+ * avoided.  Allocates no device memory. */
+#define SIXBIT_NOALLOC_GAMMA_MAX_ELEMS (((int64_t)1) << 40)
 int sixbit_block_gamma_noalloc(const void* in, const void* out, int64_t n, void* delta,
                                float* gamma_out, float* r2_out, int32_t* tdc_state,
                                const uint8_t* computed, sixbit_stream_t stream);

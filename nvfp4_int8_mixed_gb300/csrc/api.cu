@@ -47,8 +47,8 @@ int device_setup(int* num_sms, int** err) {
 }
 
 // Scratch layout: [0, 4) CTA counter of the Gamma pass (and of the pair
-// statistics), [64, 68) tensor amax, [256, ...) 4 floats per 8192-element
-// tile of those passes.
+// statistics), [64, 68) tensor amax, [256, 8448) the 4 float64 sums of each
+// of the 256 reduction chains of those passes.
 constexpr size_t kWsAmaxOffset = 64;
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -218,7 +218,7 @@ int sixbit_block_gamma(const void* in, const void* out, int64_t n, void* delta, 
   if (!aligned16(in) || !aligned16(out) || (delta && !aligned16(delta)) || !aligned16(ws)) return kEAlign;
   int sms;
   if (device_setup(&sms, nullptr) != kOk) return kELaunch;
-  return launch_block_gamma(in, out, n, delta, gamma_out, r2_out, tdc_state, computed, ws, sms, cs(stream));
+  return launch_block_gamma(in, out, n, delta, gamma_out, r2_out, tdc_state, computed, ws, cs(stream));
 }
 
 int sixbit_block_gamma_noalloc(const void* in, const void* out, int64_t n, void* delta, float* gamma_out,
@@ -228,7 +228,7 @@ int sixbit_block_gamma_noalloc(const void* in, const void* out, int64_t n, void*
   if (!aligned16(in) || !aligned16(out) || (delta && !aligned16(delta))) return kEAlign;
   int sms;
   if (device_setup(&sms, nullptr) != kOk) return kELaunch;
-  return launch_block_gamma_noalloc(in, out, n, delta, gamma_out, r2_out, tdc_state, computed, sms, cs(stream));
+  return launch_block_gamma_noalloc(in, out, n, delta, gamma_out, r2_out, tdc_state, computed, cs(stream));
 }
 
 int sixbit_pair_stats(const void* a, int a_dtype, const void* b, int b_dtype, int64_t n, double* out, void* ws,
@@ -240,7 +240,7 @@ int sixbit_pair_stats(const void* a, int a_dtype, const void* b, int b_dtype, in
   if (!aligned16(a) || !aligned16(b) || !aligned16(ws) || (reinterpret_cast<uintptr_t>(out) & 7u)) return kEAlign;
   int sms;
   if (device_setup(&sms, nullptr) != kOk) return kELaunch;
-  return launch_pair_stats(a, a_dtype == SIXBIT_F32, b, b_dtype == SIXBIT_F32, n, out, ws, sms, cs(stream));
+  return launch_pair_stats(a, a_dtype == SIXBIT_F32, b, b_dtype == SIXBIT_F32, n, out, ws, cs(stream));
 }
 
 int sixbit_dmpq_assign(const float* gamma, const float* alpha, const float* beta, const int32_t* layer_block,
@@ -277,7 +277,7 @@ int sixbit_block_gamma_mxcache(const void* in, const void* out, int64_t n, void*
   if (!aligned16(in) || !aligned16(out) || (cache && !aligned16(cache)) || !aligned16(ws)) return kEAlign;
   int sms;
   if (device_setup(&sms, nullptr) != kOk) return kELaunch;
-  return launch_block_gamma_mx(in, out, n, cache, gamma_out, r2_out, tdc_state, computed, ws, sms, cs(stream));
+  return launch_block_gamma_mx(in, out, n, cache, gamma_out, r2_out, tdc_state, computed, ws, cs(stream));
 }
 
 int sixbit_tdc_decide_and_apply_mxcache(const void* in, const void* cache, int64_t n, const float* r2, float tau_tdc,

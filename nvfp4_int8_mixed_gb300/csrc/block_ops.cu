@@ -21,7 +21,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kTile = 8192;                   // elements per tile of the Gamma pass
 constexpr int kVecPerThread = kTile / (8 * kThreads);   // 4 x 16-byte vectors per operand
-constexpr int kGammaCtasPerSm = 3;
+constexpr int kGammaCtasPerSm = 2;          // 256 CTAs on 152 SMs: at most two per SM
 
 struct GammaWs {                              // layout of the scratch buffer
   unsigned int counter;                       // CTAs finished (reset by the last one)
@@ -29,34 +29,41 @@ struct GammaWs {                              // layout of the scratch buffer
 };
 
 // The fixed reduction tree of the Gamma pass (and of the pair statistics).
-// Its result depends only on the input, never on the grid:
+// Its result depends only on the input, never on the device:
 //   * lane t of a tile (t = 0..255) owns elements j*2048 + 8t + e (j = 0..3,
 //     e = 0..7) and adds their terms one at a time in increasing element
 //     order, in float32 (round to nearest, no contraction);
 //   * the 256 lane sums: a butterfly inside each warp (partners t^16, t^8,
 //     t^4, t^2, t^1), then the 8 warp sums by w + (w+4), + (w+2), + (w+1);
-//   * tile sums go to scratch as float32; the last CTA widens them to
-//     float64, thread k adds tiles k, k+256, ... in order, and the 256
-//     thread sums are halved (k + (k+128), ..., + (k+1)).
-// All partials of one tile: 4 floats.
+//   * the float32 tile sums are widened to float64 and added in order into
+//     256 chains, chain k holding tiles k, k+256, ... (starting from +0);
+//   * the 256 chain sums are halved (k + (k+128), ..., + (k+1)).
+// The grid is min(tiles, 256) CTAs and CTA k walks exactly the tiles of
+// chain k, so it adds them into its chain as it goes; the last CTA to finish
+// only halves the 256 chain sums.  (Reading every tile partial back in one
+// CTA had cost 13 us at 34M elements: float64 throughput on one SM.)
+constexpr int kChains = 256;
+static_assert(kChains == kThreads, "the last CTA halves one chain sum per thread");
 
 // Per-tile combine of 4 lane sums, batched: each warp's butterfly result
 // goes to shared memory slot `it % kBatch` (it = the CTA's tile counter);
 // after every kBatch tiles (and after the last) one CTA barrier, threads
-// 0..4*kBatch-1 each combine one (tile, sum) over the 8 warps and store it,
-// and a second barrier frees the slots.  Two barriers per kBatch tiles
-// instead of one per tile.
+// 0..4*kBatch-1 each combine one (tile, sum) over the 8 warps into `part`,
+// and a second barrier frees the slots; then threads 0..3 add the batch's
+// tile sums, in tile order, into this CTA's chain.  Two barriers per kBatch
+// tiles instead of one per tile.  `part` is next written after the next
+// batch's first barrier, which threads 0..3 reach only after reading it.
 constexpr int kBatch = 32;
 struct TileRed {
   float w[kBatch][kThreads / 32][4];
+  float part[kBatch][4];
 };
-__device__ __forceinline__ void tile_combine4(float v[4], TileRed& red, int it, int64_t t, bool flush,
-                                              float* tile_part, int64_t tile_stride) {
+__device__ __forceinline__ void tile_combine4(float v[4], TileRed& red, int it, bool flush, double& chain) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int h = 16; h > 0; h >>= 1) v[i] = __fadd_rn(v[i], __shfl_xor_sync(0xffffffffu, v[i], h));
+    for (int o = 16; o > 0; o >>= 1) v[i] = __fadd_rn(v[i], __shfl_xor_sync(0xffffffffu, v[i], o));
   const int slot = it % kBatch;
   if (lane == 0)
 #pragma unroll
@@ -72,44 +79,53 @@ __device__ __forceinline__ void tile_combine4(float v[4], TileRed& red, int it, 
       for (int h = kThreads / 64; h > 0; h >>= 1)
 #pragma unroll
         for (int k = 0; k < h; ++k) g[k] = __fadd_rn(g[k], g[k + h]);
-      // slot b held tile t - (slot - b) * tile_stride
-      tile_part[4 * (t - int64_t(slot - b) * tile_stride) + i] = g[0];
+      red.part[b][i] = g[0];
     }
     __syncthreads();
+    if (threadIdx.x < 4)
+      for (int b = 0; b <= slot; ++b) chain = __dadd_rn(chain, double(red.part[b][threadIdx.x]));
   }
 }
 
-// End of a pass over tile partials: the last CTA to finish reduces them in
-// float64 by the fixed tree and returns true in thread 0 with the 4 sums.
-__device__ __forceinline__ bool tiles_finish(int64_t ntiles, GammaWs* ws, const float* tile_part, double out[4]) {
+// End of a pass: every CTA stores its 4 chain sums (threads 0..3 hold them);
+// the last CTA to finish halves the 256 chains' sums (chains of CTAs that do
+// not exist, when tiles < 256, are +0) and returns true in thread 0 with the
+// 4 sums.
+__device__ __forceinline__ bool tiles_finish(GammaWs* ws, double* chains, double chain, double out[4]) {
   __shared__ bool is_last;
   __shared__ double dsm[kThreads][4];
-  if (threadIdx.x < 4) __threadfence();       // this CTA's tile partials, before the ticket
+  if (threadIdx.x < 4) {
+    chains[4 * blockIdx.x + threadIdx.x] = chain;
+    __threadfence();                          // this CTA's chain sums, before the ticket
+  }
   __syncthreads();
   if (threadIdx.x == 0) is_last = atomicAdd(&ws->counter, 1u) == gridDim.x - 1;
   __syncthreads();
   if (!is_last) return false;
   __threadfence();
-  double acc[4] = {0.0, 0.0, 0.0, 0.0};
-  for (int64_t t = threadIdx.x; t < ntiles; t += kThreads) {
-    const float4 p = __ldcg(reinterpret_cast<const float4*>(tile_part) + t);
-    acc[0] += double(p.x);
-    acc[1] += double(p.y);
-    acc[2] += double(p.z);
-    acc[3] += double(p.w);
-  }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) dsm[threadIdx.x][i] = acc[i];
+  for (int i = 0; i < 4; ++i) dsm[threadIdx.x][i] = threadIdx.x < gridDim.x ? __ldcg(chains + 4 * threadIdx.x + i) : 0.0;
   __syncthreads();
-  for (int h = kThreads / 2; h > 0; h >>= 1) {
+  // halving: partners 128, 64, 32 apart through shared memory, then 16..1
+  // apart by shuffles inside warp 0 (lane k adds lane k + h; lanes >= h
+  // compute values that no later level reads)
+  for (int h = kThreads / 2; h >= 32; h >>= 1) {
     if (threadIdx.x < h)
 #pragma unroll
       for (int i = 0; i < 4; ++i) dsm[threadIdx.x][i] = __dadd_rn(dsm[threadIdx.x][i], dsm[threadIdx.x + h][i]);
     __syncthreads();
   }
+  if (threadIdx.x >= 32) return false;
+  double r[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) r[i] = dsm[threadIdx.x][i];
+#pragma unroll
+  for (int h = 16; h > 0; h >>= 1)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] = __dadd_rn(r[i], __shfl_down_sync(0xffffffffu, r[i], h));
   if (threadIdx.x != 0) return false;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) out[i] = dsm[0][i];
+  for (int i = 0; i < 4; ++i) out[i] = r[i];
   ws->counter = 0u;
   return true;
 }
@@ -139,13 +155,14 @@ __device__ __forceinline__ float add_sq(float acc, float x) { return __fadd_rn(a
 // are in flight.
 __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_kernel(
     const uint16_t* __restrict__ xin, const uint16_t* __restrict__ xout, int64_t n, uint16_t* delta, float* gamma_out,
-    float* r2_out, int32_t* tdc_state, const uint8_t* computed_ptr, GammaWs* ws, float* tile_part) {
+    float* r2_out, int32_t* tdc_state, const uint8_t* computed_ptr, GammaWs* ws, double* chains) {
   __shared__ TileRed red;
   const bool computed = computed_ptr ? (*computed_ptr != 0) : true;
   const bool do_delta = computed && delta != nullptr;
   const bool do_r2 = do_delta && r2_out != nullptr && (tdc_state ? tdc_state[0] >= 1 : true);
   const int64_t ntiles = cdiv(n, kTile);
   int it = 0;
+  double chain = 0.0;                         // this CTA's chain (threads 0..3)
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
     const int64_t base = t * kTile;
     float v[4] = {0.f, 0.f, 0.f, 0.f};          // lane sums S1, S0, Sd, So of this tile
@@ -200,10 +217,10 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_kernel(
         }
       }
     }
-    tile_combine4(v, red, it, t, t + gridDim.x >= ntiles, tile_part, gridDim.x);
+    tile_combine4(v, red, it, t + gridDim.x >= ntiles, chain);
   }
   double S[4];
-  if (tiles_finish(ntiles, ws, tile_part, S)) gamma_publish(S, do_r2, computed, gamma_out, r2_out, tdc_state);
+  if (tiles_finish(ws, chains, chain, S)) gamma_publish(S, do_r2, computed, gamma_out, r2_out, tdc_state);
 }
 
 // a7 with the compressed update cache (an extension; layout in common.cuh):
@@ -215,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_kernel(
 // before its own write).  n % 32 == 0.
 __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_mx_kernel(
     const uint16_t* __restrict__ xin, const uint16_t* __restrict__ xout, int64_t n, uint8_t* cache, float* gamma_out,
-    float* r2_out, int32_t* tdc_state, const uint8_t* computed_ptr, GammaWs* ws, float* tile_part) {
+    float* r2_out, int32_t* tdc_state, const uint8_t* computed_ptr, GammaWs* ws, double* chains) {
   __shared__ TileRed red;
   const bool computed = computed_ptr ? (*computed_ptr != 0) : true;
   const bool do_delta = computed && cache != nullptr;
@@ -225,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_mx_kernel(
   const bool first = (lane & 3) == 0;
   const int64_t ntiles = cdiv(n, kTile);
   int it = 0;
+  double chain = 0.0;                         // this CTA's chain (threads 0..3)
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
     const int64_t base = t * kTile;
     float v[4] = {0.f, 0.f, 0.f, 0.f};          // lane sums S1, S0, Sd, So of this tile (missing elements add +0)
@@ -293,10 +311,10 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_mx_kernel(
         }
       }
     }
-    tile_combine4(v, red, it, t, t + gridDim.x >= ntiles, tile_part, gridDim.x);
+    tile_combine4(v, red, it, t + gridDim.x >= ntiles, chain);
   }
   double S[4];
-  if (tiles_finish(ntiles, ws, tile_part, S)) gamma_publish(S, do_r2, computed, gamma_out, r2_out, tdc_state);
+  if (tiles_finish(ws, chains, chain, S)) gamma_publish(S, do_r2, computed, gamma_out, r2_out, tdc_state);
 }
 
 // Calibration diagnostic (DMPQ side, Figures 1 and 4): one pass over two
@@ -323,10 +341,11 @@ template <typename TA, typename TB>
 __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) pair_stats_kernel(const TA* __restrict__ a,
                                                                                const TB* __restrict__ b, int64_t n,
                                                                                double* out, GammaWs* ws,
-                                                                               float* tile_part) {
+                                                                               double* chains) {
   __shared__ TileRed red;
   const int64_t ntiles = cdiv(n, kTile);
   int it = 0;
+  double chain = 0.0;                         // this CTA's chain (threads 0..3)
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
     float v[4] = {0.f, 0.f, 0.f, 0.f};          // lane sums of (a-b)^2, b^2, a*b, a^2
 #pragma unroll
@@ -344,10 +363,10 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) pair_stats_kernel(c
         v[3] = add_sq(v[3], va[e]);
       }
     }
-    tile_combine4(v, red, it, t, t + gridDim.x >= ntiles, tile_part, gridDim.x);
+    tile_combine4(v, red, it, t + gridDim.x >= ntiles, chain);
   }
   double S[4];
-  if (tiles_finish(ntiles, ws, tile_part, S))
+  if (tiles_finish(ws, chains, chain, S))
 #pragma unroll
     for (int i = 0; i < 4; ++i) out[i] = S[i];
 }
@@ -672,22 +691,21 @@ __global__ void __launch_bounds__(kLnThreads<NB>) ln_quant_kernel(const LnQuantC
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// Scratch of a pass over n elements: the CTA counter, then 4 floats a tile.
+// Scratch of a pass: the CTA counter, then 4 float64 chain sums per CTA.
 constexpr size_t kWsHeader = 256;
-size_t tiles_ws_bytes(int64_t n) { return kWsHeader + size_t(cdiv(n, kTile)) * 4 * sizeof(float); }
+constexpr size_t kWsBytes = kWsHeader + size_t(kChains) * 4 * sizeof(double);   // 8448, whatever n
+size_t tiles_ws_bytes(int64_t) { return kWsBytes; }
 
 // Scratch-free Gamma pass.  Some callers cannot give this library scratch
 // memory: their device memory is entirely planned by another allocator, or
 // they run where allocating is not allowed (a plugin's enqueue step, a
 // latency-critical loop that cannot afford cudaMalloc's implicit device
-// synchronization).  For them the pass keeps its CTA counter and per-tile
-// partial sums in this fixed device array instead of caller scratch.  The
-// array lives on every device that loads the library, until the process
-// exits, and bounds the tensor size to kNoAllocMaxElems.
-constexpr int64_t kNoAllocMaxElems = int64_t(1) << 27;                  // 134,217,728 elements
-constexpr size_t kNoAllocBytes = kWsHeader + size_t(kNoAllocMaxElems / kTile) * 4 * sizeof(float);   // 262,400
-static_assert(kNoAllocBytes == 262400, "no-alloc scratch: header + 16384 tiles x 16 bytes");
-static __device__ __align__(256) unsigned char g_gamma_scratch[kNoAllocBytes];
+// synchronization).  For them the pass keeps its CTA counter and chain sums
+// in this fixed device array instead of caller scratch.  The array lives on
+// every device that loads the library, until the process exits; its size
+// does not depend on n, so the size limit is that of the regular pass.
+constexpr int64_t kNoAllocMaxElems = int64_t(1) << 40;
+static __device__ __align__(256) unsigned char g_gamma_scratch[kWsBytes];
 
 namespace {
 constexpr int kNoAllocMaxDevices = 64;
@@ -713,61 +731,60 @@ void* noalloc_scratch_for_current_device() {
 int64_t block_gamma_noalloc_max_elems() { return kNoAllocMaxElems; }
 
 int launch_block_gamma_noalloc(const void* xin, const void* xout, int64_t n, void* delta, float* gamma_out,
-                               float* r2_out, int32_t* tdc_state, const uint8_t* computed, int num_sms,
-                               cudaStream_t s) {
+                               float* r2_out, int32_t* tdc_state, const uint8_t* computed, cudaStream_t s) {
   if (n > kNoAllocMaxElems) return kEShape;
   void* scratch = noalloc_scratch_for_current_device();
   if (!scratch) return kELaunch;
   // The array keeps the previous call's contents: the CTA counter must start at 0.
   if (cudaMemsetAsync(scratch, 0, 256, s) != cudaSuccess) return kELaunch;
-  return launch_block_gamma(xin, xout, n, delta, gamma_out, r2_out, tdc_state, computed, scratch, num_sms, s);
+  return launch_block_gamma(xin, xout, n, delta, gamma_out, r2_out, tdc_state, computed, scratch, s);
 }
 
-int gamma_grid(int64_t n, int num_sms) {
+// One CTA per chain of the reduction tree: the grid is fixed by n alone.
+int gamma_grid(int64_t n) {
   const int64_t tiles = cdiv(n, kTile);
-  const int64_t g = int64_t(num_sms) * kGammaCtasPerSm;
-  return int(tiles < g ? tiles : g);
+  return int(tiles < kChains ? tiles : kChains);
 }
 
 size_t gamma_ws_bytes(int64_t n) { return tiles_ws_bytes(n); }
 
 int launch_block_gamma(const void* xin, const void* xout, int64_t n, void* delta, float* gamma_out, float* r2_out,
-                       int32_t* tdc_state, const uint8_t* computed, void* ws, int num_sms, cudaStream_t s) {
+                       int32_t* tdc_state, const uint8_t* computed, void* ws, cudaStream_t s) {
   GammaWs* w = static_cast<GammaWs*>(ws);
-  float* parts = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
-  gamma_kernel<<<unsigned(gamma_grid(n, num_sms)), kThreads, 0, s>>>(
+  double* chains = reinterpret_cast<double*>(static_cast<char*>(ws) + kWsHeader);
+  gamma_kernel<<<unsigned(gamma_grid(n)), kThreads, 0, s>>>(
       static_cast<const uint16_t*>(xin), static_cast<const uint16_t*>(xout), n, static_cast<uint16_t*>(delta),
-      gamma_out, r2_out, tdc_state, computed, w, parts);
+      gamma_out, r2_out, tdc_state, computed, w, chains);
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 
 int launch_block_gamma_mx(const void* xin, const void* xout, int64_t n, void* cache, float* gamma_out, float* r2_out,
-                          int32_t* tdc_state, const uint8_t* computed, void* ws, int num_sms, cudaStream_t s) {
+                          int32_t* tdc_state, const uint8_t* computed, void* ws, cudaStream_t s) {
   GammaWs* w = static_cast<GammaWs*>(ws);
-  float* parts = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
-  gamma_mx_kernel<<<unsigned(gamma_grid(n, num_sms)), kThreads, 0, s>>>(
+  double* chains = reinterpret_cast<double*>(static_cast<char*>(ws) + kWsHeader);
+  gamma_mx_kernel<<<unsigned(gamma_grid(n)), kThreads, 0, s>>>(
       static_cast<const uint16_t*>(xin), static_cast<const uint16_t*>(xout), n, static_cast<uint8_t*>(cache),
-      gamma_out, r2_out, tdc_state, computed, w, parts);
+      gamma_out, r2_out, tdc_state, computed, w, chains);
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 
 int launch_pair_stats(const void* a, int a_f32, const void* b, int b_f32, int64_t n, double* out, void* ws,
-                      int num_sms, cudaStream_t s) {
+                      cudaStream_t s) {
   GammaWs* w = static_cast<GammaWs*>(ws);
-  float* parts = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
-  const unsigned grid = unsigned(gamma_grid(n, num_sms));
+  double* chains = reinterpret_cast<double*>(static_cast<char*>(ws) + kWsHeader);
+  const unsigned grid = unsigned(gamma_grid(n));
   if (!a_f32 && !b_f32)
     pair_stats_kernel<uint16_t, uint16_t><<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(a),
-                                                                    static_cast<const uint16_t*>(b), n, out, w, parts);
+                                                                    static_cast<const uint16_t*>(b), n, out, w, chains);
   else if (!a_f32)
     pair_stats_kernel<uint16_t, float><<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(a),
-                                                                 static_cast<const float*>(b), n, out, w, parts);
+                                                                 static_cast<const float*>(b), n, out, w, chains);
   else if (!b_f32)
     pair_stats_kernel<float, uint16_t><<<grid, kThreads, 0, s>>>(static_cast<const float*>(a),
-                                                                 static_cast<const uint16_t*>(b), n, out, w, parts);
+                                                                 static_cast<const uint16_t*>(b), n, out, w, chains);
   else
     pair_stats_kernel<float, float><<<grid, kThreads, 0, s>>>(static_cast<const float*>(a), static_cast<const float*>(b),
-                                                              n, out, w, parts);
+                                                              n, out, w, chains);
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 

@@ -79,11 +79,11 @@ def test_host_helpers(lib):
     assert lib.sixbit_sf_bytes(256, 256) == 256 * 16
     assert lib.sixbit_sf_bytes(200, 1920) == 256 * 120        # rows padded to 128
     assert lib.sixbit_sf_bytes(1, 64) == 128 * 4
-    # Gamma pass scratch: a 256-byte header plus 4 float32 tile sums per
-    # 8192-element tile (17776 * 1920 elements: 4167 tiles)
-    assert lib.sixbit_workspace_size(17776, 1920) == 256 + 16 * 4167
-    assert lib.sixbit_workspace_size(1, 64) == 512                  # at least 512 bytes (the amax slot)
-    assert lib.sixbit_workspace_size(1 << 27, 1) == 262400          # the scratch-free variant's limit
+    # Gamma pass scratch: a 256-byte header, then 4 doubles for each of the
+    # 256 reduction chains, whatever the size
+    assert lib.sixbit_workspace_size(17776, 1920) == 256 + 256 * 4 * 8
+    assert lib.sixbit_workspace_size(1, 64) == 8448
+    assert lib.sixbit_workspace_size(1 << 27, 1) == 8448
 
 
 def test_argument_errors_before_launch(lib):

@@ -64,6 +64,6 @@ def test_noalloc_rejects_sizes_beyond_its_limit():
     import nvfp4_int8_mixed_gb300 as sb
     x = torch.zeros(64, dtype=torch.bfloat16, device="cuda")
     g = torch.zeros(1, device="cuda")
-    too_big = (1 << 27) + 1                             # SIXBIT_NOALLOC_GAMMA_MAX_ELEMS + 1: rejected before any launch
+    too_big = (1 << 40) + 1                             # SIXBIT_NOALLOC_GAMMA_MAX_ELEMS + 1: rejected before any launch
     rc = sb.lib().sixbit_block_gamma_noalloc(_p(x), _p(x), too_big, None, _p(g), None, None, None, None)
     assert rc == sb.ESHAPE

@@ -160,10 +160,18 @@ __device__ __forceinline__ uint32_t nvfp4_codes8(const uint32_t* pw, float r) {
   for (int e = 0; e < 4; ++e) f2_unpack(f2_mul(f2_from_bf16x2(pw[e]), r2), y[2 * e], y[2 * e + 1]);
   return e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
 }
+// max(|a|, |b|) of each bf16 half in one instruction.  The magnitude is one
+// of the inputs' magnitudes, unrounded; the sign bit of each half is the XOR
+// of the inputs' signs, so callers mask it off once at the end.  Finite
+// inputs only (a NaN gives the canonical NaN).
+__device__ __forceinline__ uint32_t bf16x2_maxabs(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 // |x| max of eight bf16 values (four packed words), as a float.
 __device__ __forceinline__ float bf16x8_absmax(const uint32_t* pw) {
-  uint32_t a = __vmaxu2(pw[0] & 0x7FFF7FFFu, pw[1] & 0x7FFF7FFFu);
-  a = __vmaxu2(a, __vmaxu2(pw[2] & 0x7FFF7FFFu, pw[3] & 0x7FFF7FFFu));
+  const uint32_t a = bf16x2_maxabs(bf16x2_maxabs(pw[0], pw[1]), bf16x2_maxabs(pw[2], pw[3])) & 0x7FFF7FFFu;
   return __uint_as_float(max(a & 0xFFFFu, a >> 16) << 16);
 }
 

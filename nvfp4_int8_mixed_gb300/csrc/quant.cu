@@ -119,12 +119,9 @@ template <> struct Block16<uint16_t> {
   __device__ void load(const uint16_t* p) { v[0] = ldg_v4(p); v[1] = ldg_v4(p + 8); }
   __device__ void zero() { v[0] = v[1] = make_uint4(0, 0, 0, 0); }
   __device__ float amax() const {
-    uint32_t a = 0;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      a = __vmaxu2(a, v[i].x & 0x7FFF7FFFu); a = __vmaxu2(a, v[i].y & 0x7FFF7FFFu);
-      a = __vmaxu2(a, v[i].z & 0x7FFF7FFFu); a = __vmaxu2(a, v[i].w & 0x7FFF7FFFu);
-    }
+    const uint32_t a0 = bf16x2_maxabs(bf16x2_maxabs(v[0].x, v[0].y), bf16x2_maxabs(v[0].z, v[0].w));
+    const uint32_t a1 = bf16x2_maxabs(bf16x2_maxabs(v[1].x, v[1].y), bf16x2_maxabs(v[1].z, v[1].w));
+    const uint32_t a = bf16x2_maxabs(a0, a1) & 0x7FFF7FFFu;
     return __uint_as_float(max(a & 0xFFFFu, a >> 16) << 16);
   }
   __device__ float at(int i) const {               // element i (compile-time i after unrolling)
@@ -291,10 +288,9 @@ __global__ void __launch_bounds__(128) int8_quant_kernel(const uint16_t* __restr
     } else {
       uint32_t acc = 0;
 #pragma unroll
-      for (int i = 0; i < NVL; ++i) {
-        acc = __vmaxu2(acc, v[i].x & 0x7FFF7FFFu); acc = __vmaxu2(acc, v[i].y & 0x7FFF7FFFu);
-        acc = __vmaxu2(acc, v[i].z & 0x7FFF7FFFu); acc = __vmaxu2(acc, v[i].w & 0x7FFF7FFFu);
-      }
+      for (int i = 0; i < NVL; ++i)
+        acc = bf16x2_maxabs(acc, bf16x2_maxabs(bf16x2_maxabs(v[i].x, v[i].y), bf16x2_maxabs(v[i].z, v[i].w)));
+      acc &= 0x7FFF7FFFu;
       amax = warp_max(__uint_as_float(max(acc & 0xFFFFu, acc >> 16) << 16));
       if (WPR > 1) {
         if (lane == 0) red[warp] = amax;

@@ -795,52 +795,65 @@ def gemm_set_report(G, T, fp4_peak: float, hbm: float, workload: str):
             "tdc_ms": mean_t["tdc"] * 1e3}
 
 
-def time_nvfp4_amax_given(sb, G, dev, reps=24):
-    """The NVFP4 quantizer's encode pass alone, with the tensor amax supplied
-    (as a producer supplies it), on each distinct K of the set.  `reps`
-    launches, rotating over copies of the activation whose total exceeds
-    300 MB (so each launch reads its input from HBM and no flush leaves dirty
-    lines to be written back during a timed launch), are captured as one CUDA
-    graph; the replay is timed with CUDA events on the launching stream and
-    divided by `reps` (median of 5 replays): the average launch duration
-    with no host launch gap inside it."""
+def _graph_launch_mean(fn, reps):
+    """Mean duration of one launch: `reps` calls fn(0..reps-1) captured as one
+    CUDA graph, the replay timed with CUDA events on the launching stream and
+    divided by `reps` (median of 5 replays), so no host launch gap is inside."""
     import torch
+    for i in range(3):
+        fn(i)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(reps):
+            fn(i)
+    graph.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ts = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) / 1e3 / reps)
+    del graph
+    return float(np.median(ts))
+
+
+def time_quantizers_graph(sb, G, dev, reps=24):
+    """Each activation quantizer alone, on each distinct K of the set: the
+    NVFP4 encode pass with the tensor amax supplied (as a producer supplies
+    it), and the INT8 quantizer writing the digit planes and row scales the
+    W4A8 GEMM reads.  The launches rotate over copies of the activation whose
+    total exceeds 300 MB, so each launch reads its input from HBM and no
+    flush leaves dirty lines to be written back during a timed launch.  The
+    per-launch figures of the step graph include its timing-event nodes;
+    these do not."""
     peak = float(load_peaks()[0]["hbm_gbs"])
-    out, seen = {}, set()
+    nv, i8, seen = {}, {}, set()
     for l in G["L"]:
         if l["K"] in seen:
             continue
         seen.add(l["K"])
         nbuf = max(2, -(-(300 << 20) // (l["x"].numel() * 2)))
         xs = [l["x"]] + [l["x"].clone() for _ in range(nbuf - 1)]
+        note = {"inputs": f"{nbuf} copies rotated ({nbuf * l['x'].numel() * 2 / 1e6:.0f} MB > L2)",
+                "timing": f"graph of {reps} launches, per-launch mean"}
         amax, _ = sb.amax(l["x"])
-        fn = lambda i: sb.quantize_act_nvfp4(xs[i % nbuf], amax_in=amax, out=(l["codes"], l["sf"], l["ga"]))
-        for i in range(3):
-            fn(i)
-        torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            for i in range(reps):
-                fn(i)
-        graph.replay()
-        torch.cuda.synchronize()
-        stream = torch.cuda.current_stream()
-        ts = []
-        for _ in range(5):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            graph.replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1) / 1e3 / reps)
-        sb.get_error()
-        del graph, xs
-        t = float(np.median(ts))
+        t = _graph_launch_mean(lambda i: sb.quantize_act_nvfp4(xs[i % nbuf], amax_in=amax,
+                                                                out=(l["codes"], l["sf"], l["ga"])), reps)
         nb = quant_bytes("nvfp4", G["M"], l["K"])
-        out[f"K={l['K']}"] = {"us": t * 1e6, "GB/s": nb / t / 1e9, "frac_hbm": nb / t / 1e9 / peak,
-                              "inputs": f"{nbuf} copies rotated ({nbuf * l['x'].numel() * 2 / 1e6:.0f} MB > L2)",
-                              "timing": f"graph of {reps} launches, per-launch mean"}
-    return out
+        nv[f"K={l['K']}"] = {"us": t * 1e6, "GB/s": nb / t / 1e9, "frac_hbm": nb / t / 1e9 / peak, **note}
+        t = _graph_launch_mean(lambda i: sb.quantize_act_int8(xs[i % nbuf], out=(None, l["planes"], l["s"])), reps)
+        nb = quant_bytes("int8", G["M"], l["K"])
+        i8[f"K={l['K']}"] = {"us": t * 1e6, "GB/s": nb / t / 1e9, "frac_hbm": nb / t / 1e9 / peak,
+                             "bytes_note": "method's 3 B/element; the kernel writes 1.5 B of digit planes in place "
+                                           "of the 1 B code", **note}
+        sb.get_error()
+        del xs
+    return nv, i8
 
 
 def run_ours(args):
@@ -977,7 +990,7 @@ def run_ours(args):
     extra = {}
     if rank == 0 and args.workload == "2b":
         extra["quantizing_producers"] = time_producers(sb, L, dev, (tl["bin"], tl["bout"]))
-        extra["quant_nvfp4_amax_given"] = time_nvfp4_amax_given(sb, G, dev)
+        extra["quant_nvfp4_amax_given"], extra["quant_int8_graph"] = time_quantizers_graph(sb, G, dev)
     del G, T
     torch.cuda.empty_cache()
 

@@ -276,7 +276,9 @@ int sixbit_tdc_decide_and_apply_mxcache(const void* in, const void* cache, int64
 
 /* Block harness: LayerNorm without affine over rows of H, eps given,
  * fp32 statistics, bf16 out.  Optional side outputs for the next quantizer:
- * amax_out (tensor max |y|, zeroed by the call) and row_amax_out [M]. */
+ * amax_out (tensor max |y|, zeroed by the call) and row_amax_out [M].
+ * Rows may be staged through shared memory by bulk copies; a bounded wait
+ * for one that gives up sets the device error word (sixbit_get_error). */
 int sixbit_layernorm_bf16(const void* x, int64_t M, int64_t H, int64_t ldx, float eps,
                           void* y, int64_t ldy, float* amax_out, float* row_amax_out,
                           const uint8_t* pred, sixbit_stream_t stream);

@@ -302,8 +302,9 @@ int sixbit_layernorm_bf16(const void* x, int64_t M, int64_t H, int64_t ldx, floa
   if (H % 8 != 0 || ldx % 8 != 0 || ldy % 8 != 0) return kEShape;
   if (!aligned16(x) || !aligned16(y)) return kEAlign;
   int sms;
-  if (device_setup(&sms, nullptr) != kOk) return kELaunch;
-  return launch_layernorm(x, M, H, ldx, eps, y, ldy, amax_out, row_amax_out, pred, sms, cs(stream));
+  int* err;
+  if (device_setup(&sms, &err) != kOk) return kELaunch;
+  return launch_layernorm(x, M, H, ldx, eps, y, ldy, amax_out, row_amax_out, pred, err, sms, cs(stream));
 }
 
 int sixbit_layernorm_quant(const void* x, int64_t M, int64_t H, int64_t ldx, float eps, void* y, int64_t ldy,
@@ -323,12 +324,13 @@ int sixbit_layernorm_quant(const void* x, int64_t M, int64_t H, int64_t ldx, flo
       (planes && !aligned16(planes)) || (amax_hist && !aligned16(amax_hist)))
     return kEAlign;
   int sms;
-  if (device_setup(&sms, nullptr) != kOk) return kELaunch;
+  int* err;
+  if (device_setup(&sms, &err) != kOk) return kELaunch;
   LnQuantCall c = {};
   c.x = static_cast<const uint16_t*>(x); c.M = M; c.H = H; c.ldx = ldx; c.eps = eps;
   c.y = static_cast<uint16_t*>(y); c.ldy = ldy;
   c.codes = codes; c.sf = sf; c.g_out = g_out; c.hist = amax_hist; c.headroom = headroom; c.nv_pred = nv_pred;
-  c.planes = planes; c.row_scale = row_scale; c.i8_pred = i8_pred; c.pred = pred;
+  c.planes = planes; c.row_scale = row_scale; c.i8_pred = i8_pred; c.pred = pred; c.err = err;
   return launch_ln_quant(c, sms, cs(stream));
 }
 

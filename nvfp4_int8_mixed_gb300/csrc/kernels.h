@@ -36,7 +36,7 @@ int launch_tdc(const void* xin, const void* delta, int64_t n, const float* r2, f
                const int32_t* tdc_state, uint8_t* compute_out, void* out, uint8_t* gates, int32_t n_gates,
                int num_sms, cudaStream_t s);
 int launch_layernorm(const void* x, int64_t M, int64_t H, int64_t ldx, float eps, void* y, int64_t ldy,
-                     float* amax_out, float* row_amax_out, const uint8_t* pred, int num_sms, cudaStream_t s);
+                     float* amax_out, float* row_amax_out, const uint8_t* pred, int* err, int num_sms, cudaStream_t s);
 
 // LayerNorm that also quantizes its output (NVFP4 by delayed scaling, INT8
 // exact per row); every output pointer is optional.  H % 16 == 0 and
@@ -60,6 +60,7 @@ struct LnQuantCall {
   float* row_scale;
   const uint8_t* i8_pred;
   const uint8_t* pred;
+  int* err;                  // device error word: set when a bounded row wait gives up
 };
 int launch_ln_quant(const LnQuantCall& c, int num_sms, cudaStream_t s);
 

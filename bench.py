@@ -856,6 +856,36 @@ def time_quantizers_graph(sb, G, dev, reps=24):
     return nv, i8
 
 
+def time_gemms_graph(sb, G, fp4_peak, hbm, reps=10):
+    """Each GEMM of the set alone: `reps` launches over rotated copies of its
+    activation operand (more than 300 MB in all, so every launch reads it
+    from HBM), captured as one CUDA graph; the per-launch mean, with the same
+    roofline fields as the step's figures.  The step's per-launch figures
+    include its timing-event nodes; these do not."""
+    out = {}
+    M = G["M"]
+    for l in G["L"]:
+        sb.quantize_act_nvfp4(l["x"], out=(l["codes"], l["sf"], l["ga"]))
+        sb.quantize_act_int8(l["x"], out=(None, l["planes"], l["s"]))
+        ops = {"w4a4": ((l["codes"], l["sf"]),
+                        lambda a, l=l: sb.qlinear_w4a4(a[0], a[1], l["ga"], l["wc"], l["wsf"], l["gw"], residual=l["r"],
+                                                       gelu=l["gelu"], out=l["y4"])),
+               "w4a8": ((l["planes"], l["s"]),
+                        lambda a, l=l: sb.qlinear_w4a8(a[0], a[1], l["wc"], l["wsf"], l["gw"], residual=l["r"],
+                                                       gelu=l["gelu"], out=l["y8"]))}
+        for mode, (a0, call) in ops.items():
+            nb = sum(t.numel() * t.element_size() for t in a0)
+            nbuf = max(2, -(-(300 << 20) // nb))
+            bufs = [a0] + [tuple(t.clone() for t in a0) for _ in range(nbuf - 1)]
+            t = _graph_launch_mean(lambda i: call(bufs[i % nbuf]), reps)
+            r = gemm_roofline(mode, M, l["N"], l["K"], l["r"] is not None, t, fp4_peak, hbm)
+            r["inputs"] = f"{nbuf} copies of the activation operand rotated ({nbuf * nb / 1e6:.0f} MB > L2)"
+            out[f"{mode}[{l['name']}]"] = r
+            del bufs
+        sb.get_error()
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -991,6 +1021,7 @@ def run_ours(args):
     if rank == 0 and args.workload == "2b":
         extra["quantizing_producers"] = time_producers(sb, L, dev, (tl["bin"], tl["bout"]))
         extra["quant_nvfp4_amax_given"], extra["quant_int8_graph"] = time_quantizers_graph(sb, G, dev)
+        extra["gemm_graph"] = time_gemms_graph(sb, G, fp4_peak, hbm)
     del G, T
     torch.cuda.empty_cache()
 

@@ -148,11 +148,10 @@ __device__ __forceinline__ float add_sq(float acc, float x) { return __fadd_rn(a
 //   d = f32(out) - f32(in); S1 += |d|; S0 += |in|;
 //   if computed: D_new = bf16(d) (stored over D_old); if r2 wanted:
 //   e = f32(D_new) - f32(D_old); Sd += e*e; So += D_old^2.
-// The sums follow the fixed tree above.  Persistent CTAs walk the tiles
-// t = blockIdx, blockIdx + grid, ...; each tile's float32 partials go to
-// scratch and the last CTA reduces them, writes Gamma / r2 and advances the
-// TDC counters.  Three CTAs per SM: while some compute, the others' loads
-// are in flight.
+// The sums follow the fixed tree above: CTA k walks the tiles of chain k
+// (t = k, k + 256, ...) and the last CTA to finish halves the chain sums,
+// writes Gamma / r2 and advances the TDC counters.  With at most two CTAs
+// on an SM, one CTA's loads are in flight while the other computes.
 __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_kernel(
     const uint16_t* __restrict__ xin, const uint16_t* __restrict__ xout, int64_t n, uint16_t* delta, float* gamma_out,
     float* r2_out, int32_t* tdc_state, const uint8_t* computed_ptr, GammaWs* ws, double* chains) {

@@ -134,7 +134,7 @@ def test_tdc_decide_and_apply(fresh, consec, r2, tau, max_skip, refresh, step):
         assert not host_bf16_bits(out).any() and host(gates).all()
 
 
-@pytest.mark.parametrize("M,H", [(256, 256), (17776, 1920), (5, 3072)])
+@pytest.mark.parametrize("M,H", [(256, 256), (17776, 1920), (5, 3072), (17776, 1024), (6000, 4096)])
 def test_layernorm(M, H):
     sb = _sb()
     x = synthetic.activations(synthetic.rng(M), M, H, 2, 30.0)

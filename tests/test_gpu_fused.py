@@ -57,7 +57,10 @@ def _check_int8(planes, rs, yf, rows):
     assert np.array_equal(host(planes)[:, rows], ref)
 
 
-@pytest.mark.parametrize("M,H", [(300, 256), (1, 64), (129, 1920), (17776, 1920), (5, 3072)])
+@pytest.mark.parametrize("M,H", [(300, 256), (1, 64), (129, 1920), (17776, 1920), (5, 3072),
+                                 # enough rows that every warp of the row-prefetch forms refills its buffers:
+                                 # 2 blocks a lane (8-warp CTAs), 6 and 8 blocks a lane (4-warp CTAs)
+                                 (17776, 1024), (6000, 3072), (5000, 4096)])
 def test_layernorm_quant_parity(M, H):
     sb = _sb()
     x = synthetic.activations(synthetic.rng(M + H), M, H, max(1, H // 100), 10.0, 50.0)

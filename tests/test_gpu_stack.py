@@ -72,6 +72,9 @@ def test_stack_decisions_and_outputs(tau_tdc, max_skip, refresh, fused, cache):
         r = codecs.bf16_to_f32(ref["outputs"][t]).astype(np.float64)
         rel = np.linalg.norm(g - r) / np.linalg.norm(r)
         assert rel <= 2e-3, (t, rel)
+        # The oracle's Gamma here is taken on the oracle's own block tensors, which
+        # differ from the device's within the output tolerance above; on the
+        # device's tensors Gamma and r2 are bit-exact (the test below).
         assert np.allclose(rec["gamma"][t], ref["gammas"][t], rtol=2e-3, atol=0), t
     flags = np.array(rec["flags"][1:])
     assert flags.any() and not flags.all()          # a real NVFP4 / INT8 mix after step 0

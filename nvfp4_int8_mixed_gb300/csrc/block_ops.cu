@@ -16,6 +16,16 @@
 
 namespace sixbit {
 
+// Test switch (set through sixbit_debug_stall_layernorm): nonzero makes every
+// warp of the LayerNorm producer's row-prefetch form wait, for its first row,
+// on a barrier that is never signalled, so that bounded wait expires and the
+// device-error path runs.
+__device__ int g_sixbit_stall_ln = 0;
+
+int set_ln_stall(int on) {
+  return cudaMemcpyToSymbol(g_sixbit_stall_ln, &on, sizeof(on)) == cudaSuccess ? kOk : kELaunch;
+}
+
 namespace {
 
 constexpr int kThreads = 256;
@@ -565,7 +575,7 @@ __global__ void __launch_bounds__(kLnThreads<NB>) ln_quant_kernel(const LnQuantC
   constexpr int LT = kLnThreads<NB>;
   if (a.pred && *a.pred == 0) return;
   extern __shared__ __align__(128) uint8_t ln_rows[];   // [LT / 32][kLnBufs][2 H] bytes
-  __shared__ __align__(8) uint64_t ln_bar[LT / 32][kLnBufs];
+  __shared__ __align__(8) uint64_t ln_bar[LT / 32][kLnBufs + 1];   // + one never signalled (test switch)
   __shared__ uint32_t lut[256];
   __shared__ float red[LT / 32];
   const bool nv = a.codes != nullptr && (a.nv_pred == nullptr || *a.nv_pred != 0);
@@ -599,7 +609,7 @@ __global__ void __launch_bounds__(kLnThreads<NB>) ln_quant_kernel(const LnQuantC
   const uint32_t rbar = uint32_t(__cvta_generic_to_shared(&ln_bar[wib][0]));
   if (PF && lane == 0) {
 #pragma unroll
-    for (int j = 0; j < kLnBufs; ++j) ln_bar_init(rbar + 8u * j);
+    for (int j = 0; j <= kLnBufs; ++j) ln_bar_init(rbar + 8u * j);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 #pragma unroll
     for (int j = 0; j < kLnBufs; ++j)          // the warp's first rows
@@ -621,7 +631,8 @@ __global__ void __launch_bounds__(kLnThreads<NB>) ln_quant_kernel(const LnQuantC
     if constexpr (PF) {
       const int j = int(k % kLnBufs);
       const uint32_t par = uint32_t(k / kLnBufs) & 1u;
-      if (!__all_sync(0xffffffffu, ln_bar_wait(rbar + 8u * j, par))) {
+      const bool stall = k == 0 && g_sixbit_stall_ln != 0;   // test switch: wait on the silent barrier
+      if (!__all_sync(0xffffffffu, ln_bar_wait(stall ? rbar + 8u * kLnBufs : rbar + 8u * j, par))) {
         // Give up: flag it, let the copies still in flight land (bounded), stop.
         if (lane == 0 && a.err) atomicExch(a.err, int(kErrWaitTimeout));
         for (int d = 1; d < kLnBufs; ++d)

@@ -1,4 +1,5 @@
-"""The device-error path of the linear layers, made to run on purpose.
+"""The device-error paths of the linear layers and the LayerNorm producers,
+made to run on purpose.
 
 Every mbarrier wait in the GEMM is bounded.  The test switch
 sixbit_debug_stall_gemm(1) makes the MMA-issuing thread wait on a barrier
@@ -16,7 +17,7 @@ import torch
 
 import synthetic
 from oracle import codecs, gemm as o_gemm, int8 as o_int8, nvfp4 as o_nvfp4
-from tests.helpers import assert_gemm_close, dev, dev_bf16, host
+from tests.helpers import assert_gemm_close, dev, dev_bf16, host, host_bf16_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -66,3 +67,48 @@ def test_expired_wait_reports_edevice_then_the_next_call_is_clean(residual):
     res = lay["residual"] if residual else None
     assert_gemm_close(host(y4), o_gemm.w4a4(rac, rasf, rga, rwc, rwsf, rgw, residual=res), "f32")
     assert_gemm_close(host(y8), o_gemm.w4a8(rq, rs, rwc, rwsf, rgw, residual=res), "f32")
+
+
+@pytest.mark.parametrize("quant", [False, True])
+def test_layernorm_expired_row_wait_reports_edevice_then_the_next_call_is_clean(quant):
+    """The LayerNorm producer's row-prefetch form (bulk copies into shared
+    memory, one bounded mbarrier wait a row): sixbit_debug_stall_layernorm(1)
+    makes each warp wait for its first row on a barrier nothing signals.  The
+    wait gives up, the kernel records SIXBIT_EDEVICE after letting its own
+    row copies land, and the next normal call on the same stream is clean."""
+    import nvfp4_int8_mixed_gb300 as sb
+    from oracle import block as o_block
+    lib = sb.lib()
+    stream = sb._stream()
+    # bf16 output with rows of 1920 (8-warp CTAs), or INT8 with rows of 3072 (4-warp CTAs):
+    # both take the prefetch form
+    M, H = (600, 3072) if quant else (600, 1920)
+    x = synthetic.activations(synthetic.rng(M + H), M, H, 4, 10.0, 50.0)
+    xd = dev_bf16(x)
+    y = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    planes = torch.empty((3, M, H // 2), dtype=torch.uint8, device="cuda")
+    rs = torch.empty(M, device="cuda")
+    run = (lambda: sb.layernorm_quant(xd, int8=(planes, rs))) if quant else (lambda: sb.layernorm(xd, out=y))
+    assert lib.sixbit_get_error(stream) == sb.OK
+    assert lib.sixbit_debug_stall_layernorm(1) == sb.OK
+    try:
+        t0 = time.perf_counter()
+        run()                                              # the launch itself succeeds
+        rc = lib.sixbit_get_error(stream)
+        dt = time.perf_counter() - t0
+        assert rc == sb.EDEVICE, rc
+        assert dt < 60.0, dt                               # the waits gave up in bounded time
+        print(f"expired row wait reported after {dt:.2f} s")
+        assert lib.sixbit_get_error(stream) == sb.OK
+    finally:
+        assert lib.sixbit_debug_stall_layernorm(0) == sb.OK
+    run()
+    assert lib.sixbit_get_error(stream) == sb.OK
+    ref = codecs.bf16_to_f32(o_block.layernorm(x)).astype(np.float64)
+    if quant:
+        got = host(rs).astype(np.float64)                  # row scales = |y| row max / 127
+        want = np.max(np.abs(ref), axis=1) / 127.0
+        assert np.all(np.abs(got - want) <= 2.0 ** -7 * want + 1e-9)
+    else:
+        got = codecs.bf16_to_f32(host_bf16_bits(y)).astype(np.float64)
+        assert np.all(np.abs(got - ref) <= 2.0 ** -7 * np.abs(ref) + 1e-6)

@@ -217,8 +217,9 @@ int sixbit_block_gamma(const void* in, const void* out, int64_t n, void* delta, 
   if (n > (int64_t(1) << 40)) return kEShape;
   if (!aligned16(in) || !aligned16(out) || (delta && !aligned16(delta)) || !aligned16(ws)) return kEAlign;
   int sms;
-  if (device_setup(&sms, nullptr) != kOk) return kELaunch;
-  return launch_block_gamma(in, out, n, delta, gamma_out, r2_out, tdc_state, computed, ws, cs(stream));
+  int* err;
+  if (device_setup(&sms, &err) != kOk) return kELaunch;
+  return launch_block_gamma(in, out, n, delta, gamma_out, r2_out, tdc_state, computed, ws, err, cs(stream));
 }
 
 int sixbit_block_gamma_noalloc(const void* in, const void* out, int64_t n, void* delta, float* gamma_out,
@@ -227,8 +228,9 @@ int sixbit_block_gamma_noalloc(const void* in, const void* out, int64_t n, void*
   if (n > block_gamma_noalloc_max_elems()) return kEShape;
   if (!aligned16(in) || !aligned16(out) || (delta && !aligned16(delta))) return kEAlign;
   int sms;
-  if (device_setup(&sms, nullptr) != kOk) return kELaunch;
-  return launch_block_gamma_noalloc(in, out, n, delta, gamma_out, r2_out, tdc_state, computed, cs(stream));
+  int* err;
+  if (device_setup(&sms, &err) != kOk) return kELaunch;
+  return launch_block_gamma_noalloc(in, out, n, delta, gamma_out, r2_out, tdc_state, computed, err, cs(stream));
 }
 
 int sixbit_pair_stats(const void* a, int a_dtype, const void* b, int b_dtype, int64_t n, double* out, void* ws,
@@ -276,8 +278,9 @@ int sixbit_block_gamma_mxcache(const void* in, const void* out, int64_t n, void*
   if (n % 32 != 0 || n > (int64_t(1) << 40)) return kEShape;
   if (!aligned16(in) || !aligned16(out) || (cache && !aligned16(cache)) || !aligned16(ws)) return kEAlign;
   int sms;
-  if (device_setup(&sms, nullptr) != kOk) return kELaunch;
-  return launch_block_gamma_mx(in, out, n, cache, gamma_out, r2_out, tdc_state, computed, ws, cs(stream));
+  int* err;
+  if (device_setup(&sms, &err) != kOk) return kELaunch;
+  return launch_block_gamma_mx(in, out, n, cache, gamma_out, r2_out, tdc_state, computed, ws, err, cs(stream));
 }
 
 int sixbit_tdc_decide_and_apply_mxcache(const void* in, const void* cache, int64_t n, const float* r2, float tau_tdc,

@@ -154,35 +154,107 @@ __device__ __forceinline__ void gamma_publish(const double S[4], bool do_r2, boo
 // acc + x*x with the product rounded once (no contraction into an FMA).
 __device__ __forceinline__ float add_sq(float acc, float x) { return __fadd_rn(acc, __fmul_rn(x, x)); }
 
+// Tile staging of the Gamma passes: thread 0 copies a tile's inputs into
+// shared memory with bulk copies (the TMA engine), completing on one mbarrier
+// per stage, two stages deep, so a CTA's next tile is in flight while it
+// works on the current one (at most two CTAs share an SM, and one CTA alone
+// on an SM would otherwise wait for every tile).  Each wait is bounded; a CTA
+// that gives up records the device error, lets its copies in flight land and
+// leaves its tile loop (its sums are then meaningless, the error says so).
+constexpr uint32_t kStageSpinCap = 1u << 22;  // polls of a bounded stage wait
+__device__ __forceinline__ void stage_bar_init(uint32_t bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar));
+}
+__device__ __forceinline__ bool stage_bar_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kStageSpinCap; ++i) {
+    uint32_t ok;
+    asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+__device__ __forceinline__ void stage_expect(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// bytes % 16 == 0, both addresses 16-byte aligned
+__device__ __forceinline__ void stage_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // a7: one pass over (in, out, previous Delta).  Per element:
 //   d = f32(out) - f32(in); S1 += |d|; S0 += |in|;
 //   if computed: D_new = bf16(d) (stored over D_old); if r2 wanted:
 //   e = f32(D_new) - f32(D_old); Sd += e*e; So += D_old^2.
 // The sums follow the fixed tree above: CTA k walks the tiles of chain k
 // (t = k, k + 256, ...) and the last CTA to finish halves the chain sums,
-// writes Gamma / r2 and advances the TDC counters.  With at most two CTAs
-// on an SM, one CTA's loads are in flight while the other computes.
+// writes Gamma / r2 and advances the TDC counters.  A tile's whole 8-element
+// groups arrive through the shared-memory stages; a partial last group is
+// read directly.
+constexpr size_t kGammaStage = size_t(3) * kTile * 2;    // in, out, Delta_old: 16 KB each
+constexpr size_t kGammaSmem = 2 * kGammaStage;             // 96 KB of dynamic shared memory
 __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_kernel(
     const uint16_t* __restrict__ xin, const uint16_t* __restrict__ xout, int64_t n, uint16_t* delta, float* gamma_out,
-    float* r2_out, int32_t* tdc_state, const uint8_t* computed_ptr, GammaWs* ws, double* chains) {
+    float* r2_out, int32_t* tdc_state, const uint8_t* computed_ptr, GammaWs* ws, double* chains, int* err) {
   __shared__ TileRed red;
+  __shared__ __align__(8) uint64_t sbar[2];
+  extern __shared__ __align__(128) uint8_t gstage[];   // [2 stages][in | out | Delta_old][kTile bf16]
   const bool computed = computed_ptr ? (*computed_ptr != 0) : true;
   const bool do_delta = computed && delta != nullptr;
   const bool do_r2 = do_delta && r2_out != nullptr && (tdc_state ? tdc_state[0] >= 1 : true);
   const int64_t ntiles = cdiv(n, kTile);
+  const uint32_t bar0 = uint32_t(__cvta_generic_to_shared(&sbar[0]));
+  const uint32_t sbase = uint32_t(__cvta_generic_to_shared(gstage));
+  auto issue = [&](int64_t t, int s) {       // tile t's whole 8-element groups into stage s
+    const int64_t base = t * kTile;
+    const uint32_t nb = uint32_t((n - base < kTile ? n - base : kTile) / 8 * 8) * 2u;
+    const uint32_t bar = bar0 + 8u * uint32_t(s), dst = sbase + uint32_t(s) * uint32_t(kGammaStage);
+    stage_expect(bar, nb * (do_r2 ? 3u : 2u));
+    if (nb) {
+      stage_copy(dst, xin + base, nb, bar);
+      stage_copy(dst + kTile * 2u, xout + base, nb, bar);
+      if (do_r2) stage_copy(dst + 2u * kTile * 2u, delta + base, nb, bar);
+    }
+  };
+  if (threadIdx.x == 0) {
+    stage_bar_init(bar0);
+    stage_bar_init(bar0 + 8u);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (blockIdx.x < ntiles) issue(blockIdx.x, 0);
+  }
+  __syncthreads();
   int it = 0;
   double chain = 0.0;                         // this CTA's chain (threads 0..3)
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
     const int64_t base = t * kTile;
+    const int s = it & 1;
+    const bool more = t + gridDim.x < ntiles;
+    // stage s ^ 1 was last read one tile ago, before that tile's closing barrier
+    if (threadIdx.x == 0 && more) issue(t + gridDim.x, s ^ 1);
+    const bool landed = stage_bar_wait(bar0 + 8u * uint32_t(s), uint32_t(it >> 1) & 1u);
+    if (__syncthreads_or(!landed)) {          // one verdict for the whole CTA
+      if (threadIdx.x == 0) {
+        if (err) atomicExch(err, int(kErrWaitTimeout));
+        stage_bar_wait(bar0 + 8u * uint32_t(s), uint32_t(it >> 1) & 1u);
+        if (more) stage_bar_wait(bar0 + 8u * uint32_t(s ^ 1), uint32_t((it + 1) >> 1) & 1u);
+      }
+      break;
+    }
+    const uint4* sv = reinterpret_cast<const uint4*>(gstage + size_t(s) * kGammaStage);
     float v[4] = {0.f, 0.f, 0.f, 0.f};          // lane sums S1, S0, Sd, So of this tile
     uint4 vi[kVecPerThread], vo[kVecPerThread], vd[kVecPerThread];
 #pragma unroll
     for (int i = 0; i < kVecPerThread; ++i) {
       const int64_t idx = base + (int64_t(i) * kThreads + threadIdx.x) * 8;
       if (idx + 8 <= n) {
-        vi[i] = ldg_nc_v4(xin + idx);
-        vo[i] = ldg_nc_v4(xout + idx);
-        if (do_r2) vd[i] = ldg_v4(delta + idx);
+        const int o = i * kThreads + threadIdx.x;   // 16-byte group within the tile
+        vi[i] = sv[o];
+        vo[i] = sv[kTile / 8 + o];
+        if (do_r2) vd[i] = sv[2 * (kTile / 8) + o];
       }
     }
 #pragma unroll
@@ -227,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_kernel(
       }
     }
     tile_combine4(v, red, it, t + gridDim.x >= ntiles, chain);
+    __syncthreads();                          // stage s read by every thread before it is refilled
   }
   double S[4];
   if (tiles_finish(ws, chains, chain, S)) gamma_publish(S, do_r2, computed, gamma_out, r2_out, tdc_state);
@@ -239,10 +312,17 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_kernel(
 // block (8 elements each): its maximum is two shuffles, and the first of the
 // four reads the old scale byte and writes the new one (so its read comes
 // before its own write).  n % 32 == 0.
+// Stage of the compressed-cache pass: in, out (16 KB each), the cached codes
+// (8 KB) and, for a whole tile, its 256 scale bytes (a partial last tile
+// reads its few scale bytes directly: a bulk copy moves multiples of 16 B).
+constexpr size_t kGammaMxStage = size_t(2) * kTile * 2 + kTile + kTile / 32;   // 41,216 bytes
+constexpr size_t kGammaMxSmem = 2 * kGammaMxStage;
 __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_mx_kernel(
     const uint16_t* __restrict__ xin, const uint16_t* __restrict__ xout, int64_t n, uint8_t* cache, float* gamma_out,
-    float* r2_out, int32_t* tdc_state, const uint8_t* computed_ptr, GammaWs* ws, double* chains) {
+    float* r2_out, int32_t* tdc_state, const uint8_t* computed_ptr, GammaWs* ws, double* chains, int* err) {
   __shared__ TileRed red;
+  __shared__ __align__(8) uint64_t sbar[2];
+  extern __shared__ __align__(128) uint8_t gstage[];   // [2 stages][in | out | codes | scales]
   const bool computed = computed_ptr ? (*computed_ptr != 0) : true;
   const bool do_delta = computed && cache != nullptr;
   const bool do_r2 = do_delta && r2_out != nullptr && (tdc_state ? tdc_state[0] >= 1 : true);
@@ -250,26 +330,63 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_mx_kernel(
   const int lane = threadIdx.x & 31;
   const bool first = (lane & 3) == 0;
   const int64_t ntiles = cdiv(n, kTile);
+  const uint32_t bar0 = uint32_t(__cvta_generic_to_shared(&sbar[0]));
+  const uint32_t sbase = uint32_t(__cvta_generic_to_shared(gstage));
+  auto issue = [&](int64_t t, int s) {       // tile t (n % 32 == 0: whole 32-element blocks) into stage s
+    const int64_t base = t * kTile;
+    const uint32_t el = uint32_t(n - base < kTile ? n - base : kTile);
+    const bool whole = el == uint32_t(kTile);
+    const uint32_t bar = bar0 + 8u * uint32_t(s), dst = sbase + uint32_t(s) * uint32_t(kGammaMxStage);
+    stage_expect(bar, 4u * el + (do_r2 ? el + (whole ? el / 32u : 0u) : 0u));
+    stage_copy(dst, xin + base, 2u * el, bar);
+    stage_copy(dst + 2u * kTile, xout + base, 2u * el, bar);
+    if (do_r2) {
+      stage_copy(dst + 4u * kTile, cache + base, el, bar);
+      if (whole) stage_copy(dst + 5u * kTile, scales + base / 32, el / 32u, bar);
+    }
+  };
+  if (threadIdx.x == 0) {
+    stage_bar_init(bar0);
+    stage_bar_init(bar0 + 8u);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (blockIdx.x < ntiles) issue(blockIdx.x, 0);
+  }
+  __syncthreads();
   int it = 0;
   double chain = 0.0;                         // this CTA's chain (threads 0..3)
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
     const int64_t base = t * kTile;
+    const int s = it & 1;
+    const bool more = t + gridDim.x < ntiles;
+    if (threadIdx.x == 0 && more) issue(t + gridDim.x, s ^ 1);   // read one tile ago, before its closing barrier
+    const bool landed = stage_bar_wait(bar0 + 8u * uint32_t(s), uint32_t(it >> 1) & 1u);
+    if (__syncthreads_or(!landed)) {          // one verdict for the whole CTA
+      if (threadIdx.x == 0) {
+        if (err) atomicExch(err, int(kErrWaitTimeout));
+        stage_bar_wait(bar0 + 8u * uint32_t(s), uint32_t(it >> 1) & 1u);
+        if (more) stage_bar_wait(bar0 + 8u * uint32_t(s ^ 1), uint32_t((it + 1) >> 1) & 1u);
+      }
+      break;
+    }
+    const uint8_t* st = gstage + size_t(s) * kGammaMxStage;
+    const bool whole = n - base >= kTile;
     float v[4] = {0.f, 0.f, 0.f, 0.f};          // lane sums S1, S0, Sd, So of this tile (missing elements add +0)
     uint4 vi[kVecPerThread], vo[kVecPerThread];
     uint2 vc[kVecPerThread];
     uint32_t vs[kVecPerThread];
 #pragma unroll
     for (int i = 0; i < kVecPerThread; ++i) {
-      const int64_t idx = base + (int64_t(i) * kThreads + threadIdx.x) * 8;
+      const int o = i * kThreads + threadIdx.x;     // 8-element group within the tile
+      const int64_t idx = base + int64_t(o) * 8;
       vi[i] = vo[i] = make_uint4(0, 0, 0, 0);
       vc[i] = make_uint2(0, 0);
       vs[i] = 0;
       if (idx < n) {                          // n % 32 == 0: whole 8-element groups
-        vi[i] = ldg_nc_v4(xin + idx);
-        vo[i] = ldg_nc_v4(xout + idx);
+        vi[i] = reinterpret_cast<const uint4*>(st)[o];
+        vo[i] = reinterpret_cast<const uint4*>(st + 2 * kTile)[o];
         if (do_r2) {
-          vc[i] = *reinterpret_cast<const uint2*>(cache + idx);
-          if (first) vs[i] = scales[idx / 32];
+          vc[i] = reinterpret_cast<const uint2*>(st + 4 * kTile)[o];
+          if (first) vs[i] = whole ? st[5 * kTile + o / 4] : scales[idx / 32];
         }
       }
     }
@@ -321,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_mx_kernel(
       }
     }
     tile_combine4(v, red, it, t + gridDim.x >= ntiles, chain);
+    __syncthreads();                          // stage s read by every thread before it is refilled
   }
   double S[4];
   if (tiles_finish(ws, chains, chain, S)) gamma_publish(S, do_r2, computed, gamma_out, r2_out, tdc_state);
@@ -820,13 +938,14 @@ void* noalloc_scratch_for_current_device() {
 int64_t block_gamma_noalloc_max_elems() { return kNoAllocMaxElems; }
 
 int launch_block_gamma_noalloc(const void* xin, const void* xout, int64_t n, void* delta, float* gamma_out,
-                               float* r2_out, int32_t* tdc_state, const uint8_t* computed, cudaStream_t s) {
+                               float* r2_out, int32_t* tdc_state, const uint8_t* computed, int* err,
+                               cudaStream_t s) {
   if (n > kNoAllocMaxElems) return kEShape;
   void* scratch = noalloc_scratch_for_current_device();
   if (!scratch) return kELaunch;
   // The array keeps the previous call's contents: the CTA counter must start at 0.
   if (cudaMemsetAsync(scratch, 0, 256, s) != cudaSuccess) return kELaunch;
-  return launch_block_gamma(xin, xout, n, delta, gamma_out, r2_out, tdc_state, computed, scratch, s);
+  return launch_block_gamma(xin, xout, n, delta, gamma_out, r2_out, tdc_state, computed, scratch, err, s);
 }
 
 // One CTA per chain of the reduction tree: the grid is fixed by n alone.
@@ -838,22 +957,28 @@ int gamma_grid(int64_t n) {
 size_t gamma_ws_bytes(int64_t n) { return tiles_ws_bytes(n); }
 
 int launch_block_gamma(const void* xin, const void* xout, int64_t n, void* delta, float* gamma_out, float* r2_out,
-                       int32_t* tdc_state, const uint8_t* computed, void* ws, cudaStream_t s) {
+                       int32_t* tdc_state, const uint8_t* computed, void* ws, int* err, cudaStream_t s) {
   GammaWs* w = static_cast<GammaWs*>(ws);
   double* chains = reinterpret_cast<double*>(static_cast<char*>(ws) + kWsHeader);
-  gamma_kernel<<<unsigned(gamma_grid(n)), kThreads, 0, s>>>(
+  // two tile stages: more than the default 48 KB of dynamic shared memory
+  if (cudaFuncSetAttribute(gamma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kGammaSmem)) != cudaSuccess)
+    return kELaunch;
+  gamma_kernel<<<unsigned(gamma_grid(n)), kThreads, kGammaSmem, s>>>(
       static_cast<const uint16_t*>(xin), static_cast<const uint16_t*>(xout), n, static_cast<uint16_t*>(delta),
-      gamma_out, r2_out, tdc_state, computed, w, chains);
+      gamma_out, r2_out, tdc_state, computed, w, chains, err);
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 
 int launch_block_gamma_mx(const void* xin, const void* xout, int64_t n, void* cache, float* gamma_out, float* r2_out,
-                          int32_t* tdc_state, const uint8_t* computed, void* ws, cudaStream_t s) {
+                          int32_t* tdc_state, const uint8_t* computed, void* ws, int* err, cudaStream_t s) {
   GammaWs* w = static_cast<GammaWs*>(ws);
   double* chains = reinterpret_cast<double*>(static_cast<char*>(ws) + kWsHeader);
-  gamma_mx_kernel<<<unsigned(gamma_grid(n)), kThreads, 0, s>>>(
+  if (cudaFuncSetAttribute(gamma_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kGammaMxSmem)) !=
+      cudaSuccess)
+    return kELaunch;
+  gamma_mx_kernel<<<unsigned(gamma_grid(n)), kThreads, kGammaMxSmem, s>>>(
       static_cast<const uint16_t*>(xin), static_cast<const uint16_t*>(xout), n, static_cast<uint8_t*>(cache),
-      gamma_out, r2_out, tdc_state, computed, w, chains);
+      gamma_out, r2_out, tdc_state, computed, w, chains, err);
   return cudaGetLastError() == cudaSuccess ? kOk : kELaunch;
 }
 

@@ -17,13 +17,14 @@ int launch_int8_quant(const void* x, int64_t M, int64_t K, int64_t ldx, const fl
 
 size_t gamma_ws_bytes(int64_t n);
 int launch_block_gamma(const void* xin, const void* xout, int64_t n, void* delta, float* gamma_out, float* r2_out,
-                       int32_t* tdc_state, const uint8_t* computed, void* ws, cudaStream_t s);
+                       int32_t* tdc_state, const uint8_t* computed, void* ws, int* err, cudaStream_t s);
 int64_t block_gamma_noalloc_max_elems();
 int launch_block_gamma_noalloc(const void* xin, const void* xout, int64_t n, void* delta, float* gamma_out,
-                               float* r2_out, int32_t* tdc_state, const uint8_t* computed, cudaStream_t s);
+                               float* r2_out, int32_t* tdc_state, const uint8_t* computed, int* err,
+                               cudaStream_t s);
 // The compressed update cache (E4M3 + power-of-two scale per 32 elements; n % 32 == 0).
 int launch_block_gamma_mx(const void* xin, const void* xout, int64_t n, void* cache, float* gamma_out, float* r2_out,
-                          int32_t* tdc_state, const uint8_t* computed, void* ws, cudaStream_t s);
+                          int32_t* tdc_state, const uint8_t* computed, void* ws, int* err, cudaStream_t s);
 int launch_tdc_mx(const void* xin, const void* cache, int64_t n, const float* r2, float tau2, int32_t max_skip,
                   int32_t refresh_every, const int32_t* step, const int32_t* tdc_state, uint8_t* compute_out,
                   void* out, uint8_t* gates, int32_t n_gates, int num_sms, cudaStream_t s);

@@ -352,17 +352,20 @@ int sixbit_qlinear_qout(int mode, const uint8_t* a, const uint8_t* a_sf, const f
  * sixbit_get_error() contract only. */
 int sixbit_debug_stall_gemm(int on);
 
-/* Test switch of the same kind for the LayerNorm producers (no counterpart
- * in the pages).  on != 0: in every LayerNorm launch on the current device
- * that stages its rows through shared memory (sixbit_layernorm_bf16 with
- * rows of up to 2048, sixbit_layernorm_quant writing a bf16 output with
- * rows of up to 2048 or a quantized output with longer rows), each warp
- * waits for its first row on a barrier nothing signals; the bounded wait
- * expires, the kernel records SIXBIT_EDEVICE, waits for its own row copies
- * in flight and stops, leaving the outputs undefined.  on = 0 restores
- * normal operation.  Synchronous; allocates nothing.  For tests of the
+/* Test switch of the same kind for the kernels that stage their inputs
+ * through shared memory with bulk copies (no counterpart in the pages):
+ * the LayerNorm producers in their row-prefetch form (sixbit_layernorm_bf16
+ * with rows of up to 2048, sixbit_layernorm_quant writing a bf16 output
+ * with rows of up to 2048 or a quantized output with longer rows) and the
+ * Gamma passes (sixbit_block_gamma, its scratch-free and compressed-cache
+ * forms).  on != 0: each warp (LayerNorm) or CTA (Gamma) waits for its first
+ * row or tile on a barrier nothing signals; the bounded wait expires, the
+ * kernel records SIXBIT_EDEVICE, waits for its own copies in flight and
+ * stops, leaving the outputs undefined (a Gamma pass still completes its
+ * CTA count, so the scratch stays consistent).  on = 0 restores normal
+ * operation.  Synchronous; allocates nothing.  For tests of the
  * sixbit_get_error() contract only. */
-int sixbit_debug_stall_layernorm(int on);
+int sixbit_debug_stall_staging(int on);
 
 /* Synchronizes `stream`, returns SIXBIT_EDEVICE if a device wait gave up
  * since the last call (and clears the word), else the stream's CUDA status

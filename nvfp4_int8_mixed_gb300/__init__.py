@@ -54,7 +54,7 @@ _SIGS = {
     "sixbit_qlinear_qout": ([_INT, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _I64, _P, _INT, _P, _I64, _P, _P, _P, _P,
                              _F, _P, _P, _P], _INT),
     "sixbit_debug_stall_gemm": ([_INT], _INT),
-    "sixbit_debug_stall_layernorm": ([_INT], _INT),
+    "sixbit_debug_stall_staging": ([_INT], _INT),
     "sixbit_int8_digit_planes": ([_P, _I64, _I64, _I64, _P, _P], _INT),
     "sixbit_get_error": ([_P], _INT),
 }

@@ -343,10 +343,10 @@ int sixbit_debug_stall_gemm(int on) {
   return set_gemm_stall(on ? 1 : 0);
 }
 
-int sixbit_debug_stall_layernorm(int on) {
+int sixbit_debug_stall_staging(int on) {
   int sms;
   if (device_setup(&sms, nullptr) != kOk) return kELaunch;
-  return set_ln_stall(on ? 1 : 0);
+  return set_stage_stall(on ? 1 : 0);
 }
 
 int sixbit_get_error(sixbit_stream_t stream) {

@@ -16,14 +16,14 @@
 
 namespace sixbit {
 
-// Test switch (set through sixbit_debug_stall_layernorm): nonzero makes every
-// warp of the LayerNorm producer's row-prefetch form wait, for its first row,
-// on a barrier that is never signalled, so that bounded wait expires and the
-// device-error path runs.
-__device__ int g_sixbit_stall_ln = 0;
+// Test switch (set through sixbit_debug_stall_staging): nonzero makes every
+// warp of the LayerNorm producer's row-prefetch form, and every CTA of the
+// Gamma passes, wait for its first row or tile on a barrier that is never
+// signalled, so that bounded wait expires and the device-error path runs.
+__device__ int g_sixbit_stall_stage = 0;
 
-int set_ln_stall(int on) {
-  return cudaMemcpyToSymbol(g_sixbit_stall_ln, &on, sizeof(on)) == cudaSuccess ? kOk : kELaunch;
+int set_stage_stall(int on) {
+  return cudaMemcpyToSymbol(g_sixbit_stall_stage, &on, sizeof(on)) == cudaSuccess ? kOk : kELaunch;
 }
 
 namespace {
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_kernel(
     const uint16_t* __restrict__ xin, const uint16_t* __restrict__ xout, int64_t n, uint16_t* delta, float* gamma_out,
     float* r2_out, int32_t* tdc_state, const uint8_t* computed_ptr, GammaWs* ws, double* chains, int* err) {
   __shared__ TileRed red;
-  __shared__ __align__(8) uint64_t sbar[2];
+  __shared__ __align__(8) uint64_t sbar[3];   // two stages + one never signalled (test switch)
   extern __shared__ __align__(128) uint8_t gstage[];   // [2 stages][in | out | Delta_old][kTile bf16]
   const bool computed = computed_ptr ? (*computed_ptr != 0) : true;
   const bool do_delta = computed && delta != nullptr;
@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_kernel(
   if (threadIdx.x == 0) {
     stage_bar_init(bar0);
     stage_bar_init(bar0 + 8u);
+    stage_bar_init(bar0 + 16u);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     if (blockIdx.x < ntiles) issue(blockIdx.x, 0);
   }
@@ -235,7 +236,8 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_kernel(
     const bool more = t + gridDim.x < ntiles;
     // stage s ^ 1 was last read one tile ago, before that tile's closing barrier
     if (threadIdx.x == 0 && more) issue(t + gridDim.x, s ^ 1);
-    const bool landed = stage_bar_wait(bar0 + 8u * uint32_t(s), uint32_t(it >> 1) & 1u);
+    const bool stall = it == 0 && g_sixbit_stall_stage != 0;   // test switch: wait on the silent barrier
+    const bool landed = stage_bar_wait(stall ? bar0 + 16u : bar0 + 8u * uint32_t(s), uint32_t(it >> 1) & 1u);
     if (__syncthreads_or(!landed)) {          // one verdict for the whole CTA
       if (threadIdx.x == 0) {
         if (err) atomicExch(err, int(kErrWaitTimeout));
@@ -321,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_mx_kernel(
     const uint16_t* __restrict__ xin, const uint16_t* __restrict__ xout, int64_t n, uint8_t* cache, float* gamma_out,
     float* r2_out, int32_t* tdc_state, const uint8_t* computed_ptr, GammaWs* ws, double* chains, int* err) {
   __shared__ TileRed red;
-  __shared__ __align__(8) uint64_t sbar[2];
+  __shared__ __align__(8) uint64_t sbar[3];   // two stages + one never signalled (test switch)
   extern __shared__ __align__(128) uint8_t gstage[];   // [2 stages][in | out | codes | scales]
   const bool computed = computed_ptr ? (*computed_ptr != 0) : true;
   const bool do_delta = computed && cache != nullptr;
@@ -348,6 +350,7 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_mx_kernel(
   if (threadIdx.x == 0) {
     stage_bar_init(bar0);
     stage_bar_init(bar0 + 8u);
+    stage_bar_init(bar0 + 16u);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     if (blockIdx.x < ntiles) issue(blockIdx.x, 0);
   }
@@ -359,7 +362,8 @@ __global__ void __launch_bounds__(kThreads, kGammaCtasPerSm) gamma_mx_kernel(
     const int s = it & 1;
     const bool more = t + gridDim.x < ntiles;
     if (threadIdx.x == 0 && more) issue(t + gridDim.x, s ^ 1);   // read one tile ago, before its closing barrier
-    const bool landed = stage_bar_wait(bar0 + 8u * uint32_t(s), uint32_t(it >> 1) & 1u);
+    const bool stall = it == 0 && g_sixbit_stall_stage != 0;   // test switch: wait on the silent barrier
+    const bool landed = stage_bar_wait(stall ? bar0 + 16u : bar0 + 8u * uint32_t(s), uint32_t(it >> 1) & 1u);
     if (__syncthreads_or(!landed)) {          // one verdict for the whole CTA
       if (threadIdx.x == 0) {
         if (err) atomicExch(err, int(kErrWaitTimeout));
@@ -749,7 +753,7 @@ __global__ void __launch_bounds__(kLnThreads<NB>) ln_quant_kernel(const LnQuantC
     if constexpr (PF) {
       const int j = int(k % kLnBufs);
       const uint32_t par = uint32_t(k / kLnBufs) & 1u;
-      const bool stall = k == 0 && g_sixbit_stall_ln != 0;   // test switch: wait on the silent barrier
+      const bool stall = k == 0 && g_sixbit_stall_stage != 0;   // test switch: wait on the silent barrier
       if (!__all_sync(0xffffffffu, ln_bar_wait(stall ? rbar + 8u * kLnBufs : rbar + 8u * j, par))) {
         // Give up: flag it, let the copies still in flight land (bounded), stop.
         if (lane == 0 && a.err) atomicExch(a.err, int(kErrWaitTimeout));

@@ -101,7 +101,7 @@ struct GemmCall {
 int launch_gemm_fp4(const GemmCall& c, int num_sms, cudaStream_t s);
 // Test switch of the GEMM's abort path (see sixbit_debug_stall_gemm).
 int set_gemm_stall(int on);
-// Test switch of the LayerNorm row prefetch's abort path (see sixbit_debug_stall_layernorm).
-int set_ln_stall(int on);
+// Test switch of the staged producers' abort paths (see sixbit_debug_stall_staging).
+int set_stage_stall(int on);
 
 }  // namespace sixbit

@@ -72,7 +72,7 @@ def test_expired_wait_reports_edevice_then_the_next_call_is_clean(residual):
 @pytest.mark.parametrize("quant", [False, True])
 def test_layernorm_expired_row_wait_reports_edevice_then_the_next_call_is_clean(quant):
     """The LayerNorm producer's row-prefetch form (bulk copies into shared
-    memory, one bounded mbarrier wait a row): sixbit_debug_stall_layernorm(1)
+    memory, one bounded mbarrier wait a row): sixbit_debug_stall_staging(1)
     makes each warp wait for its first row on a barrier nothing signals.  The
     wait gives up, the kernel records SIXBIT_EDEVICE after letting its own
     row copies land, and the next normal call on the same stream is clean."""
@@ -90,7 +90,7 @@ def test_layernorm_expired_row_wait_reports_edevice_then_the_next_call_is_clean(
     rs = torch.empty(M, device="cuda")
     run = (lambda: sb.layernorm_quant(xd, int8=(planes, rs))) if quant else (lambda: sb.layernorm(xd, out=y))
     assert lib.sixbit_get_error(stream) == sb.OK
-    assert lib.sixbit_debug_stall_layernorm(1) == sb.OK
+    assert lib.sixbit_debug_stall_staging(1) == sb.OK
     try:
         t0 = time.perf_counter()
         run()                                              # the launch itself succeeds
@@ -101,7 +101,7 @@ def test_layernorm_expired_row_wait_reports_edevice_then_the_next_call_is_clean(
         print(f"expired row wait reported after {dt:.2f} s")
         assert lib.sixbit_get_error(stream) == sb.OK
     finally:
-        assert lib.sixbit_debug_stall_layernorm(0) == sb.OK
+        assert lib.sixbit_debug_stall_staging(0) == sb.OK
     run()
     assert lib.sixbit_get_error(stream) == sb.OK
     ref = codecs.bf16_to_f32(o_block.layernorm(x)).astype(np.float64)
@@ -112,3 +112,52 @@ def test_layernorm_expired_row_wait_reports_edevice_then_the_next_call_is_clean(
     else:
         got = codecs.bf16_to_f32(host_bf16_bits(y)).astype(np.float64)
         assert np.all(np.abs(got - ref) <= 2.0 ** -7 * np.abs(ref) + 1e-6)
+
+
+@pytest.mark.parametrize("mx", [False, True])
+def test_gamma_expired_stage_wait_reports_edevice_then_the_next_call_is_clean(mx):
+    """The Gamma passes stage their tiles through shared memory by bulk copies,
+    one bounded mbarrier wait a tile.  With sixbit_debug_stall_staging(1)
+    every CTA waits for its first tile on a barrier nothing signals: the wait
+    gives up, the kernel records SIXBIT_EDEVICE after its own copies land and
+    still completes its CTA count, so the next call on the same scratch and
+    stream is clean and bit-exact."""
+    import nvfp4_int8_mixed_gb300 as sb
+    from oracle import gamma as o_gamma, mxcache
+    lib = sb.lib()
+    stream = sb._stream()
+    M, H = 300, 1920                                       # 71 tiles of 8192 elements, the last one partial
+    p = synthetic.gamma_pair(77, M, H)
+    xin, xout = dev_bf16(p["xin"]), dev_bf16(p["xout"])
+    ws = sb.workspace(int(lib.sixbit_workspace_size(M * H, 1)))
+    if mx:
+        codes, sc = mxcache.encode(codecs.bf16_to_f32(p["delta_prev"]))
+        prev_bytes, prev_val = mxcache.to_bytes(codes, sc), mxcache.decode(codes, sc)
+        fresh = lambda: dev(prev_bytes.copy())
+    else:
+        fresh = lambda: dev_bf16(p["delta_prev"])
+    state = torch.tensor([1, 0], dtype=torch.int32, device="cuda")
+    assert lib.sixbit_get_error(stream) == sb.OK
+    assert lib.sixbit_debug_stall_staging(1) == sb.OK
+    try:
+        t0 = time.perf_counter()
+        sb.block_gamma(xin, xout, delta=fresh(), tdc_state=state.clone(), ws=ws)
+        rc = lib.sixbit_get_error(stream)
+        dt = time.perf_counter() - t0
+        assert rc == sb.EDEVICE, rc
+        assert dt < 60.0, dt
+        print(f"expired stage wait reported after {dt:.2f} s")
+        assert lib.sixbit_get_error(stream) == sb.OK
+    finally:
+        assert lib.sixbit_debug_stall_staging(0) == sb.OK
+    d = fresh()
+    g, r2 = sb.block_gamma(xin, xout, delta=d, tdc_state=state, ws=ws)
+    assert lib.sixbit_get_error(stream) == sb.OK
+    rdn = o_gamma.delta(p["xin"], p["xout"])
+    assert host(g)[0] == o_gamma.gamma(p["xin"], p["xout"])
+    if mx:
+        assert host(r2)[0] == o_gamma.rel_l2_sq(rdn, prev_val)
+    else:
+        assert host(r2)[0] == o_gamma.rel_l2_sq(rdn, p["delta_prev"])
+        assert np.array_equal(host_bf16_bits(d), rdn)
+    assert host(state).tolist() == [2, 0]

@@ -17,8 +17,8 @@ def _sb():
     return sb
 
 
-@pytest.mark.parametrize("M,H", [(256, 256), (1, 8), (3, 5000), (7, 333), (3, 8191), (17, 1920),
-                                 (synthetic.M_2B, 1920)])
+@pytest.mark.parametrize("M,H", [(256, 256), (1, 8), (1, 5), (2, 3), (3, 5000), (7, 333), (3, 8191), (17, 1920),
+                                 (synthetic.M_2B, 1920)])          # n < 8: no whole group, an empty tile stage
 def test_gamma_delta_r2(M, H):
     sb = _sb()
     p = synthetic.gamma_pair(M * 7 + H, M, H)

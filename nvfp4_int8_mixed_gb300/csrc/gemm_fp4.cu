@@ -998,15 +998,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host
+// Host-side lookups below are function-local statics: C++ initializes them
+// once, and host threads calling the library at the same time wait for it.
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     cudaDriverEntryPointQueryResult q;
     void* f = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    return PFN_cuTensorMapEncodeTiled_v12000(nullptr);
+  }();
   return fn;
 }
 
@@ -1103,17 +1105,15 @@ int run(const GemmCall& c, int num_sms, cudaStream_t s) {
   p.q_pred = c.q_pred;
 
   auto kern = gemm_fp4_kernel<BN, MODE, STAGES, KB, NC, PAIR, QO>;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static const bool attr_ok = [&] {
     // The register split (setmaxnreg) assumes exactly kLaunchRegs per thread
     // at launch; any other allocation would leave the epilogue's request
     // unsatisfiable, so such a build is refused here.
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs != kLaunchRegs) return kELaunch;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cf::kSmem)) != cudaSuccess)
-      return kELaunch;
-    attr_set = true;
-  }
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs != kLaunchRegs) return false;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cf::kSmem)) == cudaSuccess;
+  }();
+  if (!attr_ok) return kELaunch;
   const int tiles = p.MT * p.NT;
   constexpr int kCtas = PAIR ? 2 : 1;
   cudaLaunchConfig_t cfg = {};
@@ -1128,13 +1128,12 @@ int run(const GemmCall& c, int num_sms, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // persistent grid: as many CTA pairs (or CTAs) as can be resident at once
-  static int resident = 0;
-  if (resident == 0) {
+  static const int resident = [&] {
     cfg.gridDim = dim3(kCtas * (num_sms / kCtas));
     int n = 0;
-    if (PAIR && cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) resident = n;
-    else resident = num_sms / kCtas;
-  }
+    if (PAIR && cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) return n;
+    return num_sms / kCtas;
+  }();
   const int units = tiles < resident ? tiles : resident;
   cfg.gridDim = dim3(kCtas * units);
   if (cudaLaunchKernelEx(&cfg, kern, tA, tB, tSA, tSB, tY, tR, p) != cudaSuccess) return kELaunch;

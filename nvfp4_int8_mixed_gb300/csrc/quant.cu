@@ -404,14 +404,15 @@ int launch_nvfp4_quant(const void* x, int dtype, int64_t M, int64_t K, int64_t l
                        uint8_t* codes, uint8_t* sf, float* g_out, const uint8_t* pred, int num_sms, cudaStream_t s) {
   const int64_t Mpad = cdiv(M, 128) * 128;
   const int64_t items = Mpad * cdiv(cdiv(K / 16, 32), 2);
-  // persistent: as many CTAs as are resident (each warp walks many items)
-  static int per_sm[2] = {0, 0};
-  int& ps = per_sm[dtype == 1 ? 0 : 1];
-  if (ps == 0) {
-    const bool ok = dtype == 1 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, nvfp4_quant_kernel<uint16_t>, kThreads, 0) == cudaSuccess
-                               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, nvfp4_quant_kernel<float>, kThreads, 0) == cudaSuccess;
-    if (!ok || ps < 1) ps = 1;
-  }
+  // persistent: as many CTAs as are resident (each warp walks many items);
+  // the residency is looked up once per input type (thread-safe statics)
+  auto resident = [](const void* kern) {
+    int n = 0;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, 0) == cudaSuccess && n > 0 ? n : 1;
+  };
+  static const int ps_bf16 = resident(reinterpret_cast<const void*>(nvfp4_quant_kernel<uint16_t>));
+  static const int ps_f32 = resident(reinterpret_cast<const void*>(nvfp4_quant_kernel<float>));
+  const int ps = dtype == 1 ? ps_bf16 : ps_f32;
   const int grid = grid_for(items, kThreads / 32, num_sms, ps);
   if (dtype == 1)
     nvfp4_quant_kernel<uint16_t><<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), M, K, ldx, amax, codes, sf,

@@ -173,7 +173,9 @@ int sixbit_qlinear_w4a8(const uint8_t* a_planes, const float* row_scale, int64_t
  * (tile k to chain k % 256, in order) and the chain sums are halved;
  * Gamma = f32(S1/S0), r2 = f32(Sd/So).  The result depends only on the
  * input, never on the GPU.  ws: sixbit_workspace_size(n, 1) bytes (a
- * 256-byte header and 4 doubles a chain: 8448 bytes whatever n). */
+ * 256-byte header and 4 doubles a chain: 8448 bytes whatever n).  Tiles
+ * are staged through shared memory by bulk copies; a bounded wait for one
+ * that gives up sets the device error word (sixbit_get_error). */
 int sixbit_block_gamma(const void* in, const void* out, int64_t n, void* delta,
                        float* gamma_out, float* r2_out, int32_t* tdc_state,
                        const uint8_t* computed, void* ws, sixbit_stream_t stream);

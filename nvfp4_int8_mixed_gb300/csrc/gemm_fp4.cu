@@ -502,6 +502,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int ntiles = p.MT * p.NT;
+  // W4A8 with a half-width last column (N % 256 == 128, e.g. N = 1920): a
+  // tile of that column runs as N = 128 MMAs, half the MMA work of a full
+  // tile, and its W rows split 64 / 64 between the pair.  The tiles that
+  // would make up the last, partial round of the pairs' round-robin are
+  // half tiles (those of the last rows), so that round takes half as long;
+  // every other tile keeps its place in row order.
+  const bool half_col = MODE == 1 && PAIR && p.N % BN == BN / 2;
+  const int units = int(gridDim.x) / kCtas;
+  const int late_n = ntiles % units;
+  const int late = half_col && p.NT > 1 && late_n <= p.MT ? late_n : 0;
+  auto tile_at = [&](int tile, int& mt, int& nt) {
+    mt = tile / p.NT;
+    nt = tile - mt * p.NT;
+    if (late > 0) {
+      const int first_late = ntiles - late, row0 = p.MT - late;
+      if (tile >= first_late) {
+        mt = row0 + (tile - first_late);
+        nt = p.NT - 1;
+      } else if (tile >= row0 * p.NT) {       // the last rows without their half tiles
+        const int j = tile - row0 * p.NT;
+        mt = row0 + j / (p.NT - 1);
+        nt = j - (j / (p.NT - 1)) * (p.NT - 1);
+      }
+    }
+  };
+  auto half_tile = [&](int nt) { return half_col && nt == p.NT - 1; };
 
   auto fail = [&]() {
     *abort_flag = 1;
@@ -516,7 +542,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kPredIssue = MODE == 1;
   const bool issue_lane = lane == 0;
   auto mma_issuer = [&]() {
-    constexpr uint32_t idesc = idesc_fp4(C::kTileM, BN);
+    constexpr uint32_t idesc_full = idesc_fp4(C::kTileM, BN);
+    constexpr uint32_t idesc_half = idesc_fp4(C::kTileM, BN / 2);
     // Descriptors of stage 0; stage s adds s * kStage bytes (>> 4) to the start address field.
     const uint64_t adesc_s0 = desc_kmajor<KB>(smem_u32(smem));
     const uint64_t bdesc_s0 = desc_kmajor<KB>(smem_u32(smem + C::offB));
@@ -529,6 +556,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait<PAIR>(never_bar, 0, abort_flag)) { fail(); ok = false; }
     }
     for (int tile = blockIdx.x / kCtas; tile < ntiles && ok; tile += gridDim.x / kCtas) {
+      int mt_, nt_;
+      tile_at(tile, mt_, nt_);
+      const uint32_t idesc = half_tile(nt_) ? idesc_half : idesc_full;
       // the epilogue warps (of both CTAs) have pulled the previous tile out of TMEM
       if (!mbar_wait<PAIR>(tempty_bar, acc_phase ^ 1u, abort_flag)) { fail(); ok = false; break; }
       tc_fence_after();
@@ -625,9 +655,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
       for (int tile = blockIdx.x / kCtas; tile < ntiles && ok; tile += gridDim.x / kCtas) {
-        const int mt = tile / p.NT, nt = tile - mt * p.NT;
+        int mt, nt;
+        tile_at(tile, mt, nt);
         const int arow = mt * C::kTileM + int(rank) * BM;          // this CTA's A rows
-        const int brow = nt * BN + int(rank) * C::kBRows;          // this CTA's W rows
+        const int brow = nt * BN + int(rank) * (half_tile(nt) ? C::kBRows / 2 : C::kBRows);   // this CTA's W rows
         for (int kt = 0; kt < p.KT; ++kt) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { fail(); ok = false; break; }
           uint8_t* sb = smem + size_t(stage) * C::kStage;
@@ -769,7 +800,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     uint32_t q_run = 0;                          // |y| max as two bf16 halves
     for (int tile = blockIdx.x / kCtas; tile < ntiles && ok; tile += gridDim.x / kCtas) {
-      const int mt = tile / p.NT, nt = tile - mt * p.NT;
+      int mt, nt;
+      tile_at(tile, mt, nt);
       if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar, acc_phase, abort_flag))) {   // warp-uniform verdict
         if (lane == 0) fail();
         break;

@@ -50,7 +50,10 @@ enum {
 
 /* Calls over M rows (amax, the activation quantizers, the linear layers, the
  * LayerNorms) return SIXBIT_OK at once when M == 0, before any check: no
- * pointer is used, so an empty tensor's NULL data pointer is accepted. */
+ * pointer is used, so an empty tensor's NULL data pointer is accepted.
+ * Calls over n elements (the Gamma passes, the pair sums, the TDC calls)
+ * need n >= 1 and return SIXBIT_EINVAL for n <= 0: a block's update is
+ * never empty, and an empty one has no defined Gamma. */
 enum { SIXBIT_F32 = 0, SIXBIT_BF16 = 1 };          /* dtype / out_dtype */
 enum { SIXBIT_EPI_GELU = 1 };                       /* epilogue flag bits */
 enum { SIXBIT_QOUT_W4A4 = 0, SIXBIT_QOUT_W4A8 = 1 };  /* sixbit_qlinear_qout mode */

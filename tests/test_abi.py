@@ -164,3 +164,29 @@ def test_quantizing_producer_argument_errors(lib):
     assert lib.sixbit_qlinear_qout(0, fake, fake, fake, None, 128, 256, fake, fake, fake, 128, None, 0, fake, 128,
                                    fake, None, fake, fake, f(2.0), None, None, None) == sb.EINVAL
     assert qo(hist=P((1 << 20) + 8)) == sb.EALIGN
+
+
+def test_empty_row_count_is_a_no_op(lib):
+    """Calls over M rows return SIXBIT_OK for M == 0 before any check or
+    device call: an empty tensor's NULL data pointer is accepted, so these
+    run on a machine without a GPU."""
+    import nvfp4_int8_mixed_gb300 as sb
+    f = ctypes.c_float
+    assert lib.sixbit_amax_bf16(None, 0, 64, 64, None, None, None) == sb.OK
+    assert lib.sixbit_quantize_act_nvfp4(None, 0, 64, 64, None, None, None, None, None, None, None) == sb.OK
+    assert lib.sixbit_quantize_act_int8(None, 0, 64, 64, None, None, None, None, None, None) == sb.OK
+    assert lib.sixbit_int8_digit_planes(None, 0, 64, 64, None, None) == sb.OK
+    assert lib.sixbit_qlinear_w4a4(None, None, None, 0, 256, None, None, None, 128, None, None, 0, 0, sb.BF16, None,
+                                   128, None, None) == sb.OK
+    assert lib.sixbit_qlinear_w4a8(None, None, 0, 256, None, None, None, 128, None, None, 0, 0, sb.BF16, None, 128,
+                                   None, None) == sb.OK
+    assert lib.sixbit_qlinear_qout(0, None, None, None, None, 0, 256, None, None, None, 128, None, 0, None, 128, None,
+                                   None, None, None, f(2.0), None, None, None) == sb.OK
+    assert lib.sixbit_layernorm_bf16(None, 0, 128, 128, f(1e-5), None, 128, None, None, None, None) == sb.OK
+    assert lib.sixbit_layernorm_quant(None, 0, 128, 128, f(1e-5), None, 128, None, None, None, None, f(2.0), None,
+                                      None, None, None, None, None) == sb.OK
+    # a negative row count is still an error
+    assert lib.sixbit_amax_bf16(None, -1, 64, 64, None, None, None) == sb.EINVAL
+    # the element-count calls have no empty form: n = 0 is rejected
+    assert lib.sixbit_block_gamma(None, None, 0, None, None, None, None, None, None, None) == sb.EINVAL
+    assert lib.sixbit_pair_stats(None, 0, None, 0, 0, None, None, None) == sb.EINVAL

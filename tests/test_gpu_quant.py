@@ -161,3 +161,22 @@ def test_int8_digit_planes_of_plain_codes(M, K, ldq):
     y = sb.qlinear_w4a8(planes, dev(s), wc, wsf, gw, out_dtype=torch.float32)
     rwc, rwsf, rgw, _ = o_nvfp4.quantize(w)
     assert_gemm_close(host(y), o_gemm.w4a8(q, s, rwc, rwsf, rgw), "f32")
+
+
+def test_empty_row_count_through_the_binding():
+    """M = 0 activations (an empty token batch) pass through every row call
+    of the binding as no-ops with empty results, and leave the stream clean."""
+    sb = _sb()
+    x = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
+    ta, ra = sb.amax(x, tensor=True, rows=True)
+    assert ra.shape == (0,)
+    codes, sf, g = sb.quantize_act_nvfp4(x)
+    assert codes.shape == (0, 64) and sf.numel() == 0
+    q, planes, s = sb.quantize_act_int8(x)
+    assert q.shape == (0, 128) and planes.shape == (3, 0, 64) and s.shape == (0,)
+    w = synthetic.rng(5).standard_normal((64, 128)).astype(np.float32) * 0.02
+    wc, wsf, gw = sb.quantize_weight_nvfp4(dev(w))
+    assert sb.qlinear_w4a4(codes, sf, g, wc, wsf, gw).shape == (0, 64)
+    assert sb.qlinear_w4a8(planes, s, wc, wsf, gw, out_dtype=torch.float32).shape == (0, 64)
+    assert sb.layernorm(x).shape == (0, 128)
+    sb.get_error()

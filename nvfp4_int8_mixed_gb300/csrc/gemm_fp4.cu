@@ -414,6 +414,76 @@ struct Params {
   const uint8_t* q_pred;
 };
 
+// Which output tile each CTA pair (or CTA) computes.  The U pairs walk the
+// tiles round-robin: pair u takes indices u, u + U, u + 2U, ..., index
+// i = jU + u being its tile of round j, and the order of the indices is row
+// order (row tile mt, then column tile nt), so the tiles of one round share
+// their A rows and W columns in L2.
+// With a half-width last column (`half`: W4A8 whose N % 256 == 128, run as
+// N = 128 MMAs at half the MMA time), the round-robin alone gives the half
+// tiles to a few pairs and leaves the last round's tiles to the first
+// ntiles % U pairs at full cost.  Where the counts allow it (`bal`), each
+// round still covers the same tiles, but within the round they go to the
+// pairs so that the e = ntiles % U pairs with one tile more than the others
+// take two half tiles, the next D - e pairs one (D = MT - e), and the rest
+// none: every pair then has at most R = ntiles / U tiles' worth of MMAs
+// instead of R + 1/2.  Half tile k (row k) goes to pair k, or to k - D for
+// k >= D; the full tiles of a round go, in row order, to the pairs without
+// a half tile in it.  D * NT >= U keeps a pair's two half tiles in
+// different rounds.  Otherwise the half tiles of the last rows fill the
+// last, partial round (`late`), and every other tile keeps its row-order
+// place.
+struct TileOrder {
+  int MT, NT, U, ntiles, e, D, late;
+  bool half, bal;
+};
+
+__host__ __device__ inline TileOrder make_tile_order(int MT, int NT, int U, bool half_col) {
+  TileOrder o;
+  o.MT = MT;
+  o.NT = NT;
+  o.U = U;
+  o.ntiles = MT * NT;
+  o.e = o.ntiles % U;
+  o.D = MT - o.e;
+  o.half = half_col && NT > 1;
+  o.bal = o.half && MT >= 2 * o.e && o.D <= U && int64_t(o.D) * NT >= U;
+  o.late = o.half && !o.bal && o.e <= MT ? o.e : 0;
+  return o;
+}
+
+__host__ __device__ inline void tile_of(const TileOrder& o, int i, int& mt, int& nt) {
+  if (o.bal) {
+    const int j = i / o.U, u = i - j * o.U;
+    const int lo = j * o.U, hi = lo + o.U < o.ntiles ? lo + o.U : o.ntiles;
+    const int k_lo = lo / o.NT, k_hi = hi / o.NT;            // half tiles k with k NT + NT - 1 in [lo, hi)
+    const int k1 = u < o.D ? u : -1, k2 = u < o.e ? u + o.D : -1;
+    if (k1 >= k_lo && k1 < k_hi) { mt = k1; nt = o.NT - 1; return; }
+    if (k2 >= k_lo && k2 < k_hi) { mt = k2; nt = o.NT - 1; return; }
+    // pairs below u that take a half tile of this round
+    const int a0 = k_lo, a1 = k_hi < (u < o.D ? u : o.D) ? k_hi : (u < o.D ? u : o.D);
+    const int b0 = k_lo > o.D ? k_lo : o.D, b1 = k_hi < o.D + (u < o.e ? u : o.e) ? k_hi : o.D + (u < o.e ? u : o.e);
+    const int below = (a1 > a0 ? a1 - a0 : 0) + (b1 > b0 ? b1 - b0 : 0);
+    const int f = (lo - k_lo) + (u - below);                // full tile index, row order
+    mt = f / (o.NT - 1);
+    nt = f - mt * (o.NT - 1);
+    return;
+  }
+  mt = i / o.NT;
+  nt = i - mt * o.NT;
+  if (o.late > 0) {
+    const int first_late = o.ntiles - o.late, row0 = o.MT - o.late;
+    if (i >= first_late) {
+      mt = row0 + (i - first_late);
+      nt = o.NT - 1;
+    } else if (i >= row0 * o.NT) {             // the last rows without their half tiles
+      const int j = i - row0 * o.NT;
+      mt = row0 + j / (o.NT - 1);
+      nt = j - (j / (o.NT - 1)) * (o.NT - 1);
+    }
+  }
+}
+
 template <int BN, int MODE, int STAGES, int KB, int NC, bool PAIR, bool QO>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -504,27 +574,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = p.MT * p.NT;
   // W4A8 with a half-width last column (N % 256 == 128, e.g. N = 1920): a
   // tile of that column runs as N = 128 MMAs, half the MMA work of a full
-  // tile, and its W rows split 64 / 64 between the pair.  The tiles that
-  // would make up the last, partial round of the pairs' round-robin are
-  // half tiles (those of the last rows), so that round takes half as long;
-  // every other tile keeps its place in row order.
+  // tile, and its W rows split 64 / 64 between the pair; make_tile_order
+  // spreads those tiles over the pairs.
   const bool half_col = MODE == 1 && PAIR && p.N % BN == BN / 2;
-  const int units = int(gridDim.x) / kCtas;
-  const int late_n = ntiles % units;
-  const int late = half_col && p.NT > 1 && late_n <= p.MT ? late_n : 0;
+  const TileOrder order = make_tile_order(p.MT, p.NT, int(gridDim.x) / kCtas, half_col);
   auto tile_at = [&](int tile, int& mt, int& nt) {
-    mt = tile / p.NT;
-    nt = tile - mt * p.NT;
-    if (late > 0) {
-      const int first_late = ntiles - late, row0 = p.MT - late;
-      if (tile >= first_late) {
-        mt = row0 + (tile - first_late);
-        nt = p.NT - 1;
-      } else if (tile >= row0 * p.NT) {       // the last rows without their half tiles
-        const int j = tile - row0 * p.NT;
-        mt = row0 + j / (p.NT - 1);
-        nt = j - (j / (p.NT - 1)) * (p.NT - 1);
-      }
+    if constexpr (MODE == 1 && PAIR) {
+      tile_of(order, tile, mt, nt);
+    } else {                                   // W4A4: plain row order
+      mt = tile / p.NT;
+      nt = tile - mt * p.NT;
     }
   };
   auto half_tile = [&](int nt) { return half_col && nt == p.NT - 1; };

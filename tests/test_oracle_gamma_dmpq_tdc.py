@@ -204,6 +204,16 @@ def test_tdc_never_skips_with_zero_threshold_or_zero_max_skip():
     assert tdc.decide(c, 1.0, 1)
 
 
+def test_tdc_needs_two_computed_updates():
+    # r2 compares the updates of two computed steps, so a block with only one
+    # computed update is never skipped, even when the caller's r2 is below
+    # the threshold (a state the device contract accepts as input)
+    one = tdc.BlockCache(fresh_count=1, consec=0, r2=np.float32(0.0), delta=None)
+    two = tdc.BlockCache(fresh_count=2, consec=0, r2=np.float32(0.0), delta=None)
+    assert not tdc.decide(one, 0.05, 1)
+    assert tdc.decide(two, 0.05, 1)
+
+
 def test_tdc_apply_identity():
     rng = np.random.default_rng(4)
     xin = _bits(rng.standard_normal((6, 40)))

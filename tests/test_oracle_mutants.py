@@ -270,6 +270,29 @@ def tdc_apply_subtracts(mp):
     _replace(mp, tdc.apply, apply)
 
 
+# ------------------------------------------------------------------ block and stack
+def qlinear_ignores_flag_int8(mp):
+    real = block.qlinear
+
+    def ql(h_bits, wq, use_nvfp4, **kw):
+        return real(h_bits, wq, False, **kw)
+    _replace(mp, real, ql)
+
+
+def qlinear_ignores_flag_nvfp4(mp):
+    real = block.qlinear
+
+    def ql(h_bits, wq, use_nvfp4, **kw):
+        return real(h_bits, wq, True, **kw)
+    _replace(mp, real, ql)
+
+
+def dmpq_never_picks_nvfp4(mp):
+    def assign(gamma_blocks, alpha, beta, layer_block, tau, step):
+        return np.zeros(len(alpha), dtype=np.uint8)
+    _replace(mp, dmpq.assign, assign)
+
+
 # ------------------------------------------------------------------ compressed cache / calibration
 def mx_scale_exponent_one_low(mp):
     real = mxcache.scale_exponent
@@ -348,6 +371,10 @@ MUTANTS = [
     (tdc_one_fresh_step_suffices, ("gamma_dmpq_tdc.test_tdc_state_machine_hand_sequence",
                                    "gamma_dmpq_tdc.test_tdc_needs_two_computed_updates")),
     (tdc_apply_subtracts, ("gamma_dmpq_tdc.test_tdc_apply_identity",)),
+    (qlinear_ignores_flag_int8, ("block.test_block_on_a_row_subset_with_the_full_tensor_amaxes",
+                                 "delayed.test_block_converges_to_dynamic_at_fixed_input")),
+    (qlinear_ignores_flag_nvfp4, ("delayed.test_int8_layers_are_unchanged_by_fusion",)),
+    (dmpq_never_picks_nvfp4, ("block.test_stack_flags_follow_gamma_and_uniform_extremes",)),
     (mx_scale_exponent_one_low, ("mxcache.test_grid_values_round_trip", "mxcache.test_scale_boundary_and_powers_of_two")),
     (mx_layout_scales_first, ("mxcache.test_layout_codes_then_scales",)),
     (r_squared_complement, ("calib.test_fit_line_recovers_exact_lines", "calib.test_fit_line_hand_example")),

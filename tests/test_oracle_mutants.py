@@ -213,6 +213,58 @@ def tree_sum_drops_ragged_tail(mp):
     _replace(mp, real, ts)
 
 
+def _tree_sum_variant(warp_serial=False, contiguous_lanes=False):
+    """The oracle's reduction tree with one step reordered."""
+    T, L, V = gamma.TILE, gamma.LANES, gamma.VEC
+
+    def ts(terms):
+        t = np.asarray(terms, dtype=F32).ravel()
+        ntiles = max(1, -(-t.size // T))
+        p = np.zeros(ntiles * T, dtype=F32)
+        p[:t.size] = t
+        if contiguous_lanes:                   # lane k adds elements 32k .. 32k + 31 of the tile
+            x = p.reshape(ntiles, L, T // L).transpose(0, 2, 1)
+        else:                                  # lane k adds elements j*2048 + 8k + e
+            x = p.reshape(ntiles, T // (L * V), L, V).transpose(0, 1, 3, 2).reshape(ntiles, T // L, L)
+        lane = np.zeros((ntiles, L), dtype=F32)
+        for i in range(x.shape[1]):
+            lane = (lane + x[:, i, :]).astype(F32)
+        g = lane.reshape(ntiles, L // 32, 32)
+        if warp_serial:                        # the 32 lanes added one after another
+            acc32 = g[:, :, 0].copy()
+            for k in range(1, 32):
+                acc32 = (acc32 + g[:, :, k]).astype(F32)
+            g[:, :, 0] = acc32
+        else:
+            idx = np.arange(32)
+            for h in (16, 8, 4, 2, 1):
+                g = (g + g[:, :, idx ^ h]).astype(F32)
+        w = g[:, :, 0].copy()
+        for h in (4, 2, 1):
+            w[:, :h] = (w[:, :h] + w[:, h:2 * h]).astype(F32)
+        tiles = w[:, 0].astype(np.float64)
+        nb = -(-ntiles // L)
+        tp = np.zeros(nb * L)
+        tp[:ntiles] = tiles
+        acc = np.zeros(L)
+        for b in range(nb):                    # lane k adds tiles k, k + 256, ... in order
+            acc = acc + tp[b * L:(b + 1) * L]
+        h = L // 2
+        while h >= 1:
+            acc[:h] = acc[:h] + acc[h:2 * h]
+            h //= 2
+        return np.float64(acc[0])
+    return ts
+
+
+def tree_warp_serial(mp):
+    _replace(mp, gamma.tree_sum, _tree_sum_variant(warp_serial=True))
+
+
+def tree_contiguous_lanes(mp):
+    _replace(mp, gamma.tree_sum, _tree_sum_variant(contiguous_lanes=True))
+
+
 def r2_denominator_not_squared(mp):
     def r2(delta_new, delta_prev):
         dn, dp = gamma._f32(delta_new), gamma._f32(delta_prev)
@@ -360,6 +412,8 @@ MUTANTS = [
     (gamma_over_output_norm, ("gamma_dmpq_tdc.test_gamma_closed_forms",)),
     (tree_sum_drops_ragged_tail, ("gamma_dmpq_tdc.test_tree_sum_matches_a_scalar_walk_of_the_tree",
                                   "gamma_dmpq_tdc.test_tree_sum_closed_forms_and_bound")),
+    (tree_warp_serial, ("gamma_dmpq_tdc.test_tree_sum_matches_a_scalar_walk_of_the_tree",)),
+    (tree_contiguous_lanes, ("gamma_dmpq_tdc.test_tree_sum_matches_a_scalar_walk_of_the_tree",)),
     (r2_denominator_not_squared, ("gamma_dmpq_tdc.test_delta_and_r2_closed_forms",)),
     (dmpq_tie_goes_to_nvfp4, ("gamma_dmpq_tdc.test_dmpq_tie_goes_to_int8_and_layer_block_map",)),
     (dmpq_step0_not_forced, ("gamma_dmpq_tdc.test_dmpq_extremes_reproduce_uniform_policies",
